@@ -1,0 +1,407 @@
+// ORACLE — test infrastructure, not product code.
+//
+// A plain, slow CPU definition of the per-token Mixture-of-Experts layer with
+// block-quantized experts: q8_K activation quantization, router top-k
+// (softmax or sigmoid, renormalised over the selected k), token -> expert
+// bucketing, per-expert gate/up integer sub-block dot products, SwiGLU, the
+// down projection, and the gate-weighted combine into the residual.
+//
+// It shares no code with the CUDA path and is only built and called by the
+// tests, by __graft_entry__.smoke() and by bench.py's CPU baseline.
+// Floating point is fp64 except where a step is defined in fp32 (the q8_K
+// quantizer).  Integer sub-block sums are int64.  Parallelism is over rows
+// or tokens only; every row is computed by one thread in a fixed order.
+//
+// Sources of the method (page title, section):
+//  * Pulsar README, "Fidelity notes": every matmul runs on activations
+//    quantized to q8_0/q8_K with integer dp4a dot products.
+//  * Pulsar README, "What it does today" (ThinkingCap paragraph):
+//    warp-cooperative Q4_K/Q6_K matmuls on q8_K activations; the FFN triple
+//    gate/up/down.  Same section: softmax routers (qwen3moe).
+//  * Pulsar digest note (rrlab.tech), section 1: a 512-way sigmoid-gated
+//    router plus a shared expert with Q2_K experts.
+//  * Pulsar README, "How the streaming works": per token, or per prefill
+//    chunk as a union across the batch, each selected expert is resolved
+//    once; kernels receive explicit per-(token, slot) gate/up/down pointers
+//    and a NULL slot means "not mine".
+//  * Pulsar README, "Fidelity notes": the per-slot sum is the combine.
+//  * Strata summary (bafh001.com): router and shared expert, ~10 experts per
+//    token.
+// The pages name the formats but print no field layout or formula; the
+// super-block fields (fp16 d, fp16 dmin, per-sub-block scale and min, codes;
+// w = d*scale*q - dmin*min), the q8_K rule (d = max|x|/127 in fp32,
+// q = round-half-away(x/d)) and the byte placement (synth/layout.py) are the
+// workload definitions this oracle follows.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int kQ4K = 0;
+constexpr int kQ2K = 1;
+
+int n_sub(int fmt) { return fmt == kQ4K ? 8 : 16; }
+int sub_len(int fmt) { return fmt == kQ4K ? 32 : 16; }
+int64_t slab_bytes(int fmt) { return fmt == kQ4K ? 4608 : 2688; }
+
+// IEEE 754 binary16 -> double, written out from the format definition.
+double half_to_double(uint16_t h) {
+  int sign = h >> 15;
+  int e = (h >> 10) & 31;
+  int m = h & 1023;
+  double v;
+  if (e == 0)
+    v = std::ldexp((double)m, -24);  // subnormal: m * 2^-24
+  else if (e == 31)
+    v = m ? NAN : INFINITY;
+  else
+    v = std::ldexp((double)(m + 1024), e - 25);  // (1 + m/1024) * 2^(e-15)
+  return sign ? -v : v;
+}
+
+uint32_t read_le32(const uint8_t* p) {
+  return (uint32_t)p[0] | ((uint32_t)p[1] << 8) | ((uint32_t)p[2] << 16) | ((uint32_t)p[3] << 24);
+}
+
+// bits [start, start+len) of a little-endian bit string
+int read_bits(const uint8_t* p, int start, int len) {
+  int v = 0;
+  for (int i = 0; i < len; ++i) {
+    int bit = start + i;
+    v |= ((p[bit / 8] >> (bit % 8)) & 1) << i;
+  }
+  return v;
+}
+
+struct SuperBlock {
+  int q[256];   // codes
+  int sc[16];   // per-sub-block scale
+  int mn[16];   // per-sub-block min
+  double d, dmin;
+};
+
+// Unpack super-block b of row n of a matrix with nb super-blocks per row.
+void unpack_sb(const uint8_t* w, int fmt, int64_t nb, int64_t n, int64_t b, SuperBlock* o) {
+  int64_t rg = n / 32;
+  int r = (int)(n % 32);
+  const uint8_t* slab = w + (rg * nb + b) * slab_bytes(fmt);
+  uint32_t dm = read_le32(slab + 4 * r);
+  o->d = half_to_double((uint16_t)(dm & 0xFFFF));
+  o->dmin = half_to_double((uint16_t)(dm >> 16));
+  if (fmt == kQ4K) {
+    const uint8_t* sm = slab + 128 + 12 * r;
+    for (int j = 0; j < 8; ++j) {
+      o->sc[j] = read_bits(sm, 6 * j, 6);
+      o->mn[j] = read_bits(sm, 48 + 6 * j, 6);
+    }
+    for (int j = 0; j < 8; ++j) {
+      const uint8_t* line = slab + 512 + 512 * j + 16 * r;
+      for (int i = 0; i < 16; ++i) {
+        o->q[32 * j + i] = line[i] & 15;
+        o->q[32 * j + 16 + i] = line[i] >> 4;
+      }
+    }
+  } else {
+    const uint8_t* sm = slab + 128 + 16 * r;
+    for (int j = 0; j < 16; ++j) {
+      o->sc[j] = sm[j] & 15;
+      o->mn[j] = sm[j] >> 4;
+    }
+    for (int j = 0; j < 16; ++j) {
+      const uint8_t* base = slab + 640 + 512 * (j / 4) + 16 * r + 4 * (j % 4);
+      for (int c = 0; c < 16; ++c) o->q[16 * j + c] = (base[c % 4] >> (2 * (c / 4))) & 3;
+    }
+  }
+}
+
+// Run f(i) for i in [0, n) on up to nthreads threads (contiguous ranges).
+template <class F>
+void parallel_for(int64_t n, int nthreads, F f) {
+  if (nthreads <= 1 || n <= 1) {
+    for (int64_t i = 0; i < n; ++i) f(i);
+    return;
+  }
+  int nt = (int)std::min<int64_t>(nthreads, n);
+  std::vector<std::thread> th;
+  for (int t = 0; t < nt; ++t) {
+    int64_t lo = n * t / nt, hi = n * (t + 1) / nt;
+    th.emplace_back([=, &f] {
+      for (int64_t i = lo; i < hi; ++i) f(i);
+    });
+  }
+  for (auto& x : th) x.join();
+}
+
+// q8_K quantization of one 256-element block, in fp32 as the format defines:
+// d = max|x| / 127 (one IEEE fp32 division), q = round-half-away(x / d)
+// (IEEE fp32 division, then rounding; |q| <= 127), q = 0 when d == 0.
+void q8k_block(const float* x, int8_t* q, float* d) {
+  float amax = 0.0f;
+  for (int i = 0; i < 256; ++i) amax = std::max(amax, std::fabs(x[i]));
+  float db = amax / 127.0f;
+  *d = db;
+  for (int i = 0; i < 256; ++i) {
+    float v = 0.0f;
+    if (db != 0.0f) {
+      v = std::round(x[i] / db);  // std::round: halfway cases away from zero
+      v = std::min(127.0f, std::max(-127.0f, v));
+    }
+    q[i] = (int8_t)v;
+  }
+}
+
+// y[n] for one activation row (codes qa[K], scales da[K/256]):
+//   y[n] = sum_b da[b] * (d_w * sum_j sc_j * isum_j  -  dmin * sum_j mn_j * bsum_j)
+// with isum_j = sum over sub-block j of q_w * q_a and bsum_j = sum of q_a.
+double row_dot(const uint8_t* w, int fmt, int64_t nb, int64_t n, const int8_t* qa, const float* da) {
+  SuperBlock sb;
+  double acc = 0.0;
+  int ns = n_sub(fmt), sl = sub_len(fmt);
+  for (int64_t b = 0; b < nb; ++b) {
+    unpack_sb(w, fmt, nb, n, b, &sb);
+    int64_t S = 0, M = 0;
+    for (int j = 0; j < ns; ++j) {
+      int64_t isum = 0, bsum = 0;
+      for (int i = 0; i < sl; ++i) {
+        int k = j * sl + i;
+        isum += (int64_t)sb.q[k] * qa[256 * b + k];
+        bsum += qa[256 * b + k];
+      }
+      S += (int64_t)sb.sc[j] * isum;
+      M += (int64_t)sb.mn[j] * bsum;
+    }
+    acc += (double)da[b] * (sb.d * (double)S - sb.dmin * (double)M);
+  }
+  return acc;
+}
+
+double silu(double g) { return g / (1.0 + std::exp(-g)); }
+
+// One expert's FFN for one token: G, U = gate/up matvecs on q8_K(x); h =
+// silu(G) * U; h is rounded to fp32 and re-quantized to q8_K (all matmuls run
+// on q8_K activations); y = down matvec.  y has H entries.
+void expert_ffn_token(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int fmt, int64_t H,
+                      int64_t I, const int8_t* xq, const float* xd, double* y, int nthreads,
+                      float* h_out, int8_t* hq_out, float* hd_out) {
+  std::vector<double> G(I), U(I);
+  int64_t nbH = H / 256, nbI = I / 256;
+  parallel_for(I, nthreads, [&](int64_t n) {
+    G[n] = row_dot(gate, fmt, nbH, n, xq, xd);
+    U[n] = row_dot(up, fmt, nbH, n, xq, xd);
+  });
+  std::vector<float> h32(I);
+  for (int64_t n = 0; n < I; ++n) h32[n] = (float)(silu(G[n]) * U[n]);
+  std::vector<int8_t> hq(I);
+  std::vector<float> hd(nbI);
+  for (int64_t b = 0; b < nbI; ++b) q8k_block(&h32[256 * b], &hq[256 * b], &hd[b]);
+  if (h_out) std::memcpy(h_out, h32.data(), sizeof(float) * I);
+  if (hq_out) std::memcpy(hq_out, hq.data(), I);
+  if (hd_out) std::memcpy(hd_out, hd.data(), sizeof(float) * nbI);
+  parallel_for(H, nthreads, [&](int64_t n) { y[n] = row_dot(down, fmt, nbI, n, hq.data(), hd.data()); });
+}
+
+}  // namespace
+
+extern "C" {
+
+// fp16 bit pattern -> double (exposed for the format pins).
+double orc_half_to_double(uint16_t h) { return half_to_double(h); }
+
+// Unpack the fields of super-block (row n, block b) of a [N, K] matrix.
+// q: 256 ints, sc/mn: n_sub ints, dd: {d, dmin}.
+void orc_unpack_sb(const uint8_t* w, int fmt, int64_t N, int64_t K, int64_t n, int64_t b, int32_t* q,
+                   int32_t* sc, int32_t* mn, double* dd) {
+  (void)N;
+  SuperBlock sb;
+  unpack_sb(w, fmt, K / 256, n, b, &sb);
+  for (int i = 0; i < 256; ++i) q[i] = sb.q[i];
+  for (int j = 0; j < n_sub(fmt); ++j) {
+    sc[j] = sb.sc[j];
+    mn[j] = sb.mn[j];
+  }
+  dd[0] = sb.d;
+  dd[1] = sb.dmin;
+}
+
+// Dequantized matrix W[N, K] in fp64: w = d * sc_j * q - dmin * mn_j.
+void orc_dequant_matrix(const uint8_t* w, int fmt, int64_t N, int64_t K, double* out) {
+  int64_t nb = K / 256;
+  int sl = sub_len(fmt);
+  SuperBlock sb;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b) {
+      unpack_sb(w, fmt, nb, n, b, &sb);
+      for (int k = 0; k < 256; ++k) {
+        int j = k / sl;
+        out[n * K + 256 * b + k] = sb.d * sb.sc[j] * sb.q[k] - sb.dmin * sb.mn[j];
+      }
+    }
+}
+
+// q8_K quantization of x[T, K] (K a multiple of 256): codes q[T, K],
+// scales d[T, K/256], and sums of every 16 consecutive codes bsum16[T, K/16].
+void orc_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bsum16) {
+  int64_t nb = K / 256;
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t b = 0; b < nb; ++b) q8k_block(x + t * K + 256 * b, q + t * K + 256 * b, d + t * nb + b);
+  if (bsum16)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t g = 0; g < K / 16; ++g) {
+        int s = 0;
+        for (int i = 0; i < 16; ++i) s += q[t * K + 16 * g + i];
+        bsum16[t * (K / 16) + g] = (int16_t)s;
+      }
+}
+
+// Integer sub-block sums of activation rows qa[T, K] against W[N, K]:
+// isum[t][n][b][j] = sum_{i in sub-block j of SB b} q_w * q_a  (int32),
+// bsum[t][b][j]    = sum_{i in sub-block j of SB b} q_a.
+void orc_subblock_dots(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, int64_t T,
+                       int32_t* isum, int32_t* bsum) {
+  int64_t nb = K / 256;
+  int ns = n_sub(fmt), sl = sub_len(fmt);
+  SuperBlock sb;
+  for (int64_t t = 0; t < T; ++t)
+    for (int64_t b = 0; b < nb; ++b)
+      for (int j = 0; j < ns; ++j) {
+        int64_t s = 0;
+        for (int i = 0; i < sl; ++i) s += qa[t * K + 256 * b + j * sl + i];
+        bsum[(t * nb + b) * ns + j] = (int32_t)s;
+      }
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b) {
+      unpack_sb(w, fmt, nb, n, b, &sb);
+      for (int64_t t = 0; t < T; ++t)
+        for (int j = 0; j < ns; ++j) {
+          int64_t s = 0;
+          for (int i = 0; i < sl; ++i) s += (int64_t)sb.q[j * sl + i] * qa[t * K + 256 * b + j * sl + i];
+          isum[((t * N + n) * nb + b) * ns + j] = (int32_t)s;
+        }
+    }
+}
+
+// y[T, N] = block-quantized W[N, K] applied to q8_K rows (qa[T, K], da[T, K/256]).
+void orc_qmatvec(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, const float* da,
+                 int64_t T, double* y, int nthreads) {
+  int64_t nb = K / 256;
+  parallel_for(N, nthreads, [&](int64_t n) {
+    for (int64_t t = 0; t < T; ++t) y[t * N + n] = row_dot(w, fmt, nb, n, qa + t * K, da + t * nb);
+  });
+}
+
+// Router: logits[t][e] = sum_h W_r[e][h] * x[t][h] (+ bias[e]) in fp64 from
+// the fp32 inputs.  Top-k by a full stable sort on descending logit (equal
+// logits: lower expert index first).  Gates renormalised over the k:
+//   route 0 (softmax): g_s = exp(l_s - l_max) / sum_sel exp(l - l_max)
+//   route 1 (sigmoid): g_s = sigma(l_s) / sum_sel sigma(l)
+// gap[t] = l_(k) - l_(k+1) (+inf when k == E).
+// forced_ids (nullable): use these ids instead of the top-k (the gates are
+// still computed from the logits of the forced ids).
+void orc_route(const float* x, const float* wr, const float* bias, int64_t T, int64_t H, int64_t E,
+               int64_t k, int route, const int32_t* forced_ids, double* logits, int32_t* ids,
+               double* gates, double* gap) {
+  std::vector<int> order(E);
+  for (int64_t t = 0; t < T; ++t) {
+    double* l = logits + t * E;
+    for (int64_t e = 0; e < E; ++e) {
+      double s = 0.0;
+      for (int64_t h = 0; h < H; ++h) s += (double)wr[e * H + h] * (double)x[t * H + h];
+      if (bias) s += (double)bias[e];
+      l[e] = s;
+    }
+    for (int64_t e = 0; e < E; ++e) order[e] = (int)e;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return l[a] > l[b]; });
+    if (gap) gap[t] = (k < E) ? l[order[k - 1]] - l[order[k]] : INFINITY;
+    int32_t* id = ids + t * k;
+    for (int64_t s = 0; s < k; ++s) id[s] = forced_ids ? forced_ids[t * k + s] : order[s];
+    double* g = gates + t * k;
+    if (route == 0) {
+      double lmax = -INFINITY;
+      for (int64_t s = 0; s < k; ++s) lmax = std::max(lmax, l[id[s]]);
+      double z = 0.0;
+      for (int64_t s = 0; s < k; ++s) z += std::exp(l[id[s]] - lmax);
+      for (int64_t s = 0; s < k; ++s) g[s] = std::exp(l[id[s]] - lmax) / z;
+    } else {
+      double z = 0.0;
+      for (int64_t s = 0; s < k; ++s) z += 1.0 / (1.0 + std::exp(-l[id[s]]));
+      for (int64_t s = 0; s < k; ++s) g[s] = (1.0 / (1.0 + std::exp(-l[id[s]]))) / z;
+    }
+  }
+}
+
+// Bucketing of the T*k (token, slot) pairs by expert, stable by token, plus
+// one bucket per shared expert holding every token.
+//   counts[e] (E + S entries), offsets[e] (E + S + 1 entries, exclusive sum),
+//   perm[offsets[e] + i] = the slot index p of the i-th pair of bucket e,
+//   where p = t*k + s for routed pairs and p = T*k + sh*T + t for shared.
+void orc_bucket(const int32_t* ids, int64_t T, int64_t k, int64_t E, int64_t S, int32_t* counts,
+                int32_t* offsets, int32_t* perm) {
+  for (int64_t e = 0; e < E + S; ++e) counts[e] = 0;
+  for (int64_t p = 0; p < T * k; ++p) counts[ids[p]]++;
+  for (int64_t sh = 0; sh < S; ++sh) counts[E + sh] = (int32_t)T;
+  offsets[0] = 0;
+  for (int64_t e = 0; e < E + S; ++e) offsets[e + 1] = offsets[e] + counts[e];
+  int64_t pos = 0;
+  for (int64_t e = 0; e < E; ++e)
+    for (int64_t t = 0; t < T; ++t)
+      for (int64_t s = 0; s < k; ++s)
+        if (ids[t * k + s] == e) perm[pos++] = (int32_t)(t * k + s);
+  for (int64_t sh = 0; sh < S; ++sh)
+    for (int64_t t = 0; t < T; ++t) perm[pos++] = (int32_t)(T * k + sh * T + t);
+}
+
+// One expert FFN (gate/up/down matrices) on T tokens of q8_K activations.
+// y[T, H].  Optionally returns h (fp32 [T, I]) and its q8_K codes/scales.
+void orc_expert_ffn(const uint8_t* gate, const uint8_t* up, const uint8_t* down, int fmt, int64_t H,
+                    int64_t I, const int8_t* xq, const float* xd, int64_t T, double* y, float* h_out,
+                    int8_t* hq_out, float* hd_out, int nthreads) {
+  for (int64_t t = 0; t < T; ++t)
+    expert_ffn_token(gate, up, down, fmt, H, I, xq + t * H, xd + t * (H / 256), y + t * H, nthreads,
+                     h_out ? h_out + t * I : nullptr, hq_out ? hq_out + t * I : nullptr,
+                     hd_out ? hd_out + t * (I / 256) : nullptr);
+}
+
+// The MoE layer on T tokens:
+//   out[t] = residual[t] + sum_{s<k} g[t][s] * FFN_{ids[t][s]}(q8_K(x[t]))
+//                        + sum_{sh<S} FFN_{E+sh}(q8_K(x[t]))
+// gate/up/down: E + S matrix pointers (host); a NULL gate pointer means the
+// expert is not present and contributes nothing.  residual may be NULL.
+// forced_ids (nullable) replaces the router's top-k.  out is fp64.
+void orc_layer_forward(int fmt, int64_t H, int64_t I, int64_t E, int64_t k, int64_t S, int route,
+                       const uint8_t* const* gate, const uint8_t* const* up, const uint8_t* const* down,
+                       const float* wr, const float* bias, const float* x, const float* residual,
+                       int64_t T, const int32_t* forced_ids, double* out, int32_t* ids, double* gates,
+                       double* gap, int nthreads) {
+  std::vector<int8_t> xq(T * H);
+  std::vector<float> xd(T * (H / 256));
+  orc_q8k_quantize(x, T, H, xq.data(), xd.data(), nullptr);
+  std::vector<double> logits(T * E);
+  orc_route(x, wr, bias, T, H, E, k, route, forced_ids, logits.data(), ids, gates, gap);
+  std::vector<double> y(H);
+  for (int64_t t = 0; t < T; ++t) {
+    double* o = out + t * H;
+    for (int64_t h = 0; h < H; ++h) o[h] = residual ? (double)residual[t * H + h] : 0.0;
+    const int8_t* q = xq.data() + t * H;
+    const float* d = xd.data() + t * (H / 256);
+    for (int64_t s = 0; s < k; ++s) {
+      int e = ids[t * k + s];
+      if (!gate[e]) continue;
+      expert_ffn_token(gate[e], up[e], down[e], fmt, H, I, q, d, y.data(), nthreads, nullptr, nullptr,
+                       nullptr);
+      for (int64_t h = 0; h < H; ++h) o[h] += gates[t * k + s] * y[h];
+    }
+    for (int64_t sh = 0; sh < S; ++sh) {
+      int64_t e = E + sh;
+      if (!gate[e]) continue;
+      expert_ffn_token(gate[e], up[e], down[e], fmt, H, I, q, d, y.data(), nthreads, nullptr, nullptr,
+                       nullptr);
+      for (int64_t h = 0; h < H; ++h) o[h] += y[h];
+    }
+  }
+}
+
+}  // extern "C"

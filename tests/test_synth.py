@@ -1,0 +1,52 @@
+"""The seeded input generators (CPU): determinism, field ranges and
+distributions, independence of streams."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.layout import FMT_Q4K, FMT_Q2K
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+def test_matrix_generator_is_deterministic_and_keyed(fmt):
+    a = synth.gen_matrix(fmt, 256, 512, 1, 0, 3, 0)
+    b = synth.gen_matrix(fmt, 256, 512, 1, 0, 3, 0)
+    c = synth.gen_matrix(fmt, 256, 512, 1, 0, 3, 1)
+    d = synth.gen_matrix(fmt, 256, 512, 2, 0, 3, 0)
+    assert a.size == synth.matrix_bytes(fmt, 256, 512)
+    np.testing.assert_array_equal(a, b)
+    assert (a != c).mean() > 0.9 and (a != d).mean() > 0.9
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+def test_generated_fields_follow_the_workload_distributions(fmt):
+    N, K = 512, 1024
+    w = synth.gen_matrix(fmt, N, K, 0, 0, 0, 0)
+    qmax, smax = (15, 63) if fmt == FMT_Q4K else (3, 15)
+    qs, scs, mns, ds, dms = [], [], [], [], []
+    for n in range(0, N, 7):
+        for b in range(K // 256):
+            q, sc, mn, d, dmin = oracle.unpack_sb(w, fmt, N, K, n, b)
+            qs.append(q); scs.append(sc); mns.append(mn); ds.append(d); dms.append(dmin)
+    q = np.concatenate(qs); sc = np.concatenate(scs); mn = np.concatenate(mns)
+    ds = np.array(ds); dms = np.array(dms)
+    for v, top in [(q, qmax), (sc, smax), (mn, smax)]:
+        hist = np.bincount(v, minlength=top + 1)
+        assert hist.size == top + 1
+        expect = v.size / (top + 1)
+        assert np.abs(hist - expect).max() < 6 * np.sqrt(expect) + 3
+    assert ds.min() >= 1e-4 * 0.999 and ds.max() <= 1e-3 * 1.001
+    assert dms.min() >= 0 and dms.max() <= 5e-4 * 1.001
+    assert abs(ds.mean() - 5.5e-4) < 3e-5 and abs(dms.mean() - 2.5e-4) < 2e-5
+
+
+def test_float_streams():
+    x = synth.activations(4, 512, 0)
+    assert x.dtype == np.float32 and x.shape == (4, 512)
+    np.testing.assert_array_equal(x, synth.activations(4, 512, 0))
+    assert not np.array_equal(x, synth.activations(4, 512, 0, layer=1))
+    wr = synth.router_weight(256, 2048, 1)
+    assert abs(wr.std() * np.sqrt(2048) - 1) < 0.01
+    b = synth.router_bias(192, 2.0, 3)
+    assert abs(b.std() - 2) < 0.4
