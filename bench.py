@@ -1,0 +1,455 @@
+#!/usr/bin/env python
+"""Benchmark of the block-quantized routed MoE layer on GB300.
+
+One step = one pass of the whole layer (q8_K quantize, router top-k,
+bucketing, expert gate/up + SwiGLU + down, combine into the residual) over
+every layer of the workload, for that workload's tokens per layer.  The
+default workload is the Qwen3.6-35B-A3B-shaped decode stack: 40 layers,
+H=2048, 256 routed experts (softmax top-8) + 1 shared expert, I=512,
+Q4_K-style weights (18.2 GB resident), one token per layer.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--T T]
+  python bench.py --impl reference ...   (the CPU oracle, as the reference arm)
+
+Prints one JSON line (rank 0).  With torchrun (N > 1) each rank runs an
+independent replica of the workload on its own GPU (the layer has no data-path
+exchange on one GPU); value = tokens of all ranks / max time over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import synth  # noqa: E402
+from synth.workloads import DEFAULT_BENCH, WORKLOADS  # noqa: E402
+
+METRIC = "MoE-layer decode tokens/s; active-expert HBM GB/s as fraction of GB300 peak"
+FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: about 3 s of work)")
+    ap.add_argument("--warmup", type=int, default=None, help="untimed warm-up steps (default 20, at least 3)")
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_BENCH, choices=sorted(WORKLOADS))
+    ap.add_argument("--T", type=int, default=None, help="tokens per layer (overrides the workload's)")
+    ap.add_argument("--layers", type=int, default=None,
+                    help="layers (overrides the workload's; smaller cases for profiling captures)")
+    ap.add_argument("--rotations", type=int, default=16, help="distinct input sets cycled through the steps")
+    ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    return ap.parse_args()
+
+
+# ----------------------------------------------------------------------------- helpers
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "block_quantized_routed_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh", ".h")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name):
+    """dram bytes per launch of the gate/up kernel from a committed ncu summary,
+    if its kernel-source hash matches the current sources (else None)."""
+    pdir = os.path.join(ROOT, "profiles")
+    if not os.path.isdir(pdir):
+        return None
+    want = kernel_source_hash()
+    for f in sorted(os.listdir(pdir)):
+        if not f.endswith(".md"):
+            continue
+        txt = open(os.path.join(pdir, f)).read()
+        m = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+workload:\s*(\S+)\s+source_hash:\s*(\w+)",
+                      txt, flags=re.M)
+        if m and m.group(2) == workload_name and m.group(3) == want:
+            return float(m.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.out = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        load = [s for s in sm if s > 0.5 * max(sm)] or sm
+        return {"sm_mhz": statistics.median(load), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def host_inputs(wl, T, R):
+    """x [R, L, T, H] fp32 (rotation r, layer l)."""
+    return np.stack([np.stack([synth.activations(T, wl.H, wl.seed, l, r) for l in range(wl.layers)])
+                     for r in range(R)])
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+
+def oracle_layers(wl, T, x_rl, layers, nthreads):
+    """Run the oracle on the given layers of one rotation (x_rl [L, T, H]);
+    experts are generated on the host for the routed ones only.  Returns
+    (outputs {layer: fp64 [T, H]}, seconds spent in the oracle)."""
+    import oracle
+    outs, spent = {}, 0.0
+    for l in layers:
+        wr = synth.router_weight(wl.E, wl.H, wl.seed, l)
+        bias = synth.router_bias(wl.E, wl.bias_std, wl.seed, l) if wl.bias_std > 0 else None
+        x = x_rl[l]
+        _, ids, _, _ = oracle.route(x, wr, bias, wl.k, wl.route)
+        need = sorted(set(ids.reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
+        experts = [None] * (wl.E + wl.S)
+        for e in need:
+            experts[e] = (synth.gen_matrix(wl.fmt, wl.I, wl.H, wl.seed, l, e, 0),
+                          synth.gen_matrix(wl.fmt, wl.I, wl.H, wl.seed, l, e, 1),
+                          synth.gen_matrix(wl.fmt, wl.H, wl.I, wl.seed, l, e, 2))
+        t0 = time.perf_counter()
+        out, _, _, _ = oracle.layer_forward(wl.fmt, wl.H, wl.I, wl.E, wl.k, wl.S, wl.route, experts, wr, bias, x,
+                                            residual=x, nthreads=nthreads)
+        spent += time.perf_counter() - t0
+        outs[l] = out
+    return outs, spent
+
+
+def cpu_baseline(wl, T, x_host, budget_s):
+    import oracle
+    nthreads = oracle.default_threads()
+    done, spent = 0, 0.0
+    layers = []
+    while spent < budget_s and done < wl.layers * 4:
+        l = done % wl.layers
+        _, s = oracle_layers(wl, T, x_host[0], [l], nthreads)
+        spent += s
+        layers.append(l)
+        done += 1
+    tok_s = (done / wl.layers) * T / spent
+    return {"value": tok_s, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
+            "sample": f"{done} of {wl.layers} layers x {T} token(s) of rotation 0 ({spent:.1f} s of oracle time); "
+                      f"tokens/s = layers done / layers per step * tokens / seconds"}
+
+
+# ----------------------------------------------------------------------------- reference arm
+
+def run_reference(args, wl, T):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    K = args.steps if args.steps is not None else 3
+    W = max(args.warmup if args.warmup is not None else 1, 0)
+    x_host = host_inputs(wl, T, 1)
+    nthreads = oracle.default_threads()
+    # size each step's sample so that the whole run stays within ~2 minutes
+    _, t_layer = oracle_layers(wl, T, x_host[0], [0], nthreads)
+    per_step = max(1, min(wl.layers, int(120.0 / max(K + W, 1) / max(t_layer, 1e-3))))
+    for i in range(W):
+        oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads)
+    spent = 0.0
+    for i in range(K):
+        _, s = oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads)
+        spent += s
+    tok_s = (K * per_step / wl.layers) * T / spent
+    line = {
+        "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": 1e3 * spent / K, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64 (int64 sub-block sums)", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": wl.layers, "T": T, "sample_layers_per_step": per_step},
+        "cpu_baseline": {"kind": "oracle", "cores": nthreads, "value": tok_s, "unit": "tokens/s",
+                         "sample": f"{per_step} of {wl.layers} layers per step, {T} token(s) per layer"},
+        "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- our arm
+
+def run_ours(args, wl, T):
+    import torch
+
+    import block_quantized_routed_gb300 as moe
+    import synth.gpu
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    moe.load()
+    L, H, R = wl.layers, wl.H, args.rotations
+    bank = synth.gpu.ExpertBank(wl.fmt, wl.H, wl.I, wl.E + wl.S, L, wl.seed, device=dev)
+    routers = [torch.from_numpy(synth.router_weight(wl.E, H, wl.seed, l)).to(dev) for l in range(L)]
+    biases = [torch.from_numpy(synth.router_bias(wl.E, wl.bias_std, wl.seed, l)).to(dev) if wl.bias_std > 0 else None
+              for l in range(L)]
+    layers = [moe.MoeLayer(wl.desc(T), bank.table(l), routers[l], biases[l], device=dev) for l in range(L)]
+    x_host = host_inputs(wl, T, R)
+    xs = torch.from_numpy(x_host).to(dev)                      # [R, L, T, H]
+    x_static = torch.empty((L, T, H), dtype=torch.float32, device=dev)
+    out = torch.empty((L, T, H), dtype=torch.float32, device=dev)
+    ids_buf = torch.empty((L, T, wl.k), dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def body(record_ids=False):
+        for l in range(L):
+            layers[l].forward(x_static[l], residual=x_static[l], out=out[l],
+                              ids_out=ids_buf[l] if record_ids else None)
+
+    # unique active experts per layer for every rotation (counted from the routing)
+    union = np.zeros((R, L), np.int64)
+    for r in range(R):
+        x_static.copy_(xs[r])
+        body(record_ids=True)
+        ids = ids_buf.cpu().numpy()
+        for l in range(L):
+            union[r, l] = len(set(ids[l].reshape(-1).tolist())) + wl.S
+    for l in range(L):
+        st = moe.moe_get_status(layers[l].ws)
+        if st != 0:
+            raise RuntimeError(f"layer {l}: device status {moe.moe_status_string(st)}")
+    out_r0 = None
+    x_static.copy_(xs[0])
+    body()
+    torch.cuda.synchronize()
+    out_r0 = out.cpu().numpy()
+
+    # CUDA graph of one step, with trace events around each layer's expert kernels
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(4 * L)]
+    use_graph = not args.no_graph
+    graph = None
+    if use_graph:
+        moe.moe_trace_events(events)
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            body()
+        moe.moe_trace_events(None)
+
+    stream = torch.cuda.current_stream()
+
+    def step(i):
+        x_static.copy_(xs[i % R], non_blocking=True)
+        if use_graph:
+            graph.replay()
+        else:
+            moe.moe_trace_events(events)
+            body()
+            moe.moe_trace_events(None)
+
+    W = max(3, args.warmup if args.warmup is not None else 20)
+    for i in range(W):
+        step(i)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for i in range(5):
+        step(i)
+    torch.cuda.synchronize()
+    t_step = (time.perf_counter() - t0) / 5
+    K = args.steps if args.steps is not None else int(min(20000, max(20, 3.0 / max(t_step, 1e-6))))
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    ev0.record(stream)
+    for i in range(K):
+        step(W + i)
+    ev1.record(stream)
+    torch.cuda.synchronize()
+    clock_info = clocks.stop()
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    if world > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([ms_total], device=dev)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        ms_total = float(tt.item())
+    ms_step = ms_total / K
+
+    # per-kernel durations of the last step (trace events)
+    gu_ms = [events[4 * l].elapsed_time(events[4 * l + 1]) for l in range(L)]
+    dn_ms = [events[4 * l + 2].elapsed_time(events[4 * l + 3]) for l in range(L)]
+
+    # bytes
+    gu_bytes = synth.layout.matrix_bytes(wl.fmt, wl.I, wl.H)
+    dn_bytes = synth.layout.matrix_bytes(wl.fmt, wl.H, wl.I)
+    exp_bytes = 2 * gu_bytes + dn_bytes
+    steps_rot = [(W + i) % R for i in range(K)]
+    active_bytes_total = float(sum(union[r].sum() for r in steps_rot)) * exp_bytes
+    active_gbs = active_bytes_total / (ms_total * 1e-3) / 1e9
+    last_r = (W + K - 1) % R
+    gu_alg = union[last_r] * 2 * gu_bytes                        # per launch (layer) of the last step
+    dn_alg = union[last_r] * dn_bytes
+    gu_gbs = float(np.sum(gu_alg) / (np.sum(gu_ms) * 1e-3) / 1e9)
+    dn_gbs = float(np.sum(dn_alg) / (np.sum(dn_ms) * 1e-3) / 1e9)
+    peak, peak_src = measured_peaks()
+
+    # end to end through the public call with host buffers: pinned H2D of the
+    # step's inputs, the layers, D2H of the outputs, every step
+    x_pinned = torch.from_numpy(x_host).pin_memory()
+    out_pinned = torch.empty((L, T, H), dtype=torch.float32).pin_memory()
+    Ke = max(10, min(K, 2000))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(Ke):
+        x_static.copy_(x_pinned[i % R], non_blocking=True)
+        if use_graph:
+            graph.replay()
+        else:
+            body()
+        out_pinned.copy_(out, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    h2d = L * T * H * 4
+    d2h = L * T * H * 4
+
+    tokens_per_step = T * world
+    value = tokens_per_step / (ms_step * 1e-3)
+    launches_per_layer = 6 if T * wl.k <= 256 else 10
+    line = {
+        "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
+        "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "int8 x int4/int2 -> int32 (dp4a) + fp32", "data": "synthetic",
+        "config": {"workload": wl.name, "layers": L, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.k,
+                   "n_shared": wl.S, "route": ["softmax", "sigmoid"][wl.route], "fmt": ["q4_k", "q2_k"][wl.fmt],
+                   "parallelism": f"replicas{world}",
+                   "l2": "inputs larger than L2: each step streams %.0f MB of distinct expert weights "
+                         "plus %.0f MB of router weights (L2 129 MB)" % (
+                             np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
+                   "graph": use_graph, "rotations": R},
+        "clocks": clock_info,
+        "us_per_layer": 1e3 * ms_step / L,
+        "active_expert_bytes_per_step": active_bytes_total / K,
+        "active_expert_gbs": active_gbs,
+        "active_frac_of_8tbs": active_gbs / NOMINAL_HBM_GBS,
+        "active_frac_of_measured": active_gbs / peak,
+        "roofline": {"bound": "hbm", "kernel": "gateup_kernel (expert gate/up GEMV + SwiGLU + q8_K requant)",
+                     "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
+                     "peak_source": peak_src,
+                     "traffic": profiled_traffic(wl.name),
+                     "algorithmic_bytes_per_launch": float(np.mean(gu_alg)),
+                     "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
+                     "down_kernel_gbs": dn_gbs, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms))},
+        "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+        "gpu_launches": launches_per_layer * L * K,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(wl, T, x_host, args.cpu_budget_s)
+        # parity spot check of the bench's own launch configuration on the first layers
+        import oracle
+        outs, _ = oracle_layers(wl, T, x_host[0], [0, L - 1], oracle.default_threads())
+        worst = 0.0
+        for l, ref in outs.items():
+            err = np.abs(out_r0[l] - ref) / (1e-4 + 1e-3 * np.linalg.norm(ref, axis=1, keepdims=True))
+            worst = max(worst, float(err.max()))
+        line["parity_spot_check"] = {"layers": sorted(outs), "worst_err_over_tol": worst}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def main():
+    args = parse_args()
+    wl = WORKLOADS[args.workload]
+    T = args.T or wl.T
+    if args.T:
+        wl = wl.with_T(T)
+    if args.layers:
+        import dataclasses
+        wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}_l{args.layers}")
+    if args.impl == "reference":
+        run_reference(args, wl, T)
+    else:
+        run_ours(args, wl, T)
+
+
+if __name__ == "__main__":
+    main()

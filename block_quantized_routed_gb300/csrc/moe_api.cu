@@ -1,0 +1,358 @@
+// C ABI of the block-quantized MoE layer: argument validation, workspace
+// plans and the launch sequences.  Every entry point validates on the host
+// before it touches the GPU, so a rejected call launches nothing.
+#include <cstdint>
+#include <cstring>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Carve {
+  size_t off = 0;
+  size_t take(size_t bytes) {
+    const size_t at = off;
+    off = align_up(off + bytes);
+    return at;
+  }
+};
+
+cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+int check(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+}  // namespace
+
+bool desc_valid(const moe_layer_desc* d, int* why) {
+  *why = MOE_ERR_INVALID_ARG;
+  if (!d) return false;
+  *why = MOE_ERR_UNSUPPORTED;
+  if (d->H <= 0 || d->I <= 0 || d->H % 256 || d->I % 256 || d->H > MOE_MAX_DIM || d->I > MOE_MAX_DIM) return false;
+  if (d->E < 1 || d->E > MOE_MAX_EXPERTS) return false;
+  if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->E) return false;
+  if (d->n_shared < 0 || d->n_shared > MOE_MAX_SHARED) return false;
+  if (d->route != MOE_ROUTE_SOFTMAX && d->route != MOE_ROUTE_SIGMOID) return false;
+  if (d->fmt != MOE_FMT_Q4K && d->fmt != MOE_FMT_Q2K) return false;
+  if (d->T_max < 1 || (int64_t)d->T_max * (d->top_k + d->n_shared) > (int64_t)1 << 28) return false;
+  return true;
+}
+
+WsPlan plan_workspace(const moe_layer_desc& d) {
+  WsPlan p{};
+  const size_t T = (size_t)d.T_max, H = (size_t)d.H, I = (size_t)d.I, E = (size_t)d.E;
+  const size_t k = (size_t)d.top_k, S = (size_t)d.n_shared, EpS = E + S;
+  const size_t P = T * (k + S);
+  p.max_tiles = (int)P;
+  p.n_chunks = (int)((T * k + kBucketChunk - 1) / kBucketChunk);
+  Carve c;
+  p.pub.status = c.take(16);
+  p.n_tiles = p.pub.status + 4;
+  p.pub.xq = c.take(T * H);
+  p.pub.xd = c.take(T * (H / 256) * 4);
+  p.pub.xbs = c.take(T * (H / 16) * 2);
+  p.pub.logits = c.take(T * E * 4);
+  p.pub.ids = c.take(T * k * 4);
+  p.pub.gates = c.take(T * k * 4);
+  p.pub.gap = c.take(T * 4);
+  p.pub.counts = c.take(EpS * 4);
+  p.pub.offsets = c.take((EpS + 1) * 4);
+  p.pub.perm = c.take(P * 4);
+  p.pub.inv = c.take(P * 4);
+  p.pub.h = c.take(P * I * 4);
+  p.pub.hq = c.take(P * I);
+  p.pub.hd = c.take(P * (I / 256) * 4);
+  p.pub.hbs = c.take(P * (I / 16) * 2);
+  p.pub.y = c.take(P * H * 4);
+  p.tiles = c.take((size_t)p.max_tiles * sizeof(Tile));
+  p.req_cnt = c.take((size_t)p.max_tiles * (I / 256) * 4);
+  p.chunk_cnt = c.take((size_t)(p.n_chunks > 0 ? p.n_chunks : 1) * EpS * 4);
+  p.total = c.off;
+  p.pub.total = p.total;
+  return p;
+}
+
+namespace {
+thread_local void* const* g_trace_events = nullptr;
+thread_local int g_trace_n = 0;
+thread_local int g_trace_next = 0;
+}  // namespace
+
+void trace_record(cudaStream_t s) {
+  if (!g_trace_events || g_trace_next >= g_trace_n) return;
+  cudaEvent_t ev = static_cast<cudaEvent_t>(g_trace_events[g_trace_next++]);
+  if (!ev || cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) != cudaSuccess) {
+    // a profiling record must not turn into the next launch's error: consume
+    // the error and stop tracing
+    cudaGetLastError();
+    g_trace_events = nullptr;
+  }
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+size_t moe_layer_workspace_size(const moe_layer_desc* desc) {
+  int why;
+  if (!desc_valid(desc, &why)) return 0;
+  return plan_workspace(*desc).total;
+}
+
+int moe_workspace_layout(const moe_layer_desc* desc, moe_ws_layout* out) {
+  int why;
+  if (!out) return MOE_ERR_INVALID_ARG;
+  if (!desc_valid(desc, &why)) return why;
+  *out = plan_workspace(*desc).pub;
+  return MOE_OK;
+}
+
+int moe_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bsum16, void* stream) {
+  if (T < 0 || K <= 0 || K % 256) return T < 0 || K <= 0 ? MOE_ERR_INVALID_ARG : MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !q || !d) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(q, 16) || !aligned(d, 4) || (bsum16 && !aligned(bsum16, 4)))
+    return MOE_ERR_INVALID_ARG;
+  return check(launch_q8k_quantize(x, T, K, q, d, bsum16, as_stream(stream)));
+}
+
+int moe_route_topk(const float* x, const float* w_router, const float* bias, int32_t T, int32_t H, int32_t E,
+                   int32_t k, int32_t route, float* logits, int32_t* ids, float* gates, float* gap, void* stream) {
+  if (T < 0 || H <= 0 || E < 1 || k < 1) return MOE_ERR_INVALID_ARG;
+  if (H % 4 || E > MOE_MAX_EXPERTS || k > MOE_MAX_TOPK || k > E) return MOE_ERR_UNSUPPORTED;
+  if (route != MOE_ROUTE_SOFTMAX && route != MOE_ROUTE_SIGMOID) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!x || !w_router || !logits || !ids || !gates) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = as_stream(stream);
+  cudaError_t e = launch_router(x, w_router, bias, T, H, E, logits, s);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  return check(launch_topk(logits, T, E, k, route, ids, gates, gap, s));
+}
+
+size_t moe_bucket_workspace_size(int32_t T, int32_t k, int32_t E, int32_t n_shared) {
+  if (T < 0 || k < 1 || E < 1 || n_shared < 0) return 0;
+  const size_t n_chunks = ((size_t)T * k + kBucketChunk - 1) / kBucketChunk;
+  return 256 + align_up((n_chunks > 0 ? n_chunks : 1) * (size_t)(E + n_shared) * 4);
+}
+
+int moe_bucket(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t n_shared, int32_t* counts,
+               int32_t* offsets, int32_t* perm, int32_t* inv, void* ws, size_t ws_bytes, void* stream) {
+  if (T < 0 || k < 1 || E < 1 || n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (E > MOE_MAX_EXPERTS || n_shared > MOE_MAX_SHARED || k > MOE_MAX_TOPK) return MOE_ERR_UNSUPPORTED;
+  if (!counts || !offsets || !ws || (T > 0 && (!ids || !perm))) return MOE_ERR_INVALID_ARG;
+  if (!aligned(ws, kAlign)) return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_bucket_workspace_size(T, k, E, n_shared)) return MOE_ERR_WORKSPACE;
+  cudaStream_t s = as_stream(stream);
+  int* status = static_cast<int*>(ws);
+  int32_t* chunk_cnt = reinterpret_cast<int32_t*>(static_cast<char*>(ws) + 256);
+  if ((int64_t)T * k <= kSmallPairs)
+    return check(launch_route_bucket_small(nullptr, T, E, k, 0, n_shared, const_cast<int32_t*>(ids), nullptr,
+                                           nullptr, counts, offsets, perm, inv, nullptr, 1, 0, nullptr, nullptr,
+                                           nullptr, status, s));
+  return check(launch_bucket_large(ids, T, k, E, n_shared, counts, offsets, perm, inv, chunk_cnt, status, s));
+}
+
+size_t moe_expert_ffn_workspace_size(const moe_layer_desc* desc, int32_t T) {
+  int why;
+  if (!desc_valid(desc, &why) || T < 0 || T > desc->T_max) return 0;
+  const size_t P = (size_t)T * (desc->top_k + desc->n_shared), I = (size_t)desc->I;
+  Carve c;
+  c.take(16);
+  c.take(P * sizeof(Tile));
+  c.take(P * (I / 256) * 4);
+  c.take(P * I * 4);
+  c.take(P * I);
+  c.take(P * (I / 256) * 4);
+  c.take(P * (I / 16) * 2);
+  return c.off;
+}
+
+int moe_expert_ffn(const moe_layer_desc* desc, const moe_expert_ptrs* table, const int8_t* q, const float* d,
+                   const int16_t* bsum16, const int32_t* counts, const int32_t* offsets, const int32_t* perm,
+                   int32_t T, float* y_slots, void* ws, size_t ws_bytes, void* stream) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (T < 0 || T > desc->T_max) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!table || !q || !d || !bsum16 || !counts || !offsets || !perm || !y_slots || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(bsum16, 16) || !aligned(y_slots, 16) || !aligned(ws, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < moe_expert_ffn_workspace_size(desc, T)) return MOE_ERR_WORKSPACE;
+  const size_t P = (size_t)T * (desc->top_k + desc->n_shared), I = (size_t)desc->I;
+  char* base = static_cast<char*>(ws);
+  Carve c;
+  int* status = reinterpret_cast<int*>(base + c.take(16));
+  Tile* tiles = reinterpret_cast<Tile*>(base + c.take(P * sizeof(Tile)));
+  int32_t* req_cnt = reinterpret_cast<int32_t*>(base + c.take(P * (I / 256) * 4));
+  FfnArgs a{};
+  a.h = reinterpret_cast<float*>(base + c.take(P * I * 4));
+  a.hq = reinterpret_cast<int8_t*>(base + c.take(P * I));
+  a.hd = reinterpret_cast<float*>(base + c.take(P * (I / 256) * 4));
+  a.hbs = reinterpret_cast<int16_t*>(base + c.take(P * (I / 16) * 2));
+  cudaStream_t s = as_stream(stream);
+  const int TT = pick_tile_tokens(T, desc->H);
+  const int EpS = desc->E + desc->n_shared;
+  int32_t* n_tiles = status + 1;
+  if (launch_plan(counts, offsets, EpS, table, TT, desc->I / 256, tiles, n_tiles, req_cnt, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  a.fmt = desc->fmt;
+  a.H = desc->H;
+  a.I = desc->I;
+  a.T = T;
+  a.k = desc->top_k;
+  a.TT = TT;
+  a.table = table;
+  a.xq = q;
+  a.xd = d;
+  a.xbs = bsum16;
+  a.perm = perm;
+  a.tiles = tiles;
+  a.n_tiles = n_tiles;
+  a.max_tiles = (int)P;
+  a.req_cnt = req_cnt;
+  a.y = y_slots;
+  a.status = status;
+  return check(launch_expert_ffn(a, s));
+}
+
+int moe_combine(const float* y_slots, const float* gates, int32_t T, int32_t H, int32_t k, int32_t n_shared,
+                const float* residual, float* out, void* stream) {
+  if (T < 0 || H <= 0 || k < 1 || n_shared < 0) return MOE_ERR_INVALID_ARG;
+  if (H % 4) return MOE_ERR_UNSUPPORTED;
+  if (T == 0) return MOE_OK;
+  if (!y_slots || !gates || !out) return MOE_ERR_INVALID_ARG;
+  if (!aligned(y_slots, 16) || !aligned(out, 16) || (residual && !aligned(residual, 16))) return MOE_ERR_INVALID_ARG;
+  return check(launch_combine(y_slots, gates, T, H, k, n_shared, residual, out, as_stream(stream)));
+}
+
+int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, const float* w_router,
+                      const float* router_bias, const float* x, const float* residual, float* out, int32_t T,
+                      int32_t* ids_out, float* gates_out, void* ws, size_t ws_bytes, void* stream) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (T < 0 || T > desc->T_max) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!table || !w_router || !x || !out || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(out, 16) || !aligned(w_router, 16) || !aligned(ws, kAlign) ||
+      (residual && !aligned(residual, 16)))
+    return MOE_ERR_INVALID_ARG;
+  const WsPlan p = plan_workspace(*desc);
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  int* status = static_cast<int*>(at(p.pub.status));
+  int32_t* n_tiles = reinterpret_cast<int32_t*>(at(p.n_tiles));
+  int8_t* xq = static_cast<int8_t*>(at(p.pub.xq));
+  float* xd = static_cast<float*>(at(p.pub.xd));
+  int16_t* xbs = static_cast<int16_t*>(at(p.pub.xbs));
+  float* logits = static_cast<float*>(at(p.pub.logits));
+  int32_t* ids = static_cast<int32_t*>(at(p.pub.ids));
+  float* gates = static_cast<float*>(at(p.pub.gates));
+  float* gap = static_cast<float*>(at(p.pub.gap));
+  int32_t* counts = static_cast<int32_t*>(at(p.pub.counts));
+  int32_t* offsets = static_cast<int32_t*>(at(p.pub.offsets));
+  int32_t* perm = static_cast<int32_t*>(at(p.pub.perm));
+  int32_t* inv = static_cast<int32_t*>(at(p.pub.inv));
+  Tile* tiles = static_cast<Tile*>(at(p.tiles));
+  int32_t* req_cnt = static_cast<int32_t*>(at(p.req_cnt));
+  int32_t* chunk_cnt = static_cast<int32_t*>(at(p.chunk_cnt));
+  const int H = desc->H, E = desc->E, k = desc->top_k, S = desc->n_shared;
+  const int TT = pick_tile_tokens(T, H);
+  const int nIB = desc->I / 256;
+  cudaStream_t s = as_stream(stream);
+
+  if (launch_q8k_quantize(x, T, H, xq, xd, xbs, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_router(x, w_router, router_bias, T, H, E, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if ((int64_t)T * k <= kSmallPairs) {
+    if (launch_route_bucket_small(logits, T, E, k, desc->route, S, ids, gates, gap, counts, offsets, perm, inv, table,
+                                  TT, nIB, tiles, n_tiles, req_cnt, status, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    if (launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    if (launch_plan(counts, offsets, E + S, table, TT, nIB, tiles, n_tiles, req_cnt, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+  }
+  FfnArgs a{};
+  a.fmt = desc->fmt;
+  a.H = H;
+  a.I = desc->I;
+  a.T = T;
+  a.k = k;
+  a.TT = TT;
+  a.table = table;
+  a.xq = xq;
+  a.xd = xd;
+  a.xbs = xbs;
+  a.perm = perm;
+  a.tiles = tiles;
+  a.n_tiles = n_tiles;
+  a.max_tiles = p.max_tiles;
+  a.h = static_cast<float*>(at(p.pub.h));
+  a.hq = static_cast<int8_t*>(at(p.pub.hq));
+  a.hd = static_cast<float*>(at(p.pub.hd));
+  a.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+  a.req_cnt = req_cnt;
+  a.y = static_cast<float*>(at(p.pub.y));
+  a.status = status;
+  if (launch_expert_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine(a.y, gates, T, H, k, S, residual, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (ids_out && cudaMemcpyAsync(ids_out, ids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (gates_out &&
+      cudaMemcpyAsync(gates_out, gates, sizeof(float) * T * k, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+int moe_get_status(void* ws, void* stream) {
+  if (!ws) return MOE_ERR_INVALID_ARG;
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  int v = 0;
+  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  return v;
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_WORKSPACE: return "workspace too small";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_DEVICE_BOUNDS: return "device: index out of range";
+    case MOE_ERR_DEVICE_TIMEOUT: return "device: bounded wait ran out";
+    default: return "unknown status";
+  }
+}
+
+int moe_trace_events(void* const* events, int32_t n_events) {
+  if (n_events < 0 || (n_events > 0 && !events)) return MOE_ERR_INVALID_ARG;
+  g_trace_events = n_events > 0 ? events : nullptr;
+  g_trace_n = n_events;
+  g_trace_next = 0;
+  return MOE_OK;
+}
+
+int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, int32_t T,
+                            int32_t* isum, int32_t* bsum, void* stream) {
+  if (fmt != MOE_FMT_Q4K && fmt != MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED;
+  if (N <= 0 || K <= 0 || N % 256 || K % 256 || T < 1 || T > 16) return MOE_ERR_UNSUPPORTED;
+  if (!w || !q || !isum || !bsum) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
+  return check(launch_debug_dots(fmt, w, N, K, q, T, isum, bsum, as_stream(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,94 @@
+// Host-side internals shared by the translation units of the MoE library.
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "moe_q8k.h"
+
+namespace moe {
+
+// Largest (token, slot) pair count handled by the single-CTA top-k+bucket kernel.
+constexpr int kSmallPairs = 256;
+// Pairs per CTA of the multi-CTA bucketing kernels.
+constexpr int kBucketChunk = 1024;
+
+// A unit of expert work: `count` rows of bucket `expert` starting at bucket
+// position `start`; flag 1 = the expert's gate pointer is NULL (not present).
+struct Tile {
+  int expert, start, count, flag;
+};
+
+// Full workspace plan of moe_layer_forward (public regions + internal ones).
+struct WsPlan {
+  moe_ws_layout pub;
+  size_t tiles;       // Tile [max_tiles]
+  size_t n_tiles;     // int32 (inside the status block: status[1])
+  size_t req_cnt;     // int32 [max_tiles * I/256]  arrival counters
+  size_t chunk_cnt;   // int32 [n_chunks * (E + S)]
+  int max_tiles;
+  int n_chunks;
+  size_t total;
+};
+
+bool desc_valid(const moe_layer_desc* d, int* why);
+WsPlan plan_workspace(const moe_layer_desc& d);
+
+// token-group size of the expert kernels for T tokens of hidden size H
+int pick_tile_tokens(int T, int H);
+
+// ---- launchers (return cudaGetLastError of the launch) ---------------------
+cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bs,
+                                cudaStream_t s);
+cudaError_t launch_router(const float* x, const float* w, const float* bias, int T, int H, int E,
+                          float* logits, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int route, int32_t* ids, float* gates,
+                        float* gap, cudaStream_t s);
+// single CTA: top-k (optional: logits != nullptr), bucketing, tile plan; T*k <= kSmallPairs
+cudaError_t launch_route_bucket_small(const float* logits, int T, int E, int k, int route, int S,
+                                      int32_t* ids, float* gates, float* gap, int32_t* counts,
+                                      int32_t* offsets, int32_t* perm, int32_t* inv,
+                                      const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles,
+                                      int32_t* n_tiles, int32_t* req_cnt, int* status, cudaStream_t s);
+// multi-CTA bucketing for any T*k
+cudaError_t launch_bucket_large(const int32_t* ids, int T, int k, int E, int S, int32_t* counts,
+                                int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* chunk_cnt,
+                                int* status, cudaStream_t s);
+// tile plan from counts/offsets (single CTA)
+cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int EpS,
+                        const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles, int32_t* n_tiles,
+                        int32_t* req_cnt, cudaStream_t s);
+
+struct FfnArgs {
+  int fmt, H, I, T, k, TT;
+  const moe_expert_ptrs* table;
+  const int8_t* xq;
+  const float* xd;
+  const int16_t* xbs;
+  const int32_t* perm;
+  const Tile* tiles;
+  const int32_t* n_tiles;
+  int max_tiles;
+  float* h;
+  int8_t* hq;
+  float* hd;
+  int16_t* hbs;
+  int32_t* req_cnt;
+  float* y;          // slot-indexed [T*(k+S), H]
+  int* status;
+};
+cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
+
+// profiling hook state (per host thread): records the next event if tracing
+void trace_record(cudaStream_t s);
+
+cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S,
+                           const float* residual, float* out, cudaStream_t s);
+
+cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t* q, int T, int32_t* isum,
+                              int32_t* bsum, cudaStream_t s);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,409 @@
+// q8_K quantization, router logits, top-k gates, token -> expert bucketing
+// and the expert tile plan.
+//
+// Sources: Pulsar README, "Fidelity notes" (q8_0/q8_K activations), "What it
+// does today" (softmax router), "How the streaming works" (one expert union
+// per batch or prefill chunk; explicit per-(token, slot) pointers, NULL =
+// not mine); Pulsar digest note, section 1 (sigmoid-gated router + shared
+// expert); Strata summary (router and shared expert resident on the GPU).
+#include <cfloat>
+#include <climits>
+#include <cmath>
+
+#include "moe_device.cuh"
+#include "moe_internal.h"
+
+namespace moe {
+namespace {
+
+// ---------------------------------------------------------------- q8_K
+// one warp per 256-element block
+__global__ void __launch_bounds__(256) q8k_quantize_kernel(const float* __restrict__ x, int64_t nblocks,
+                                                           int8_t* __restrict__ q, float* __restrict__ d,
+                                                           int16_t* __restrict__ bs) {
+  const int lane = threadIdx.x & 31;
+  const int64_t blk = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (blk >= nblocks) return;
+  const float4* src = reinterpret_cast<const float4*>(x + blk * 256 + 8 * lane);
+  float4 a = __ldg(src), b = __ldg(src + 1);
+  float v[8] = {a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w};
+  q8k_block_warp(v, lane, q + blk * 256, d + blk, bs ? bs + blk * 16 : nullptr);
+}
+
+// ---------------------------------------------------------------- router
+// One warp per expert row e: logits[t, e] = sum_h w[e, h] * x[t, h] (+ bias[e]).
+// Each lane accumulates a strided partial sum (h = 4*lane + 128*i), then a
+// butterfly reduction: a fixed order, so results are deterministic.
+constexpr int kRouterTok = 8;
+
+__global__ void __launch_bounds__(128) router_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                     const float* __restrict__ bias, int T, int H, int E,
+                                                     float* __restrict__ logits) {
+  const int lane = threadIdx.x & 31;
+  const int nwarps = gridDim.x * (blockDim.x >> 5);
+  const int H4 = H >> 2;
+  for (int e = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); e < E; e += nwarps) {
+    const float4* wr = reinterpret_cast<const float4*>(w + (int64_t)e * H);
+    const float be = bias ? __ldg(bias + e) : 0.0f;
+    for (int t0 = 0; t0 < T; t0 += kRouterTok) {
+      float acc[kRouterTok];
+#pragma unroll
+      for (int t = 0; t < kRouterTok; ++t) acc[t] = 0.0f;
+      for (int h4 = lane; h4 < H4; h4 += 32) {
+        const float4 wv = __ldg(wr + h4);
+#pragma unroll
+        for (int t = 0; t < kRouterTok; ++t) {
+          if (t0 + t < T) {
+            const float4 xv = __ldg(reinterpret_cast<const float4*>(x + (int64_t)(t0 + t) * H) + h4);
+            acc[t] = fmaf(wv.x, xv.x, acc[t]);
+            acc[t] = fmaf(wv.y, xv.y, acc[t]);
+            acc[t] = fmaf(wv.z, xv.z, acc[t]);
+            acc[t] = fmaf(wv.w, xv.w, acc[t]);
+          }
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < kRouterTok; ++t) {
+        float v = acc[t];
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+        if (lane == 0 && t0 + t < T) logits[(int64_t)(t0 + t) * E + e] = v + be;
+      }
+    }
+  }
+}
+
+// ---------------------------------------------------------------- top-k
+// One warp per token.  Lane l owns experts e = l + 32*i; a bit per owned
+// expert marks it as taken.  k+1 rounds of a warp arg-max (larger logit wins,
+// equal logits: lower index) give the k ids in descending order and the gap.
+// NaN logits are treated as -inf.
+__device__ __forceinline__ void warp_topk(const float* __restrict__ l, int E, int k, int route, int lane,
+                                          int32_t* ids, float* gates, float* gap) {
+  uint32_t taken = 0;
+  float sel_v[MOE_MAX_TOPK];
+  int sel_e[MOE_MAX_TOPK];
+  float next_v = -INFINITY;
+  const int rounds = k < E ? k + 1 : k;
+  for (int r = 0; r < rounds; ++r) {
+    float bv = -INFINITY;
+    int be = INT_MAX;
+    int i = 0;
+    for (int e = lane; e < E; e += 32, ++i) {
+      if (taken & (1u << i)) continue;
+      float v = l[e];
+      if (v != v) v = -INFINITY;
+      if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
+      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
+    }
+    if (r < k) {
+      if ((be & 31) == lane) taken |= 1u << (be >> 5);
+      if (r < MOE_MAX_TOPK) { sel_v[r] = bv; sel_e[r] = be; }
+    } else {
+      next_v = bv;
+    }
+  }
+  // gates, renormalised over the k selected
+  float z = 0.0f;
+  float g[MOE_MAX_TOPK];
+#pragma unroll
+  for (int s = 0; s < MOE_MAX_TOPK; ++s) {
+    if (s < k) {
+      g[s] = route == MOE_ROUTE_SOFTMAX ? expf(sel_v[s] - sel_v[0]) : 1.0f / (1.0f + expf(-sel_v[s]));
+      z += g[s];
+    }
+  }
+  if (lane == 0) {
+    const float inv = 1.0f / z;
+#pragma unroll
+    for (int s = 0; s < MOE_MAX_TOPK; ++s)
+      if (s < k) {
+        ids[s] = sel_e[s];
+        gates[s] = g[s] * inv;
+      }
+    if (gap) *gap = k < E ? sel_v[k - 1] - next_v : INFINITY;
+  }
+}
+
+__global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
+                                                   int route, int32_t* __restrict__ ids,
+                                                   float* __restrict__ gates, float* __restrict__ gap) {
+  const int lane = threadIdx.x & 31;
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t >= T) return;
+  warp_topk(logits + (int64_t)t * E, E, k, route, lane, ids + (int64_t)t * k, gates + (int64_t)t * k,
+            gap ? gap + t : nullptr);
+}
+
+// ---------------------------------------------------------------- scans
+// Exclusive scan in place of n <= 2*blockDim ints in shared memory; returns
+// the total.  Called by every thread of the block (blockDim a multiple of 32).
+__device__ int block_exclusive_scan(int* a, int n) {
+  __shared__ int wsum[32];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+  const int i0 = 2 * tid, i1 = 2 * tid + 1;
+  const int v0 = i0 < n ? a[i0] : 0, v1 = i1 < n ? a[i1] : 0;
+  const int s = v0 + v1;
+  int x = s;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) wsum[warp] = x;
+  __syncthreads();
+  if (warp == 0) {
+    int v = lane < nw ? wsum[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      if (lane >= o) v += y;
+    }
+    wsum[lane] = v;
+  }
+  __syncthreads();
+  const int excl = x - s + (warp > 0 ? wsum[warp - 1] : 0);
+  const int total = wsum[nw - 1];
+  if (i0 < n) a[i0] = excl;
+  if (i1 < n) a[i1] = excl + v0;
+  __syncthreads();
+  return total;
+}
+
+// Tile plan from counts/offsets: each expert with count c gets ceil(c/TT)
+// tiles of up to TT rows, experts in ascending order.  Also zeroes the
+// requant arrival counters of every tile.  All threads of the block call it;
+// `scratch` holds >= EpS ints of shared memory.
+__device__ void build_tiles(const int32_t* counts, const int32_t* offsets, int EpS,
+                            const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles, int32_t* n_tiles,
+                            int32_t* req_cnt, int* scratch) {
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) scratch[e] = (counts[e] + TT - 1) / TT;
+  __syncthreads();
+  const int total = block_exclusive_scan(scratch, EpS);
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) {
+    const int c = counts[e];
+    if (c == 0) continue;
+    const int flag = (table && table[e].gate == nullptr) ? 1 : 0;
+    int ti = scratch[e];
+    for (int st = 0; st < c; st += TT, ++ti) {
+      Tile tl;
+      tl.expert = e;
+      tl.start = offsets[e] + st;
+      tl.count = min(TT, c - st);
+      tl.flag = flag;
+      tiles[ti] = tl;
+    }
+  }
+  for (int i = threadIdx.x; i < total * nIB; i += blockDim.x) req_cnt[i] = 0;
+  if (threadIdx.x == 0) *n_tiles = total;
+}
+
+// ---------------------------------------------------------------- small path
+// One CTA of 1024 threads: top-k of T tokens (one warp each), bucketing of
+// the T*k <= kSmallPairs pairs, and the tile plan.
+__global__ void __launch_bounds__(1024) route_bucket_small_kernel(
+    const float* __restrict__ logits, int T, int E, int k, int route, int S, int32_t* ids,
+    float* gates, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+    const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles, int32_t* n_tiles, int32_t* req_cnt,
+    int* status) {
+  __shared__ int s_ids[kSmallPairs];
+  __shared__ int s_cnt[MOE_MAX_EXPERTS + MOE_MAX_SHARED + 1];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int P = T * k, EpS = E + S;
+  if (logits) {
+    for (int t = warp; t < T; t += blockDim.x >> 5)
+      warp_topk(logits + (int64_t)t * E, E, k, route, lane, ids + t * k, gates + t * k, gap ? gap + t : nullptr);
+    __syncthreads();
+    __threadfence_block();
+  }
+  for (int e = tid; e < EpS; e += blockDim.x) s_cnt[e] = 0;
+  for (int p = tid; p < P; p += blockDim.x) {
+    int e = ids[p];
+    if (e < 0 || e >= E) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      e = -1;
+    }
+    s_ids[p] = e;
+  }
+  __syncthreads();
+  for (int p = tid; p < P; p += blockDim.x)
+    if (s_ids[p] >= 0) atomicAdd(&s_cnt[s_ids[p]], 1);
+  for (int sh = tid; sh < S; sh += blockDim.x) s_cnt[E + sh] = T;
+  __syncthreads();
+  for (int e = tid; e < EpS; e += blockDim.x) counts[e] = s_cnt[e];
+  __syncthreads();
+  const int total = block_exclusive_scan(s_cnt, EpS);   // s_cnt now holds offsets
+  for (int e = tid; e < EpS; e += blockDim.x) offsets[e] = s_cnt[e];
+  if (tid == 0) offsets[EpS] = total;
+  // stable positions: rank of p among earlier pairs of the same expert
+  for (int p = tid; p < P; p += blockDim.x) {
+    const int e = s_ids[p];
+    if (e < 0) continue;
+    int rank = 0;
+    for (int q = 0; q < p; ++q) rank += (s_ids[q] == e);
+    const int pos = s_cnt[e] + rank;
+    perm[pos] = p;
+    if (inv) inv[p] = pos;
+  }
+  for (int i = tid; i < S * T; i += blockDim.x) {
+    const int sh = i / T, t = i % T;
+    const int pos = s_cnt[E + sh] + t;
+    const int p = P + sh * T + t;
+    perm[pos] = p;
+    if (inv) inv[p] = pos;
+  }
+  __syncthreads();
+  __threadfence_block();
+  if (tiles) build_tiles(counts, offsets, EpS, table, TT, nIB, tiles, n_tiles, req_cnt, s_cnt);
+}
+
+// ---------------------------------------------------------------- large path
+__global__ void __launch_bounds__(1024) bucket_count_kernel(const int32_t* __restrict__ ids, int P, int E,
+                                                            int EpS, int32_t* __restrict__ chunk_cnt,
+                                                            int* status) {
+  __shared__ int hist[MOE_MAX_EXPERTS + MOE_MAX_SHARED];
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) hist[e] = 0;
+  __syncthreads();
+  const int p = blockIdx.x * kBucketChunk + threadIdx.x;
+  if (p < P) {
+    const int e = ids[p];
+    if (e >= 0 && e < E)
+      atomicAdd(&hist[e], 1);
+    else
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+  }
+  __syncthreads();
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) chunk_cnt[(int64_t)blockIdx.x * EpS + e] = hist[e];
+}
+
+// chunk_cnt[c][e] -> exclusive base of chunk c within bucket e; counts; offsets
+__global__ void __launch_bounds__(1024) bucket_scan_kernel(int32_t* __restrict__ chunk_cnt, int n_chunks,
+                                                           int T, int E, int S, int32_t* counts,
+                                                           int32_t* offsets) {
+  __shared__ int s_cnt[MOE_MAX_EXPERTS + MOE_MAX_SHARED + 1];
+  const int EpS = E + S;
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) {
+    int run = 0;
+    if (e < E) {
+      for (int c = 0; c < n_chunks; ++c) {
+        const int v = chunk_cnt[(int64_t)c * EpS + e];
+        chunk_cnt[(int64_t)c * EpS + e] = run;
+        run += v;
+      }
+    } else {
+      run = T;
+    }
+    s_cnt[e] = run;
+    counts[e] = run;
+  }
+  __syncthreads();
+  const int total = block_exclusive_scan(s_cnt, EpS);
+  for (int e = threadIdx.x; e < EpS; e += blockDim.x) offsets[e] = s_cnt[e];
+  if (threadIdx.x == 0) offsets[EpS] = total;
+}
+
+__global__ void __launch_bounds__(1024) bucket_scatter_kernel(const int32_t* __restrict__ ids, int T, int k,
+                                                              int E, int S, const int32_t* __restrict__ chunk_cnt,
+                                                              const int32_t* __restrict__ offsets,
+                                                              int32_t* __restrict__ perm, int32_t* inv) {
+  __shared__ int s_ids[kBucketChunk];
+  const int P = T * k, EpS = E + S;
+  const int base = blockIdx.x * kBucketChunk;
+  const int n = min(kBucketChunk, P - base);
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = ids[base + i];
+    s_ids[i] = (e >= 0 && e < E) ? e : -1;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int e = s_ids[i];
+    if (e < 0) continue;
+    int rank = 0;
+    for (int q = 0; q < i; ++q) rank += (s_ids[q] == e);
+    const int pos = offsets[e] + chunk_cnt[(int64_t)blockIdx.x * EpS + e] + rank;
+    perm[pos] = base + i;
+    if (inv) inv[base + i] = pos;
+  }
+  if (blockIdx.x == 0) {
+    for (int i = threadIdx.x; i < S * T; i += blockDim.x) {
+      const int sh = i / T, t = i % T;
+      const int pos = offsets[E + sh] + t;
+      perm[pos] = P + sh * T + t;
+      if (inv) inv[P + sh * T + t] = pos;
+    }
+  }
+}
+
+__global__ void __launch_bounds__(1024) plan_kernel(const int32_t* counts, const int32_t* offsets, int EpS,
+                                                    const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles,
+                                                    int32_t* n_tiles, int32_t* req_cnt) {
+  __shared__ int scratch[MOE_MAX_EXPERTS + MOE_MAX_SHARED + 1];
+  build_tiles(counts, offsets, EpS, table, TT, nIB, tiles, n_tiles, req_cnt, scratch);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- launchers
+cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bs,
+                                cudaStream_t s) {
+  const int64_t nblocks = T * (K / 256);
+  if (nblocks == 0) return cudaSuccess;
+  const int per = 8;  // warps (blocks of 256 elements) per CTA
+  q8k_quantize_kernel<<<(unsigned)((nblocks + per - 1) / per), 32 * per, 0, s>>>(x, nblocks, q, d, bs);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_router(const float* x, const float* w, const float* bias, int T, int H, int E, float* logits,
+                          cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  const int warps = 2;                       // rows per CTA: spread the rows over many SMs
+  int grid = (E + warps - 1) / warps;
+  router_kernel<<<grid, 32 * warps, 0, s>>>(x, w, bias, T, H, E, logits);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_topk(const float* logits, int T, int E, int k, int route, int32_t* ids, float* gates,
+                        float* gap, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  topk_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, T, E, k, route, ids, gates, gap);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_bucket_small(const float* logits, int T, int E, int k, int route, int S, int32_t* ids,
+                                      float* gates, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
+                                      int32_t* inv, const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles,
+                                      int32_t* n_tiles, int32_t* req_cnt, int* status, cudaStream_t s) {
+  route_bucket_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, route, S, ids, gates, gap, counts, offsets, perm,
+                                                inv, table, TT, nIB, tiles, n_tiles, req_cnt, status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_bucket_large(const int32_t* ids, int T, int k, int E, int S, int32_t* counts, int32_t* offsets,
+                                int32_t* perm, int32_t* inv, int32_t* chunk_cnt, int* status, cudaStream_t s) {
+  const int P = T * k;
+  const int n_chunks = (P + kBucketChunk - 1) / kBucketChunk;
+  if (n_chunks > 0) {
+    bucket_count_kernel<<<n_chunks, 1024, 0, s>>>(ids, P, E, E + S, chunk_cnt, status);
+    cudaError_t err = cudaGetLastError();
+    if (err != cudaSuccess) return err;
+  }
+  bucket_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, n_chunks, T, E, S, counts, offsets);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  bucket_scatter_kernel<<<n_chunks > 0 ? n_chunks : 1, 1024, 0, s>>>(ids, T, k, E, S, chunk_cnt, offsets, perm,
+                                                                     inv);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int EpS, const moe_expert_ptrs* table,
+                        int TT, int nIB, Tile* tiles, int32_t* n_tiles, int32_t* req_cnt, cudaStream_t s) {
+  plan_kernel<<<1, 1024, 0, s>>>(counts, offsets, EpS, table, TT, nIB, tiles, n_tiles, req_cnt);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

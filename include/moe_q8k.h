@@ -1,0 +1,231 @@
+/*
+ * moe_q8k.h — C ABI of the block-quantized routed MoE layer for GB300 (sm_103a).
+ *
+ * The operation is the per-token Mixture-of-Experts layer of the SSD/RAM-tiered
+ * MoE engines described on the Pulsar README and the Strata pages: a router
+ * chooses top-k experts per token (softmax or sigmoid gates renormalised over
+ * the k), tokens are bucketed by expert, every selected expert and the shared
+ * expert run gate/up matrix-vector products on q8_K-quantized activations
+ * against block-quantized weights (integer sub-block dot products), a SwiGLU,
+ * and the down projection on the re-quantized intermediate, and the outputs
+ * are combined with the gates into the residual.
+ *
+ * Conventions for every entry point:
+ *  - Pointers are DEVICE pointers owned by the caller unless stated otherwise.
+ *    Every call is asynchronous on `stream` (a cudaStream_t passed as void*;
+ *    NULL = the legacy default stream) and allocates no memory.
+ *  - Arguments are validated on the host before anything is launched; a bad
+ *    argument returns a negative status and launches nothing.  Errors found
+ *    on the device (an out-of-range expert id, a bounded wait that ran out)
+ *    are recorded in the workspace status word and read with moe_get_status.
+ *  - Calls are reentrant for distinct workspaces; calls sharing a workspace
+ *    must be ordered on one stream.
+ *  - Results are deterministic: no floating-point atomics; every sum is taken
+ *    in a fixed order.
+ *
+ * Matrix byte format (both formats): W[N, K] with N, K multiples of 256 is a
+ * sequence of "slabs", one per (row group of 32 rows, 256-column super-block),
+ * row-group-major.  A slab holds the super-blocks of its 32 rows field by
+ * field: 32 x {fp16 d, fp16 dmin} words, then the 32 scale/min records, then
+ * the code lines (16 bytes per row per line).  Full bit-level description:
+ * synth/layout.py.  Q4_K-style: 144 bytes per super-block, 4-bit codes,
+ * eight 32-weight sub-blocks with 6-bit scale and min.  Q2_K-style: 84 bytes
+ * per super-block, 2-bit codes, sixteen 16-weight sub-blocks with 4-bit scale
+ * and min.  weight = d * scale_j * q - dmin * min_j.  Every matrix pointer
+ * must be 16-byte aligned.
+ */
+#ifndef MOE_Q8K_H
+#define MOE_Q8K_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define MOE_OK 0
+#define MOE_ERR_INVALID_ARG (-1)    /* NULL or misaligned pointer, bad size  */
+#define MOE_ERR_UNSUPPORTED (-2)    /* shape outside the supported range     */
+#define MOE_ERR_WORKSPACE (-3)      /* workspace too small                   */
+#define MOE_ERR_CUDA (-4)           /* a CUDA launch or API call failed      */
+#define MOE_ERR_DEVICE_BOUNDS (-5)  /* device saw an out-of-range index      */
+#define MOE_ERR_DEVICE_TIMEOUT (-6) /* a bounded device wait ran out         */
+
+/* ---- limits ------------------------------------------------------------ */
+#define MOE_MAX_EXPERTS 1024 /* E                                          */
+#define MOE_MAX_SHARED 2     /* n_shared                                   */
+#define MOE_MAX_TOPK 16      /* top_k                                      */
+#define MOE_MAX_DIM 16384    /* H and I                                    */
+
+typedef enum { MOE_FMT_Q4K = 0, MOE_FMT_Q2K = 1 } moe_wfmt;
+typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID = 1 } moe_route_kind;
+
+/* Shape of one MoE layer. */
+typedef struct {
+  int32_t H;        /* hidden size, multiple of 256, <= MOE_MAX_DIM            */
+  int32_t I;        /* expert intermediate size, multiple of 256               */
+  int32_t E;        /* routed experts, 1..MOE_MAX_EXPERTS                      */
+  int32_t top_k;    /* experts per token, 1..min(E, MOE_MAX_TOPK)              */
+  int32_t n_shared; /* always-on shared experts, 0..MOE_MAX_SHARED             */
+  int32_t route;    /* moe_route_kind                                          */
+  int32_t fmt;      /* moe_wfmt of every expert matrix                         */
+  int32_t T_max;    /* largest token count of a call (sizes the workspace)     */
+} moe_layer_desc;
+
+/* One expert's matrices: gate [I, H], up [I, H], down [H, I].  In a pointer
+ * table a NULL gate means "not mine": the expert is not present and
+ * contributes nothing (Pulsar README, "How the streaming works": explicit
+ * per-(token, slot) gate/up/down pointers, NULL = not mine). */
+typedef struct {
+  const void* gate;
+  const void* up;
+  const void* down;
+} moe_expert_ptrs;
+
+/* Byte offsets of the intermediate results inside a moe_layer_forward
+ * workspace (for inspection after the call; all 256-byte aligned).
+ * P = T_max * (top_k + n_shared) is the number of (token, slot) rows. */
+typedef struct {
+  size_t status;   /* int32[4]: [0] = device status word                       */
+  size_t xq;       /* int8  [T_max, H]      q8_K codes of x                    */
+  size_t xd;       /* float [T_max, H/256]  q8_K scales of x                   */
+  size_t xbs;      /* int16 [T_max, H/16]   sums of 16 codes                   */
+  size_t logits;   /* float [T_max, E]                                         */
+  size_t ids;      /* int32 [T_max, top_k]                                     */
+  size_t gates;    /* float [T_max, top_k]                                     */
+  size_t gap;      /* float [T_max]  l_(k) - l_(k+1)                           */
+  size_t counts;   /* int32 [E + n_shared]                                     */
+  size_t offsets;  /* int32 [E + n_shared + 1]                                 */
+  size_t perm;     /* int32 [P]  bucket position -> slot index                 */
+  size_t inv;      /* int32 [P]  slot index -> bucket position                 */
+  size_t h;        /* float [P, I]     silu(G) * U, rows in bucket order       */
+  size_t hq;       /* int8  [P, I]     q8_K codes of h                         */
+  size_t hd;       /* float [P, I/256]                                         */
+  size_t hbs;      /* int16 [P, I/16]                                          */
+  size_t y;        /* float [P, H]     expert outputs, indexed by slot index   */
+  size_t total;    /* bytes required                                           */
+} moe_ws_layout;
+
+/* Workspace bytes moe_layer_forward needs for `desc` (0 if desc is invalid). */
+size_t moe_layer_workspace_size(const moe_layer_desc* desc);
+
+/* Offsets of the intermediates in that workspace.  Returns MOE_OK or
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED. */
+int moe_workspace_layout(const moe_layer_desc* desc, moe_ws_layout* out);
+
+/* q8_K quantization of x[T, K] (fp32, row-major, K a multiple of 256):
+ * per 256-element block d = max|x| / 127 (IEEE fp32 division) and
+ * q = round-half-away-from-zero(x / d) (IEEE fp32 division), q = 0 when
+ * d = 0; bsum16 = sums of each 16 consecutive codes.
+ * Outputs q int8 [T, K], d float [T, K/256], bsum16 int16 [T, K/16]
+ * (bsum16 may be NULL).  Source: Pulsar README, "Fidelity notes" (all
+ * matmuls run on q8_0/q8_K activations with integer dp4a dots). */
+int moe_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bsum16,
+                     void* stream);
+
+/* Router and top-k.  logits[t, e] = sum_h w_router[e, h] * x[t, h] + bias[e]
+ * in fp32 from the unquantized fp32 x [T, H]; w_router fp32 [E, H]; bias fp32
+ * [E] or NULL.  The k largest logits are selected (equal logits: lower expert
+ * index first) into ids int32 [T, k] in descending order; gates float [T, k]:
+ * route 0 softmax over the k selected logits, route 1 sigmoid of each
+ * selected logit divided by their sum.  gap float [T] (nullable) =
+ * l_(k) - l_(k+1), +inf when k == E.  logits float [T, E] is an output the
+ * caller provides.  Sources: Pulsar README, "What it does today" (softmax
+ * router, qwen3moe); Pulsar digest note, section 1 (512-way sigmoid-gated
+ * router + shared expert); Strata summary (~10 experts per token). */
+int moe_route_topk(const float* x, const float* w_router, const float* bias, int32_t T, int32_t H,
+                   int32_t E, int32_t k, int32_t route, float* logits, int32_t* ids, float* gates,
+                   float* gap, void* stream);
+
+/* Workspace bytes moe_bucket needs for T tokens, k slots, E experts. */
+size_t moe_bucket_workspace_size(int32_t T, int32_t k, int32_t E, int32_t n_shared);
+
+/* Bucketing of the T*k (token, slot) pairs by expert (a counting sort, stable
+ * by token) plus one bucket per shared expert holding every token.
+ *   counts  int32 [E + n_shared]
+ *   offsets int32 [E + n_shared + 1] (exclusive prefix sum of counts)
+ *   perm    int32 [T*(k + n_shared)]: perm[offsets[e] + i] is the slot index of
+ *           the i-th pair of bucket e; slot index = t*k + s for routed pairs and
+ *           T*k + sh*T + t for shared expert sh.
+ *   inv     int32 [T*(k + n_shared)] (nullable): inv[perm[j]] = j.
+ * ids outside [0, E) are recorded as MOE_ERR_DEVICE_BOUNDS in the status word
+ * of ws and skipped.  Source: Pulsar README, "How the streaming works" (per
+ * prefill chunk, one expert union across the whole batch). */
+int moe_bucket(const int32_t* ids, int32_t T, int32_t k, int32_t E, int32_t n_shared,
+               int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, void* ws,
+               size_t ws_bytes, void* stream);
+
+/* Workspace bytes moe_expert_ffn needs for `desc` with T tokens. */
+size_t moe_expert_ffn_workspace_size(const moe_layer_desc* desc, int32_t T);
+
+/* Expert FFNs over the buckets.  For every expert e with a non-NULL gate in
+ * `table` (device array of E + n_shared entries) and every slot row j of its
+ * bucket (token t of slot perm[j]):
+ *   G = gate_e . q8_K(x_t),  U = up_e . q8_K(x_t)   (integer sub-block dots)
+ *   h = silu(G) * U  (fp32),  y_slots[perm[j]] = down_e . q8_K(h)
+ * Rows of experts whose gate is NULL are written as zeros.  Each expert's
+ * weights are read once for all the tokens of its bucket (per group of up to
+ * 16 tokens).  q/d/bsum16: q8_K of x as moe_q8k_quantize writes them (T rows
+ * of H).  counts/offsets/perm: as moe_bucket writes them.  y_slots float
+ * [T*(k + n_shared), H] indexed by slot index.  Sources: Pulsar README, "What
+ * it does today" (warp-cooperative Q4_K/Q6_K matmuls on q8_K activations,
+ * FFN triple gate/up/down) and "How the streaming works". */
+int moe_expert_ffn(const moe_layer_desc* desc, const moe_expert_ptrs* table, const int8_t* q,
+                   const float* d, const int16_t* bsum16, const int32_t* counts,
+                   const int32_t* offsets, const int32_t* perm, int32_t T, float* y_slots,
+                   void* ws, size_t ws_bytes, void* stream);
+
+/* Gate-weighted combine into the residual, in a fixed order:
+ *   out[t] = (sum_{s<k} gates[t, s] * y_slots[t*k + s] + sum_sh y_slots[T*k + sh*T + t])
+ *            + residual[t]
+ * residual float [T, H] may be NULL (treated as 0) and may alias out.
+ * Source: Pulsar README, "Fidelity notes" (the per-slot sum). */
+int moe_combine(const float* y_slots, const float* gates, int32_t T, int32_t H, int32_t k,
+                int32_t n_shared, const float* residual, float* out, void* stream);
+
+/* The whole layer: q8_K(x), router top-k, bucketing, expert FFNs and the
+ * combine, on T <= desc->T_max tokens.  x float [T, H]; w_router float [E, H];
+ * router_bias float [E] or NULL; residual float [T, H] or NULL (may alias
+ * out); out float [T, H]; table: device array of E + n_shared expert pointer
+ * records.  ids_out int32 [T, k] and gates_out float [T, k] are optional
+ * copies of the routing (NULL to skip).  ws: at least
+ * moe_layer_workspace_size(desc) bytes, 256-byte aligned; the intermediates
+ * stay in it after the call at the offsets moe_workspace_layout gives. */
+int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table,
+                      const float* w_router, const float* router_bias, const float* x,
+                      const float* residual, float* out, int32_t T, int32_t* ids_out,
+                      float* gates_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronizes `stream`, then reads and clears the status word of a
+ * workspace written by moe_layer_forward, moe_bucket or moe_expert_ffn.
+ * Returns MOE_OK, a device-recorded error, or MOE_ERR_CUDA. */
+int moe_get_status(void* ws, void* stream);
+
+/* Human-readable name of a status code (static string). */
+const char* moe_status_string(int status);
+
+/* Profiling hook.  While set, every expert-FFN launch sequence issued by this
+ * host thread (moe_layer_forward, moe_expert_ffn) records the next four
+ * unused entries of `events` (cudaEvent_t handles created by the caller with
+ * timing enabled) on its stream: immediately before and after the gate/up
+ * kernel, and immediately before and after the down kernel.  Records use
+ * cudaEventRecordExternal, so they also work inside stream capture.  When
+ * the array is used up, recording stops.  events = NULL or n_events = 0
+ * turns the hook off.  Returns MOE_OK or MOE_ERR_INVALID_ARG. */
+int moe_trace_events(void* const* events, int32_t n_events);
+
+/* Test hook: the integer sub-block sums of the device dot routine that the
+ * expert kernels use, for matrix w [N, K] against q8_K codes q [T, K]:
+ *   isum int32 [T, N, K/256, n_sub] = sum over sub-block j of q_w * q_a,
+ *   bsum int32 [T, K/256, n_sub]    = sum over sub-block j of q_a,
+ * n_sub = 8 (Q4_K-style) or 16 (Q2_K-style).  T <= 16. */
+int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q,
+                            int32_t T, int32_t* isum, int32_t* bsum, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_Q8K_H */

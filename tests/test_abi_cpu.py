@@ -1,0 +1,105 @@
+"""The C-ABI library on the CPU: it builds, loads, exports every function the
+header declares, sizes workspaces, and rejects bad arguments on the host
+before any GPU work (no compute call is made here)."""
+import ctypes
+
+import pytest
+
+import block_quantized_routed_gb300 as moe
+from block_quantized_routed_gb300 import _build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return moe.load()
+
+
+def desc(**kw):
+    d = dict(H=2048, I=512, E=256, top_k=8, n_shared=1, route=0, fmt=0, T_max=1)
+    d.update(kw)
+    return moe.LayerDesc(**d)
+
+
+def test_every_declared_function_is_exported(lib):
+    names = _build.header_functions()
+    assert len(names) >= 13
+    for n in ["moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_expert_ffn", "moe_combine",
+              "moe_layer_forward"]:
+        assert n in names
+    raw = ctypes.CDLL(_build.LIB)
+    for n in names:
+        assert hasattr(raw, n), n
+
+
+def test_status_strings(lib):
+    assert moe.moe_status_string(0) == "ok"
+    assert "workspace" in moe.moe_status_string(moe.MOE_ERR_WORKSPACE)
+    assert moe.moe_status_string(12345) == "unknown status"
+
+
+@pytest.mark.parametrize("bad", [dict(H=500), dict(I=0), dict(E=0), dict(E=2000), dict(top_k=0), dict(top_k=17),
+                                 dict(E=4, top_k=5), dict(n_shared=3), dict(route=2), dict(fmt=5), dict(T_max=0),
+                                 dict(H=16640)])
+def test_invalid_descriptors(lib, bad):
+    d = desc(**bad)
+    assert moe.moe_layer_workspace_size(d) == 0
+    with pytest.raises(moe.MoeError):
+        moe.moe_workspace_layout(d)
+
+
+def test_workspace_layout_regions(lib):
+    for d in [desc(), desc(H=4096, I=1024, E=512, top_k=10, T_max=8192, fmt=1, route=1),
+              desc(H=512, I=256, E=16, top_k=2, n_shared=0, T_max=4)]:
+        total = moe.moe_layer_workspace_size(d)
+        lay = moe.moe_workspace_layout(d)
+        assert lay.total == total > 0
+        T, H, I, E, k, S = d.T_max, d.H, d.I, d.E, d.top_k, d.n_shared
+        P = T * (k + S)
+        sizes = dict(status=16, xq=T * H, xd=T * H // 256 * 4, xbs=T * H // 16 * 2, logits=T * E * 4,
+                     ids=T * k * 4, gates=T * k * 4, gap=T * 4, counts=(E + S) * 4, offsets=(E + S + 1) * 4,
+                     perm=P * 4, inv=P * 4, h=P * I * 4, hq=P * I, hd=P * I // 256 * 4, hbs=P * I // 16 * 2,
+                     y=P * H * 4)
+        spans = sorted((getattr(lay, n), getattr(lay, n) + s, n) for n, s in sizes.items())
+        for (a0, a1, n0), (b0, b1, n1) in zip(spans, spans[1:]):
+            assert a1 <= b0, (n0, n1)
+        for a0, a1, n in spans:
+            assert a0 % 256 == 0 and a1 <= total
+    assert moe.moe_layer_workspace_size(desc(T_max=16)) > moe.moe_layer_workspace_size(desc(T_max=1))
+
+
+def test_host_validation_rejects_before_launch(lib):
+    L = moe.load()
+    d = desc(T_max=4)
+    fake = ctypes.c_void_p(0x10000)     # never dereferenced: validation fails first
+    # T > T_max
+    rc = L.moe_layer_forward(ctypes.byref(d), fake, fake, None, fake, None, fake, 5, None, None, fake, 1 << 40, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # NULL x
+    rc = L.moe_layer_forward(ctypes.byref(d), fake, fake, None, None, None, fake, 1, None, None, fake, 1 << 40, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # workspace too small
+    rc = L.moe_layer_forward(ctypes.byref(d), fake, fake, None, fake, None, fake, 1, None, None, fake, 1024, None)
+    assert rc == moe.MOE_ERR_WORKSPACE
+    # misaligned x
+    rc = L.moe_layer_forward(ctypes.byref(d), fake, fake, None, ctypes.c_void_p(0x10004), None, fake, 1, None, None,
+                             fake, 1 << 40, None)
+    assert rc == moe.MOE_ERR_INVALID_ARG
+    # unsupported shape
+    bad = desc(H=300)
+    rc = L.moe_layer_forward(ctypes.byref(bad), fake, fake, None, fake, None, fake, 1, None, None, fake, 1 << 40, None)
+    assert rc == moe.MOE_ERR_UNSUPPORTED
+    # T == 0 is a no-op
+    rc = L.moe_layer_forward(ctypes.byref(d), None, None, None, None, None, None, 0, None, None, None, 0, None)
+    assert rc == moe.MOE_OK
+    assert L.moe_q8k_quantize(fake, 2, 300, fake, fake, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_q8k_quantize(fake, 0, 256, fake, fake, None, None) == moe.MOE_OK
+    assert L.moe_route_topk(fake, fake, None, 1, 256, 8, 9, 0, fake, fake, fake, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_route_topk(fake, fake, None, 1, 256, 8, 2, 7, fake, fake, fake, None, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_bucket(fake, 4, 2, 8, 0, fake, fake, fake, None, fake, 8, None) == moe.MOE_ERR_WORKSPACE
+    assert L.moe_bucket(fake, 4, 2, 4096, 0, fake, fake, fake, None, fake, 1 << 20, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_combine(fake, fake, 1, 258, 2, 0, None, fake, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_debug_subblock_dots(0, fake, 256, 256, fake, 17, fake, fake, None) == moe.MOE_ERR_UNSUPPORTED
+    assert L.moe_get_status(None, None) == moe.MOE_ERR_INVALID_ARG
+    assert moe.moe_bucket_workspace_size(8192, 10, 512, 1) >= 80 * 513 * 4
+    assert moe.moe_expert_ffn_workspace_size(d, 5) == 0

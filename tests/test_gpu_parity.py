@@ -1,0 +1,306 @@
+"""GPU parity of every step of the layer against the oracle, through the C ABI.
+
+Integer results are compared bit for bit: q8_K codes/scales/16-sums, the
+integer sub-block dot sums of the device dot routine, expert ids (away from
+near-ties), bucket counts/offsets/permutation.  Floating-point results use
+the per-row tolerance of tests/gpu_util.py.  Sizes span several 32-row
+groups, several 256-column blocks and ragged token counts."""
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from synth.layout import FMT_Q4K, FMT_Q2K
+from tests import fieldpack
+from tests.gpu_util import assert_close_rows, routing_ok, to_dev
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe():
+    import block_quantized_routed_gb300 as m
+    m.load()
+    return m
+
+
+def dev(a):
+    return to_dev(a, torch)
+
+
+# ------------------------------------------------------------------ q8_K
+
+@pytest.mark.parametrize("T,K", [(1, 256), (4, 512), (13, 2048), (64, 6144)])
+def test_q8k_quantize_bit_exact(moe, T, K):
+    rng = np.random.default_rng(T * K)
+    x = (rng.standard_normal((T, K)) * rng.uniform(1e-3, 1e2, (T, 1))).astype(np.float32)
+    x[0, :256] = 0.0                                     # all-zero block
+    if T > 2:
+        x[1, :256] = np.round(x[1, :256] * 2) / 2        # many exact .5 ratios
+        x[2, 5] = 1e-42                                  # subnormal inside a block
+    q = torch.empty((T, K), dtype=torch.int8, device="cuda")
+    d = torch.empty((T, K // 256), dtype=torch.float32, device="cuda")
+    bs = torch.empty((T, K // 16), dtype=torch.int16, device="cuda")
+    moe.moe_q8k_quantize(dev(x), q, d, bs)
+    rq, rd, rbs = oracle.q8k_quantize(x)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(d.cpu().numpy().view(np.uint32), rd.view(np.uint32))
+    np.testing.assert_array_equal(bs.cpu().numpy(), rbs)
+
+
+def test_q8k_golden_blocks(moe):
+    import json, os
+    cases = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "q8k_blocks.json")))["cases"]
+    x = np.zeros((len(cases), 256), np.float32)
+    for i, c in enumerate(cases):
+        for k, v in c["x"].items():
+            x[i, int(k)] = v
+    q = torch.empty((len(cases), 256), dtype=torch.int8, device="cuda")
+    d = torch.empty((len(cases), 1), dtype=torch.float32, device="cuda")
+    bs = torch.empty((len(cases), 16), dtype=torch.int16, device="cuda")
+    moe.moe_q8k_quantize(dev(x), q, d, bs)
+    q, d, bs = q.cpu().numpy(), d.cpu().numpy(), bs.cpu().numpy()
+    for i, c in enumerate(cases):
+        want = np.zeros(256, np.int8)
+        for k, v in c["q"].items():
+            want[int(k)] = v
+        np.testing.assert_array_equal(q[i], want)
+        assert d[i, 0] == np.float32(c["d"])
+        np.testing.assert_array_equal(bs[i], c["bsum16"])
+
+
+# ------------------------------------------------------------------ integer dots
+
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("N,K,T", [(256, 256, 1), (512, 1024, 3), (256, 2048, 16)])
+def test_subblock_dots_bit_exact(moe, fmt, N, K, T):
+    w = synth.gen_matrix(fmt, N, K, 5, 0, 1, 0)
+    x = synth.activations(T, K, 5)
+    xq, _, _ = oracle.q8k_quantize(x)
+    ns = 8 if fmt == FMT_Q4K else 16
+    isum = torch.empty((T, N, K // 256, ns), dtype=torch.int32, device="cuda")
+    bsum = torch.empty((T, K // 256, ns), dtype=torch.int32, device="cuda")
+    moe.moe_debug_subblock_dots(fmt, dev(w), N, K, dev(xq), isum, bsum)
+    risum, rbsum = oracle.subblock_dots(w, fmt, N, K, xq)
+    np.testing.assert_array_equal(isum.cpu().numpy(), risum)
+    np.testing.assert_array_equal(bsum.cpu().numpy(), rbsum)
+
+
+def test_subblock_dots_extreme_codes(moe):
+    """q_w = 15 with scale 63 against q_a = -127 everywhere: the largest sums."""
+    fmt, N, K = FMT_Q4K, 256, 512
+    q = np.full((N, 2, 256), 15)
+    sc = np.full((N, 2, 8), 63)
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, sc, np.ones((N, 2), np.float16), np.ones((N, 2), np.float16))
+    xq = np.full((2, K), -127, np.int8)
+    isum = torch.empty((2, N, 2, 8), dtype=torch.int32, device="cuda")
+    bsum = torch.empty((2, 2, 8), dtype=torch.int32, device="cuda")
+    moe.moe_debug_subblock_dots(fmt, dev(w), N, K, dev(xq), isum, bsum)
+    assert (isum.cpu().numpy() == 32 * 15 * -127).all()
+    assert (bsum.cpu().numpy() == 32 * -127).all()
+
+
+# ------------------------------------------------------------------ routing
+
+@pytest.mark.parametrize("route", [0, 1])
+@pytest.mark.parametrize("T,H,E,k,bias", [(1, 2048, 256, 8, False), (4, 4096, 512, 10, False),
+                                          (16, 6144, 192, 8, True), (37, 512, 16, 2, False), (5, 256, 4, 4, False)])
+def test_route_topk(moe, route, T, H, E, k, bias):
+    x = synth.activations(T, H, 11)
+    wr = synth.router_weight(E, H, 11)
+    b = synth.router_bias(E, 2.0, 11) if bias else None
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    gap = torch.empty((T,), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(dev(x), dev(wr), None if b is None else dev(b), k, route, logits, ids, gates, gap)
+    rl, rids, rg, rgap = oracle.route(x, wr, b, k, route)
+    np.testing.assert_allclose(logits.cpu().numpy(), rl, rtol=0, atol=1e-4 * np.abs(rl).max())
+    routing_ok(ids.cpu().numpy(), rids, rgap, rl)
+    # gates against the oracle's gates for the GPU's ids
+    _, _, rg2, _ = oracle.route(x, wr, b, k, route, forced_ids=ids.cpu().numpy())
+    np.testing.assert_allclose(gates.cpu().numpy(), rg2, rtol=1e-5, atol=1e-6)
+    g = gap.cpu().numpy()
+    fin = np.isfinite(rgap)
+    np.testing.assert_allclose(g[fin], rgap[fin], rtol=0, atol=1e-4)
+    assert (np.isinf(g) == ~fin).all()
+
+
+def test_route_ties_pick_lower_index(moe):
+    T, H, E, k = 2, 256, 64, 4
+    x = np.ones((T, H), np.float32)
+    wr = np.zeros((E, H), np.float32)
+    wr[[5, 9, 30, 31, 40], :] = 1.0 / H               # five equal logits of 1.0
+    logits = torch.empty((T, E), dtype=torch.float32, device="cuda")
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(dev(x), dev(wr), None, k, 0, logits, ids, gates)
+    np.testing.assert_array_equal(ids.cpu().numpy(), [[5, 9, 30, 31]] * T)
+    np.testing.assert_allclose(gates.cpu().numpy(), 0.25, rtol=1e-6)
+
+
+# ------------------------------------------------------------------ bucketing
+
+@pytest.mark.parametrize("T,k,E,S", [(1, 8, 256, 1), (4, 10, 512, 1), (16, 8, 192, 0), (3, 2, 3, 1),
+                                     (300, 10, 512, 1), (1000, 8, 64, 0), (8192, 10, 512, 1)])
+def test_bucket_bit_exact(moe, T, k, E, S):
+    rng = np.random.default_rng(T + E)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    counts = torch.empty(E + S, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + S + 1, dtype=torch.int32, device="cuda")
+    perm = torch.empty(T * (k + S), dtype=torch.int32, device="cuda")
+    inv = torch.empty(T * (k + S), dtype=torch.int32, device="cuda")
+    ws = torch.zeros(moe.moe_bucket_workspace_size(T, k, E, S), dtype=torch.uint8, device="cuda")
+    moe.moe_bucket(dev(ids), E, S, counts, offsets, perm, inv, ws)
+    rc, ro, rp = oracle.bucket(ids, E, S)
+    np.testing.assert_array_equal(counts.cpu().numpy(), rc)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), ro)
+    np.testing.assert_array_equal(perm.cpu().numpy(), rp)
+    p = perm.cpu().numpy()
+    np.testing.assert_array_equal(inv.cpu().numpy()[p], np.arange(p.size))
+    assert moe.moe_get_status(ws) == 0
+
+
+def test_bucket_flags_out_of_range_ids(moe):
+    ids = np.array([[0, 1], [2, 7]], np.int32)        # 7 >= E
+    E = 4
+    counts = torch.empty(E, dtype=torch.int32, device="cuda")
+    offsets = torch.empty(E + 1, dtype=torch.int32, device="cuda")
+    perm = torch.zeros(4, dtype=torch.int32, device="cuda")
+    ws = torch.zeros(moe.moe_bucket_workspace_size(2, 2, E, 0), dtype=torch.uint8, device="cuda")
+    moe.moe_bucket(dev(ids), E, 0, counts, offsets, perm, None, ws)
+    assert moe.moe_get_status(ws) == moe.MOE_ERR_DEVICE_BOUNDS
+    assert moe.moe_get_status(ws) == 0                # read-and-clear
+    np.testing.assert_array_equal(counts.cpu().numpy(), [1, 1, 1, 0])
+
+
+# ------------------------------------------------------------------ expert FFN + combine
+
+def _experts_host(fmt, E, H, I, seed, layer=0):
+    return [(synth.gen_matrix(fmt, I, H, seed, layer, e, 0), synth.gen_matrix(fmt, I, H, seed, layer, e, 1),
+             synth.gen_matrix(fmt, H, I, seed, layer, e, 2)) for e in range(E)]
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("T,H,I,E,k,S", [(4, 512, 256, 16, 2, 0), (5, 768, 512, 8, 3, 1), (17, 256, 256, 4, 2, 1)])
+def test_expert_ffn_and_combine(moe, fmt, T, H, I, E, k, S):
+    ex = _experts_host(fmt, E + S, H, I, seed=21)
+    table = moe.expert_table([tuple(dev(m) for m in e) for e in ex])
+    rng = np.random.default_rng(T * H)
+    ids = np.stack([rng.choice(E, k, replace=False) for _ in range(T)]).astype(np.int32)
+    gates = rng.uniform(0.1, 1.0, (T, k)).astype(np.float32)
+    x = synth.activations(T, H, 21)
+    xq, xd, xbs = oracle.q8k_quantize(x)
+    rc, ro, rp = oracle.bucket(ids, E, S)
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=0, fmt=fmt, T_max=T)
+    y = torch.full((T * (k + S), H), float("nan"), dtype=torch.float32, device="cuda")
+    ws = torch.zeros(moe.moe_expert_ffn_workspace_size(desc, T), dtype=torch.uint8, device="cuda")
+    moe.moe_expert_ffn(desc, table, dev(xq), dev(xd), dev(xbs), dev(rc), dev(ro), dev(rp), T, y, ws)
+    yg = y.cpu().numpy()
+    for t in range(T):
+        slots = [(t * k + s, ids[t, s]) for s in range(k)] + [(T * k + sh * T + t, E + sh) for sh in range(S)]
+        for p, e in slots:
+            ref = oracle.expert_ffn(*ex[e], fmt, H, I, xq[t:t + 1], xd[t:t + 1])
+            assert_close_rows(yg[p:p + 1], ref, f"y slot {p} (expert {e})")
+    res = synth.normal_f32((T, H), 1.0, 21, synth.TAG_RESIDUAL)
+    out = torch.empty((T, H), dtype=torch.float32, device="cuda")
+    moe.moe_combine(y, dev(gates), T, H, k, S, dev(res), out)
+    want = res.astype(np.float64).copy()
+    for t in range(T):
+        for s in range(k):
+            want[t] += gates[t, s] * yg[t * k + s]
+        for sh in range(S):
+            want[t] += yg[T * k + sh * T + t]
+    np.testing.assert_allclose(out.cpu().numpy(), want, rtol=1e-5, atol=1e-5 * np.abs(want).max())
+
+
+# ------------------------------------------------------------------ whole layer
+
+CASES = [
+    # fmt, route, H, I, E, k, S, T, bias
+    (FMT_Q4K, 0, 512, 256, 16, 2, 0, 4, False),      # the tiny workload
+    (FMT_Q4K, 0, 2048, 512, 64, 8, 1, 1, False),     # decode, shared expert
+    (FMT_Q2K, 1, 1024, 512, 64, 10, 1, 4, False),    # Q2_K, sigmoid, verify window
+    (FMT_Q4K, 0, 768, 512, 32, 8, 0, 16, True),      # skewed router, 16 tokens
+    (FMT_Q2K, 0, 256, 256, 8, 8, 1, 3, False),       # k = E
+    (FMT_Q4K, 1, 256, 768, 1, 1, 0, 7, False),       # one expert
+    (FMT_Q4K, 1, 512, 256, 40, 10, 1, 40, False),    # more than the single-CTA bucket (400 pairs)
+]
+
+
+@pytest.mark.parametrize("case", CASES, ids=lambda c: "fmt%d_r%d_H%d_I%d_E%d_k%d_S%d_T%d" % c[:8])
+def test_layer_forward(moe, case):
+    fmt, route, H, I, E, k, S, T, use_bias = case
+    seed = H + E + T
+    ex = _experts_host(fmt, E + S, H, I, seed)
+    table = moe.expert_table([tuple(dev(m) for m in e) for e in ex])
+    wr = synth.router_weight(E, H, seed)
+    bias = synth.router_bias(E, 2.0, seed) if use_bias else None
+    x = synth.activations(T, H, seed)
+    res = synth.normal_f32((T, H), 1.0, seed, synth.TAG_RESIDUAL)
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    layer = moe.MoeLayer(desc, table, dev(wr), None if bias is None else dev(bias))
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    gates = torch.empty((T, k), dtype=torch.float32, device="cuda")
+    out = layer.forward(dev(x), residual=dev(res), ids_out=ids, gates_out=gates)
+    assert moe.moe_get_status(layer.ws) == 0
+    gids = ids.cpu().numpy()
+    rl, rids, _, rgap = oracle.route(x, wr, bias, k, route)
+    routing_ok(gids, rids, rgap, rl)
+    ref, _, rgates, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex, wr, bias, x, residual=res,
+                                             forced_ids=gids)
+    np.testing.assert_allclose(gates.cpu().numpy(), rgates, rtol=1e-5, atol=1e-6)
+    assert_close_rows(out.cpu().numpy(), ref)
+    # the intermediate h re-quantization, decided in fp32 on both sides
+    P = T * (k + S)
+    h = layer.ws_view("h", torch.float32, (P, I)).cpu().numpy()
+    hq = layer.ws_view("hq", torch.int8, (P, I)).cpu().numpy()
+    hd = layer.ws_view("hd", torch.float32, (P, I // 256)).cpu().numpy()
+    rq, rd, _ = oracle.q8k_quantize(h)
+    np.testing.assert_array_equal(hq, rq)
+    np.testing.assert_array_equal(hd, rd)
+
+
+def test_layer_forward_is_deterministic(moe):
+    fmt, route, H, I, E, k, S, T = FMT_Q4K, 0, 1024, 512, 32, 4, 1, 9
+    ex = _experts_host(fmt, E + S, H, I, 3)
+    table = moe.expert_table([tuple(dev(m) for m in e) for e in ex])
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    layer = moe.MoeLayer(desc, table, dev(synth.router_weight(E, H, 3)))
+    x = dev(synth.activations(T, H, 3))
+    a = layer.forward(x).cpu().numpy()
+    b = layer.forward(x).cpu().numpy()
+    np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_layer_forward_null_expert_is_not_mine(moe):
+    fmt, H, I, E, k, S, T = FMT_Q4K, 512, 256, 8, 2, 1, 6
+    ex = _experts_host(fmt, E + S, H, I, 8)
+    wr = synth.router_weight(E, H, 8)
+    x = synth.activations(T, H, 8)
+    _, rids, _, _ = oracle.route(x, wr, None, k, 0)
+    dead = int(rids[0, 0])
+    dev_ex = [None if e == dead else tuple(dev(m) for m in ex[e]) for e in range(E + S)]
+    host_ex = [None if e == dead else ex[e] for e in range(E + S)]
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=0, fmt=fmt, T_max=T)
+    layer = moe.MoeLayer(desc, moe.expert_table(dev_ex), dev(wr))
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    out = layer.forward(dev(x), ids_out=ids).cpu().numpy()
+    ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, 0, host_ex, wr, None, x, forced_ids=ids.cpu().numpy())
+    assert_close_rows(out, ref)
+
+
+def test_layer_forward_in_place_residual(moe):
+    fmt, H, I, E, k, S, T = FMT_Q2K, 512, 256, 8, 2, 0, 2
+    ex = _experts_host(fmt, E, H, I, 4)
+    wr = synth.router_weight(E, H, 4)
+    x = synth.activations(T, H, 4)
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=0, fmt=fmt, T_max=T)
+    layer = moe.MoeLayer(desc, moe.expert_table([tuple(dev(m) for m in e) for e in ex]), dev(wr))
+    xd = dev(x)
+    ids = torch.empty((T, k), dtype=torch.int32, device="cuda")
+    layer.forward(xd, residual=xd, out=xd, ids_out=ids)
+    ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, 0, ex, wr, None, x, residual=x,
+                                        forced_ids=ids.cpu().numpy())
+    assert_close_rows(xd.cpu().numpy(), ref)
