@@ -86,9 +86,9 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload_name):
-    """dram bytes per launch of the gate/up kernel from a committed ncu summary,
-    if its kernel-source hash matches the current sources (else None)."""
+def profiled_traffic(workload_name, kernel):
+    """dram bytes per launch of `kernel` from a committed ncu summary, if its
+    kernel-source hash matches the current sources (else None)."""
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
@@ -97,10 +97,10 @@ def profiled_traffic(workload_name):
         if not f.endswith(".md"):
             continue
         txt = open(os.path.join(pdir, f)).read()
-        m = re.search(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+workload:\s*(\S+)\s+source_hash:\s*(\w+)",
-                      txt, flags=re.M)
-        if m and m.group(2) == workload_name and m.group(3) == want:
-            return float(m.group(1))
+        for m in re.finditer(r"^traffic_bytes_per_launch:\s*([0-9.eE+]+)\s+kernel:\s*(\S+)\s+workload:\s*(\S+)"
+                             r"\s+source_hash:\s*(\w+)", txt, flags=re.M):
+            if m.group(2) == kernel and m.group(3) == workload_name and m.group(4) == want:
+                return float(m.group(1))
     return None
 
 
@@ -260,47 +260,66 @@ def run_ours(args, wl, T):
     routers = [torch.from_numpy(synth.router_weight(wl.E, H, wl.seed, l)).to(dev) for l in range(L)]
     biases = [torch.from_numpy(synth.router_bias(wl.E, wl.bias_std, wl.seed, l)).to(dev) if wl.bias_std > 0 else None
               for l in range(L)]
-    layers = [moe.MoeLayer(wl.desc(T), bank.table(l), routers[l], biases[l], device=dev) for l in range(L)]
+    tables = [bank.table(l) for l in range(L)]
     x_host = host_inputs(wl, T, R)
     xs = torch.from_numpy(x_host).to(dev)                      # [R, L, T, H]
     x_static = torch.empty((L, T, H), dtype=torch.float32, device=dev)
     out = torch.empty((L, T, H), dtype=torch.float32, device=dev)
     ids_buf = torch.empty((L, T, wl.k), dtype=torch.int32, device=dev)
+    desc = wl.desc(T)
+    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device=dev)
+    rows = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=x_static[l], residual=x_static[l],
+                 out=out[l], ids_out=ids_buf[l]) for l in range(L)]
+    stack = moe.stack_pointer_table(rows, device=dev)
+    # the single-launch stack serves decode shapes; other shapes run layer by layer
+    try:
+        x_static.copy_(xs[0])
+        moe.moe_stack_forward(desc, stack, T, ws)
+        stacked = True
+    except moe.MoeError as err:
+        if err.status != moe.MOE_ERR_UNSUPPORTED:
+            raise
+        stacked = False
+        layers = [moe.MoeLayer(desc, tables[l], routers[l], biases[l], device=dev) for l in range(L)]
     torch.cuda.synchronize()
 
-    def body(record_ids=False):
-        for l in range(L):
-            layers[l].forward(x_static[l], residual=x_static[l], out=out[l],
-                              ids_out=ids_buf[l] if record_ids else None)
+    def body():
+        if stacked:
+            moe.moe_stack_forward(desc, stack, T, ws)
+        else:
+            for l in range(L):
+                layers[l].forward(x_static[l], residual=x_static[l], out=out[l], ids_out=ids_buf[l])
 
     # unique active experts per layer for every rotation (counted from the routing)
     union = np.zeros((R, L), np.int64)
     for r in range(R):
         x_static.copy_(xs[r])
-        body(record_ids=True)
+        body()
         ids = ids_buf.cpu().numpy()
         for l in range(L):
             union[r, l] = len(set(ids[l].reshape(-1).tolist())) + wl.S
-    for l in range(L):
-        st = moe.moe_get_status(layers[l].ws)
+    for w_ in ([ws] if stacked else [ly.ws for ly in layers]):
+        st = moe.moe_get_status(w_)
         if st != 0:
-            raise RuntimeError(f"layer {l}: device status {moe.moe_status_string(st)}")
-    out_r0 = None
+            raise RuntimeError(f"device status {moe.moe_status_string(st)}")
     x_static.copy_(xs[0])
     body()
     torch.cuda.synchronize()
     out_r0 = out.cpu().numpy()
 
-    # CUDA graph of one step, with trace events around each layer's expert kernels
+    # CUDA graph of one step, with trace events around the expert launches
     events = [torch.cuda.Event(enable_timing=True) for _ in range(4 * L)]
     use_graph = not args.no_graph
     graph = None
+    moe.moe_trace_events(events)
     if use_graph:
-        moe.moe_trace_events(events)
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             body()
-        moe.moe_trace_events(None)
+    else:
+        body()
+    n_traced = moe.moe_trace_used()
+    moe.moe_trace_events(None)
 
     stream = torch.cuda.current_stream()
 
@@ -349,9 +368,17 @@ def run_ours(args, wl, T):
         ms_total = float(tt.item())
     ms_step = ms_total / K
 
-    # per-kernel durations of the last step (trace events)
-    gu_ms = [events[4 * l].elapsed_time(events[4 * l + 1]) for l in range(L)]
-    dn_ms = [events[4 * l + 2].elapsed_time(events[4 * l + 3]) for l in range(L)]
+    # phase stamps (SM cycles of CTA 0) of the single-launch kernel's last layer
+    phases = None
+    phase_ws = ws if stacked else layers[-1].ws
+    st = moe.MoeLayer.ws_view_of(phase_ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,)).cpu().numpy()
+    order = [0, 1, 2, 9, 10, 11, 3, 4, 5, 6, 7, 8]
+    names = ["router+quant", "barrier1", "topk+stage", "counts+scan", "positions", "tile_plan", "gate_up",
+             "barrier2", "down", "barrier3", "combine"]
+    seq = st[order].astype(np.float64)
+    if seq[0] > 0 and (np.diff(seq) >= 0).all():
+        mhz = clock_info.get("sm_mhz") or 2070.0
+        phases = {n: round(float(v) / mhz, 3) for n, v in zip(names, np.diff(seq))}
 
     # bytes
     gu_bytes = synth.layout.matrix_bytes(wl.fmt, wl.I, wl.H)
@@ -361,11 +388,43 @@ def run_ours(args, wl, T):
     active_bytes_total = float(sum(union[r].sum() for r in steps_rot)) * exp_bytes
     active_gbs = active_bytes_total / (ms_total * 1e-3) / 1e9
     last_r = (W + K - 1) % R
-    gu_alg = union[last_r] * 2 * gu_bytes                        # per launch (layer) of the last step
-    dn_alg = union[last_r] * dn_bytes
-    gu_gbs = float(np.sum(gu_alg) / (np.sum(gu_ms) * 1e-3) / 1e9)
-    dn_gbs = float(np.sum(dn_alg) / (np.sum(dn_ms) * 1e-3) / 1e9)
     peak, peak_src = measured_peaks()
+    router_bytes = wl.E * wl.H * 4
+    if stacked:
+        # one launch per step moves every layer's router weights and active experts' 3 matrices
+        launch_ms = events[0].elapsed_time(events[1])
+        alg = float(union[last_r].sum() * exp_bytes + L * router_bytes)
+        gbs = alg / (launch_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "kernel": "decode_fused_kernel (all layers of a step, one cooperative launch)",
+                    "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
+                    "traffic": profiled_traffic(wl.name, "decode_fused_kernel"),
+                    "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * launch_ms}
+        launches_per_step = 1
+    else:
+        per_layer = n_traced // L
+        if per_layer == 2:
+            fz_ms = [events[2 * l].elapsed_time(events[2 * l + 1]) for l in range(L)]
+            alg = union[last_r] * exp_bytes + router_bytes
+            gbs = float(np.sum(alg) / (np.sum(fz_ms) * 1e-3) / 1e9)
+            roofline = {"bound": "hbm", "kernel": "decode_fused_kernel (one layer, one cooperative launch)",
+                        "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
+                        "traffic": profiled_traffic(wl.name, "decode_fused_kernel"),
+                        "algorithmic_bytes_per_launch": float(np.mean(alg)), "avg_launch_us": 1e3 * float(np.mean(fz_ms))}
+            launches_per_step = L
+        else:
+            gu_ms = [events[4 * l].elapsed_time(events[4 * l + 1]) for l in range(L)]
+            dn_ms = [events[4 * l + 2].elapsed_time(events[4 * l + 3]) for l in range(L)]
+            gu_alg = union[last_r] * 2 * gu_bytes
+            dn_alg = union[last_r] * dn_bytes
+            gu_gbs = float(np.sum(gu_alg) / (np.sum(gu_ms) * 1e-3) / 1e9)
+            dn_gbs = float(np.sum(dn_alg) / (np.sum(dn_ms) * 1e-3) / 1e9)
+            roofline = {"bound": "hbm", "kernel": "gateup_kernel (expert gate/up GEMV + SwiGLU + q8_K requant)",
+                        "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
+                        "peak_source": peak_src, "traffic": profiled_traffic(wl.name, "gateup_kernel"),
+                        "algorithmic_bytes_per_launch": float(np.mean(gu_alg)),
+                        "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
+                        "down_kernel_gbs": dn_gbs, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms))}
+            launches_per_step = L * (10 if T * wl.k > 256 else 6)
 
     # end to end through the public call with host buffers: pinned H2D of the
     # step's inputs, the layers, D2H of the outputs, every step
@@ -390,7 +449,6 @@ def run_ours(args, wl, T):
 
     tokens_per_step = T * world
     value = tokens_per_step / (ms_step * 1e-3)
-    launches_per_layer = 6 if T * wl.k <= 256 else 10
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -401,23 +459,18 @@ def run_ours(args, wl, T):
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct expert weights "
                          "plus %.0f MB of router weights (L2 129 MB)" % (
                              np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
-                   "graph": use_graph, "rotations": R},
+                   "graph": use_graph, "rotations": R, "single_launch_stack": stacked},
         "clocks": clock_info,
         "us_per_layer": 1e3 * ms_step / L,
         "active_expert_bytes_per_step": active_bytes_total / K,
         "active_expert_gbs": active_gbs,
         "active_frac_of_8tbs": active_gbs / NOMINAL_HBM_GBS,
         "active_frac_of_measured": active_gbs / peak,
-        "roofline": {"bound": "hbm", "kernel": "gateup_kernel (expert gate/up GEMV + SwiGLU + q8_K requant)",
-                     "achieved": gu_gbs, "peak": peak, "unit": "GB/s", "frac": gu_gbs / peak,
-                     "peak_source": peak_src,
-                     "traffic": profiled_traffic(wl.name),
-                     "algorithmic_bytes_per_launch": float(np.mean(gu_alg)),
-                     "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
-                     "down_kernel_gbs": dn_gbs, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms))},
+        "roofline": roofline,
+        "decode_phases_us": phases,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
-        "gpu_launches": launches_per_layer * L * K,
+        "gpu_launches": launches_per_step * K,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(wl, T, x_host, args.cpu_budget_s)

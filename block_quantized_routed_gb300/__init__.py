@@ -21,8 +21,8 @@ __all__ = [
     "MoeError", "LayerDesc", "WsLayout", "FMT_Q4K", "FMT_Q2K", "ROUTE_SOFTMAX", "ROUTE_SIGMOID",
     "load", "lib", "moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_bucket_workspace_size",
     "moe_expert_ffn", "moe_expert_ffn_workspace_size", "moe_combine", "moe_layer_forward",
-    "moe_layer_workspace_size", "moe_workspace_layout", "moe_get_status", "moe_status_string",
-    "moe_debug_subblock_dots", "moe_trace_events", "expert_table", "MoeLayer",
+    "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "stack_pointer_table", "moe_get_status", "moe_status_string",
+    "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "expert_table", "MoeLayer",
 ]
 
 FMT_Q4K = 0
@@ -56,7 +56,7 @@ class LayerDesc(ctypes.Structure):
 class WsLayout(ctypes.Structure):
     _fields_ = [(n, ctypes.c_size_t) for n in
                 ("status", "xq", "xd", "xbs", "logits", "ids", "gates", "gap", "counts", "offsets", "perm", "inv",
-                 "h", "hq", "hd", "hbs", "y", "total")]
+                 "h", "hq", "hd", "hbs", "y", "phase_ns", "total")]
 
 
 _lib = None
@@ -84,10 +84,12 @@ def load():
         "moe_expert_ffn": (ctypes.c_int, [D, P, P, P, P, P, P, P, I32, P, P, SZ, P]),
         "moe_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P, P]),
         "moe_layer_forward": (ctypes.c_int, [D, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
+        "moe_stack_forward": (ctypes.c_int, [D, I32, P, I32, P, SZ, P]),
         "moe_get_status": (ctypes.c_int, [P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_debug_subblock_dots": (ctypes.c_int, [I32, P, I32, I32, P, I32, P, P, P]),
         "moe_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), I32]),
+        "moe_trace_used": (I32, []),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -187,6 +189,25 @@ def moe_layer_forward(desc, table, w_router, router_bias, x, residual, out, ids_
                                     ws.numel() * ws.element_size(), _stream(stream)), "moe_layer_forward")
 
 
+def moe_stack_forward(desc, layers, T, ws, stream=None):
+    """layers: int64 device tensor [n_layers, 8] of moe_layer_ptrs records
+    (see stack_pointer_table)."""
+    _check(load().moe_stack_forward(ctypes.byref(_desc(desc)), layers.shape[0], _ptr(layers), T, _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)), "moe_stack_forward")
+
+
+def stack_pointer_table(rows, device="cuda"):
+    """Device array of moe_layer_ptrs from per-layer dicts with keys table,
+    w_router, router_bias, x, residual, out, ids_out, gates_out (tensors or
+    None).  The returned tensor keeps references to every tensor it points at."""
+    import torch
+    keys = ["table", "w_router", "router_bias", "x", "residual", "out", "ids_out", "gates_out"]
+    vals = [[0 if r.get(k2) is None else int(r[k2].data_ptr()) for k2 in keys] for r in rows]
+    t = torch.tensor(vals, dtype=torch.int64, device=device)
+    t._refs = [dict(r) for r in rows]
+    return t
+
+
 def moe_get_status(ws, stream=None) -> int:
     return int(load().moe_get_status(_ptr(ws), _stream(stream)))
 
@@ -203,15 +224,20 @@ def moe_trace_events(events):
         _check(load().moe_trace_events(None, 0), "moe_trace_events")
         return
     import torch
-    for ev in events:
-        if not ev.cuda_event:           # torch creates the CUDA event on its first record
-            ev.record(torch.cuda.current_stream())
-    torch.cuda.current_stream().synchronize()
+    fresh = [ev for ev in events if not ev.cuda_event]
+    for ev in fresh:                    # torch creates the CUDA event on its first record
+        ev.record(torch.cuda.current_stream())
+    if fresh:
+        torch.cuda.current_stream().synchronize()
     if any(not ev.cuda_event for ev in events):
         raise MoeError(MOE_ERR_INVALID_ARG, "moe_trace_events")
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(ev.cuda_event) for ev in events])
     _trace_keep = (arr, list(events))
     _check(load().moe_trace_events(arr, len(events)), "moe_trace_events")
+
+
+def moe_trace_used() -> int:
+    return int(load().moe_trace_used())
 
 
 def moe_debug_subblock_dots(fmt, w, N, K, q, isum, bsum, stream=None):
@@ -265,10 +291,14 @@ class MoeLayer:
 
     def ws_view(self, name, dtype, shape):
         """A view of an intermediate region of the workspace (after a call)."""
+        return MoeLayer.ws_view_of(self.ws, self.layout, name, dtype, shape)
+
+    @staticmethod
+    def ws_view_of(ws, layout, name, dtype, shape):
         import torch
-        off = getattr(self.layout, name)
+        off = getattr(layout, name)
         n = 1
         for s in shape:
             n *= s
         itemsize = torch.empty((), dtype=dtype).element_size()
-        return self.ws[off:off + n * itemsize].view(dtype).view(*shape)
+        return ws[off:off + n * itemsize].view(dtype).view(*shape)

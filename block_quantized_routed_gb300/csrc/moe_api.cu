@@ -11,6 +11,7 @@ namespace moe {
 namespace {
 
 constexpr size_t kAlign = 256;
+constexpr size_t kDecodeSmemMax = 200 * 1024;
 
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
@@ -55,6 +56,7 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
   Carve c;
   p.pub.status = c.take(16);
   p.n_tiles = p.pub.status + 4;
+  p.bar = p.pub.status + 8;
   p.pub.xq = c.take(T * H);
   p.pub.xd = c.take(T * (H / 256) * 4);
   p.pub.xbs = c.take(T * (H / 16) * 2);
@@ -74,6 +76,8 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
   p.tiles = c.take((size_t)p.max_tiles * sizeof(Tile));
   p.req_cnt = c.take((size_t)p.max_tiles * (I / 256) * 4);
   p.chunk_cnt = c.take((size_t)(p.n_chunks > 0 ? p.n_chunks : 1) * EpS * 4);
+  p.phase_ns = c.take(16 * 8);
+  p.pub.phase_ns = p.phase_ns;
   p.total = c.off;
   p.pub.total = p.total;
   return p;
@@ -271,6 +275,54 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
   const int nIB = desc->I / 256;
   cudaStream_t s = as_stream(stream);
 
+  if (T <= kDecodeMaxT && (int64_t)T * k <= kSmallPairs) {
+    if (decode_smem_bytes(T, H, desc->I, E, k, S) <= kDecodeSmemMax) {
+      DecodeArgs d{};
+      d.fmt = desc->fmt;
+      d.H = H;
+      d.I = desc->I;
+      d.E = E;
+      d.k = k;
+      d.S = S;
+      d.route = desc->route;
+      d.T = T;
+      d.table = table;
+      d.w_router = w_router;
+      d.bias = router_bias;
+      d.x = x;
+      d.residual = residual;
+      d.out = out;
+      d.xq = xq;
+      d.xd = xd;
+      d.xbs = xbs;
+      d.logits = logits;
+      d.gap = gap;
+      d.ids = ids;
+      d.gates = gates;
+      d.counts = counts;
+      d.offsets = offsets;
+      d.perm = perm;
+      d.inv = inv;
+      d.h = static_cast<float*>(at(p.pub.h));
+      d.hq = static_cast<int8_t*>(at(p.pub.hq));
+      d.hd = static_cast<float*>(at(p.pub.hd));
+      d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+      d.y = static_cast<float*>(at(p.pub.y));
+      d.bar = static_cast<unsigned long long*>(at(p.bar));
+      d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
+      d.status = status;
+      d.ids_out = ids_out;
+      d.gates_out = gates_out;
+      d.n_layers = 1;
+      d.layers = nullptr;
+      trace_record(s);
+      const cudaError_t err = launch_decode_fused(d, s);
+      trace_record(s);
+      if (err == cudaSuccess) return MOE_OK;
+      if (err != cudaErrorCooperativeLaunchTooLarge) return MOE_ERR_CUDA;
+      cudaGetLastError();  // not co-resident on this device: use the multi-kernel path
+    }
+  }
   if (launch_q8k_quantize(x, T, H, xq, xd, xbs, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_router(x, w_router, router_bias, T, H, E, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
   if ((int64_t)T * k <= kSmallPairs) {
@@ -316,12 +368,69 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
   return MOE_OK;
 }
 
+int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
+                      void* ws, size_t ws_bytes, void* stream) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (n_layers < 0 || T < 0 || T > desc->T_max) return MOE_ERR_INVALID_ARG;
+  if (n_layers == 0 || T == 0) return MOE_OK;
+  if (!layers || !ws || !aligned(ws, kAlign) || !aligned(layers, 8)) return MOE_ERR_INVALID_ARG;
+  const int H = desc->H, E = desc->E, k = desc->top_k, S = desc->n_shared;
+  if (T > kDecodeMaxT || (int64_t)T * k > kSmallPairs || decode_smem_bytes(T, H, desc->I, E, k, S) > kDecodeSmemMax)
+    return MOE_ERR_UNSUPPORTED;
+  const WsPlan p = plan_workspace(*desc);
+  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  char* base = static_cast<char*>(ws);
+  auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  DecodeArgs d{};
+  d.fmt = desc->fmt;
+  d.H = H;
+  d.I = desc->I;
+  d.E = E;
+  d.k = k;
+  d.S = S;
+  d.route = desc->route;
+  d.T = T;
+  d.xq = static_cast<int8_t*>(at(p.pub.xq));
+  d.xd = static_cast<float*>(at(p.pub.xd));
+  d.xbs = static_cast<int16_t*>(at(p.pub.xbs));
+  d.logits = static_cast<float*>(at(p.pub.logits));
+  d.gap = static_cast<float*>(at(p.pub.gap));
+  d.ids = static_cast<int32_t*>(at(p.pub.ids));
+  d.gates = static_cast<float*>(at(p.pub.gates));
+  d.counts = static_cast<int32_t*>(at(p.pub.counts));
+  d.offsets = static_cast<int32_t*>(at(p.pub.offsets));
+  d.perm = static_cast<int32_t*>(at(p.pub.perm));
+  d.inv = static_cast<int32_t*>(at(p.pub.inv));
+  d.h = static_cast<float*>(at(p.pub.h));
+  d.hq = static_cast<int8_t*>(at(p.pub.hq));
+  d.hd = static_cast<float*>(at(p.pub.hd));
+  d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+  d.y = static_cast<float*>(at(p.pub.y));
+  d.bar = static_cast<unsigned long long*>(at(p.bar));
+  d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
+  d.status = static_cast<int*>(at(p.pub.status));
+  d.n_layers = n_layers;
+  d.layers = layers;
+  cudaStream_t s = as_stream(stream);
+  trace_record(s);
+  const cudaError_t err = launch_decode_fused(d, s);
+  trace_record(s);
+  if (err == cudaErrorCooperativeLaunchTooLarge) {
+    cudaGetLastError();
+    return MOE_ERR_UNSUPPORTED;
+  }
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 int moe_get_status(void* ws, void* stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
   if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
   int v = 0;
   if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
-  if (v != 0 && cudaMemset(ws, 0, sizeof(int)) != cudaSuccess) return MOE_ERR_CUDA;
+  // clear the status block (status word, tile count and the grid-barrier
+  // counter, which a timed-out barrier leaves out of step)
+  if (v != 0 && cudaMemset(ws, 0, 16) != cudaSuccess) return MOE_ERR_CUDA;
   return v;
 }
 
@@ -345,6 +454,8 @@ int moe_trace_events(void* const* events, int32_t n_events) {
   g_trace_next = 0;
   return MOE_OK;
 }
+
+int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }
 
 int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, int32_t T,
                             int32_t* isum, int32_t* bsum, void* stream) {

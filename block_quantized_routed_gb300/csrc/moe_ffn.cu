@@ -30,13 +30,11 @@ namespace {
 
 constexpr int kThreads = 128;  // 4 warps per CTA
 
-template <int TT>
-__host__ __device__ constexpr size_t gateup_smem(int H) {
-  return (size_t)TT * H + (size_t)TT * (H / 8) + (size_t)TT * (H / 256) * 4 + (size_t)4 * 2 * TT * 32 * 4;
-}
-template <int TT>
-__host__ __device__ constexpr size_t down_smem(int I) {
-  return (size_t)TT * I + (size_t)TT * (I / 8) + (size_t)TT * (I / 256) * 4;
+// shared memory: q8_K rows [TT][K], 16-sums [TT][K/16], scales [TT][K/256],
+// row offsets [TT], per-warp accumulators [4][NM][TT][32]
+__host__ __device__ constexpr size_t ffn_smem(int TT, int K, int NM) {
+  return (size_t)TT * K + (size_t)TT * (K / 8) + (size_t)TT * (K / 256) * 4 + (size_t)TT * 4 +
+         (size_t)4 * NM * TT * 32 * 4;
 }
 
 // Copy the q8_K rows of `cnt` tokens into shared memory: codes [TT][K],
@@ -59,16 +57,18 @@ __device__ __forceinline__ void stage_rows(int cnt, int K, const int8_t* __restr
   }
 }
 
-template <int FMT, int TT>
+template <int FMT>
 __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ __align__(16) uint8_t smem[];
   __shared__ int s_last;
+  const int TT = a.TT;
   const int H = a.H, I = a.I, nbH = H / 256, nRG = I / 32, nIB = I / 256;
   int8_t* s_act = reinterpret_cast<int8_t*>(smem);
   int16_t* s_bs = reinterpret_cast<int16_t*>(smem + (size_t)TT * H);
   float* s_da = reinterpret_cast<float*>(smem + (size_t)TT * H + (size_t)TT * (H / 8));
-  float* s_red = s_da + TT * nbH;  // [4 warps][2][TT][32]
+  int* s_off = reinterpret_cast<int*>(s_da + TT * nbH);
+  float* s_red = reinterpret_cast<float*>(s_off + TT);  // [4 warps][2][TT][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = *a.n_tiles * nRG;
 
@@ -84,9 +84,10 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
                s_da);
     __syncthreads();
 
-    float accg[TT], accu[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) accg[t] = accu[t] = 0.0f;
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) s_off[t] = t * H;
+    float* accw = s_red + (size_t)warp * 2 * TT * 32;
+    for (int i = lane; i < 2 * TT * 32; i += 32) accw[i] = 0.0f;
+    __syncthreads();
     const uint8_t* gbase = static_cast<const uint8_t*>(ep.gate) + (size_t)rg * nbH * F::kSlabBytes;
     const uint8_t* ubase = static_cast<const uint8_t*>(ep.up) + (size_t)rg * nbH * F::kSlabBytes;
 #pragma unroll 1
@@ -94,21 +95,8 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
       SbRegs<FMT> sg, su;
       load_sb<FMT>(gbase + (size_t)b * F::kSlabBytes, lane, sg);
       load_sb<FMT>(ubase + (size_t)b * F::kSlabBytes, lane, su);
-#pragma unroll
-      for (int t = 0; t < TT; ++t) {
-        if (t < cnt) {
-          const int8_t* act = s_act + (size_t)t * H + 256 * b;
-          const int16_t* bs = s_bs + (size_t)t * (H / 16) + 16 * b;
-          const float da = s_da[t * nbH + b];
-          accg[t] += sb_contrib<FMT>(sg, act, bs, da);
-          accu[t] += sb_contrib<FMT>(su, act, bs, da);
-        }
-      }
-    }
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      s_red[((warp * 2 + 0) * TT + t) * 32 + lane] = accg[t];
-      s_red[((warp * 2 + 1) * TT + t) * 32 + lane] = accu[t];
+      sb_accum<FMT>(sg, s_act, s_bs, s_da, s_off, b, cnt, accw, lane);
+      sb_accum<FMT>(su, s_act, s_bs, s_da, s_off, b, cnt, accw + TT * 32, lane);
     }
     __syncthreads();
     // h = silu(G) * U for the 32 rows of this group and the tile's tokens
@@ -143,14 +131,17 @@ __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
   }
 }
 
-template <int FMT, int TT>
-__global__ void __launch_bounds__(kThreads, 4) down_kernel(FfnArgs a) {
+template <int FMT>
+__global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ __align__(16) uint8_t smem[];
+  const int TT = a.TT;
   const int H = a.H, I = a.I, nbI = I / 256, nQuad = H / 128;
   int8_t* s_act = reinterpret_cast<int8_t*>(smem);
   int16_t* s_bs = reinterpret_cast<int16_t*>(smem + (size_t)TT * I);
   float* s_da = reinterpret_cast<float*>(smem + (size_t)TT * I + (size_t)TT * (I / 8));
+  int* s_off = reinterpret_cast<int*>(s_da + TT * nbI);
+  float* s_red = reinterpret_cast<float*>(s_off + TT);  // [4 warps][TT][32]
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int n_items = *a.n_tiles * nQuad;
 
@@ -168,23 +159,19 @@ __global__ void __launch_bounds__(kThreads, 4) down_kernel(FfnArgs a) {
     __syncthreads();
     stage_rows(cnt, I, a.hq, a.hbs, a.hd, [&](int tt) { return (int64_t)(tl.start + tt); }, s_act, s_bs, s_da);
     __syncthreads();
-    float acc[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) acc[t] = 0.0f;
+    for (int t = threadIdx.x; t < cnt; t += blockDim.x) s_off[t] = t * I;
+    float* accw = s_red + (size_t)warp * TT * 32;
+    for (int i = lane; i < TT * 32; i += 32) accw[i] = 0.0f;
+    __syncthreads();
     const uint8_t* dbase = static_cast<const uint8_t*>(ep.down) + (size_t)rg * nbI * F::kSlabBytes;
-#pragma unroll 2
+#pragma unroll 1
     for (int b = 0; b < nbI; ++b) {
       SbRegs<FMT> sd;
       load_sb<FMT>(dbase + (size_t)b * F::kSlabBytes, lane, sd);
-#pragma unroll
-      for (int t = 0; t < TT; ++t)
-        if (t < cnt)
-          acc[t] += sb_contrib<FMT>(sd, s_act + (size_t)t * I + 256 * b, s_bs + (size_t)t * (I / 16) + 16 * b,
-                                    s_da[t * nbI + b]);
+      sb_accum<FMT>(sd, s_act, s_bs, s_da, s_off, b, cnt, accw, lane);
     }
-#pragma unroll
-    for (int t = 0; t < TT; ++t)
-      if (t < cnt) a.y[(size_t)a.perm[tl.start + t] * H + row] = acc[t];
+    __syncwarp();
+    for (int t = 0; t < cnt; ++t) a.y[(size_t)a.perm[tl.start + t] * H + row] = accw[t * 32 + lane];
   }
 }
 
@@ -272,12 +259,12 @@ cudaError_t occupancy(const void* kern, size_t smem, int* per_sm) {
   return cudaSuccess;
 }
 
-template <int FMT, int TT>
+template <int FMT>
 cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
   const int sms = num_sms();
   {
-    const size_t smem = gateup_smem<TT>(a.H);
-    auto kern = gateup_kernel<FMT, TT>;
+    const size_t smem = ffn_smem(a.TT, a.H, 2);
+    auto kern = gateup_kernel<FMT>;
     int per_sm = 0;
     cudaError_t err = occupancy(reinterpret_cast<const void*>(kern), smem, &per_sm);
     if (err != cudaSuccess) return err;
@@ -290,8 +277,8 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
     if (err != cudaSuccess) return err;
   }
   {
-    const size_t smem = down_smem<TT>(a.I);
-    auto kern = down_kernel<FMT, TT>;
+    const size_t smem = ffn_smem(a.TT, a.I, 1);
+    auto kern = down_kernel<FMT>;
     int per_sm = 0;
     cudaError_t err = occupancy(reinterpret_cast<const void*>(kern), smem, &per_sm);
     if (err != cudaSuccess) return err;
@@ -305,34 +292,17 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
   }
 }
 
-template <int FMT>
-cudaError_t launch_ffn_fmt(const FfnArgs& a, cudaStream_t s) {
-  switch (a.TT) {
-    case 1: return launch_ffn_t<FMT, 1>(a, s);
-    case 2: return launch_ffn_t<FMT, 2>(a, s);
-    case 4: return launch_ffn_t<FMT, 4>(a, s);
-    case 8: return launch_ffn_t<FMT, 8>(a, s);
-    case 16: return launch_ffn_t<FMT, 16>(a, s);
-    default: return cudaErrorInvalidValue;
-  }
-}
-
 }  // namespace
 
 int pick_tile_tokens(int T, int H) {
-  int tt = 1;
-  while (tt < T && tt < 16) tt <<= 1;
+  int tt = T < 16 ? (T > 0 ? T : 1) : 16;
   const size_t budget = 80 * 1024;
-  while (tt > 1) {
-    size_t need = (size_t)tt * H + (size_t)tt * (H / 8) + (size_t)tt * (H / 256) * 4 + (size_t)8 * tt * 32 * 4;
-    if (need <= budget) break;
-    tt >>= 1;
-  }
+  while (tt > 1 && ffn_smem(tt, H, 2) > budget) --tt;
   return tt;
 }
 
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
-  return a.fmt == kQ4K ? launch_ffn_fmt<kQ4K>(a, s) : launch_ffn_fmt<kQ2K>(a, s);
+  return a.fmt == kQ4K ? launch_ffn_t<kQ4K>(a, s) : launch_ffn_t<kQ2K>(a, s);
 }
 
 cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S, const float* residual,

@@ -27,6 +27,8 @@ struct WsPlan {
   size_t n_tiles;     // int32 (inside the status block: status[1])
   size_t req_cnt;     // int32 [max_tiles * I/256]  arrival counters
   size_t chunk_cnt;   // int32 [n_chunks * (E + S)]
+  size_t bar;         // uint64 grid-barrier counter (inside the status block)
+  size_t phase_ns;    // uint64 [16]  phase stamps of the single-launch decode kernel
   int max_tiles;
   int n_chunks;
   size_t total;
@@ -82,6 +84,44 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 
 // profiling hook state (per host thread): records the next event if tracing
 void trace_record(cudaStream_t s);
+
+// Single-launch decode layer (cooperative kernel); see moe_decode.cu.
+struct DecodeArgs {
+  int fmt, H, I, E, k, S, route, T;
+  const moe_expert_ptrs* table;
+  const float* w_router;
+  const float* bias;
+  const float* x;
+  const float* residual;
+  float* out;
+  int8_t* xq;
+  float* xd;
+  int16_t* xbs;
+  float* logits;
+  float* gap;
+  int32_t* ids;
+  float* gates;
+  int32_t* counts;
+  int32_t* offsets;
+  int32_t* perm;
+  int32_t* inv;
+  float* h;
+  int8_t* hq;
+  float* hd;
+  int16_t* hbs;
+  float* y;
+  unsigned long long* bar;
+  unsigned long long* phase_ns;   // [16] SM-cycle stamps of CTA 0 (nullable)
+  int* status;
+  int32_t* ids_out;
+  float* gates_out;
+  int n_layers;                   // layers of this launch (stack); 1 for one layer
+  const moe_layer_ptrs* layers;   // device array of n_layers records, or NULL: use the fields above
+};
+size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S);
+cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+// largest token count of the single-launch decode path
+constexpr int kDecodeMaxT = 16;
 
 cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S,
                            const float* residual, float* out, cudaStream_t s);

@@ -74,62 +74,6 @@ __global__ void __launch_bounds__(128) router_kernel(const float* __restrict__ x
 }
 
 // ---------------------------------------------------------------- top-k
-// One warp per token.  Lane l owns experts e = l + 32*i; a bit per owned
-// expert marks it as taken.  k+1 rounds of a warp arg-max (larger logit wins,
-// equal logits: lower index) give the k ids in descending order and the gap.
-// NaN logits are treated as -inf.
-__device__ __forceinline__ void warp_topk(const float* __restrict__ l, int E, int k, int route, int lane,
-                                          int32_t* ids, float* gates, float* gap) {
-  uint32_t taken = 0;
-  float sel_v[MOE_MAX_TOPK];
-  int sel_e[MOE_MAX_TOPK];
-  float next_v = -INFINITY;
-  const int rounds = k < E ? k + 1 : k;
-  for (int r = 0; r < rounds; ++r) {
-    float bv = -INFINITY;
-    int be = INT_MAX;
-    int i = 0;
-    for (int e = lane; e < E; e += 32, ++i) {
-      if (taken & (1u << i)) continue;
-      float v = l[e];
-      if (v != v) v = -INFINITY;
-      if (v > bv || (v == bv && e < be)) { bv = v; be = e; }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, o);
-      if (ov > bv || (ov == bv && oe < be)) { bv = ov; be = oe; }
-    }
-    if (r < k) {
-      if ((be & 31) == lane) taken |= 1u << (be >> 5);
-      if (r < MOE_MAX_TOPK) { sel_v[r] = bv; sel_e[r] = be; }
-    } else {
-      next_v = bv;
-    }
-  }
-  // gates, renormalised over the k selected
-  float z = 0.0f;
-  float g[MOE_MAX_TOPK];
-#pragma unroll
-  for (int s = 0; s < MOE_MAX_TOPK; ++s) {
-    if (s < k) {
-      g[s] = route == MOE_ROUTE_SOFTMAX ? expf(sel_v[s] - sel_v[0]) : 1.0f / (1.0f + expf(-sel_v[s]));
-      z += g[s];
-    }
-  }
-  if (lane == 0) {
-    const float inv = 1.0f / z;
-#pragma unroll
-    for (int s = 0; s < MOE_MAX_TOPK; ++s)
-      if (s < k) {
-        ids[s] = sel_e[s];
-        gates[s] = g[s] * inv;
-      }
-    if (gap) *gap = k < E ? sel_v[k - 1] - next_v : INFINITY;
-  }
-}
-
 __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                    int route, int32_t* __restrict__ ids,
                                                    float* __restrict__ gates, float* __restrict__ gap) {
@@ -138,41 +82,6 @@ __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ log
   if (t >= T) return;
   warp_topk(logits + (int64_t)t * E, E, k, route, lane, ids + (int64_t)t * k, gates + (int64_t)t * k,
             gap ? gap + t : nullptr);
-}
-
-// ---------------------------------------------------------------- scans
-// Exclusive scan in place of n <= 2*blockDim ints in shared memory; returns
-// the total.  Called by every thread of the block (blockDim a multiple of 32).
-__device__ int block_exclusive_scan(int* a, int n) {
-  __shared__ int wsum[32];
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
-  const int i0 = 2 * tid, i1 = 2 * tid + 1;
-  const int v0 = i0 < n ? a[i0] : 0, v1 = i1 < n ? a[i1] : 0;
-  const int s = v0 + v1;
-  int x = s;
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) {
-    const int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
-  }
-  if (lane == 31) wsum[warp] = x;
-  __syncthreads();
-  if (warp == 0) {
-    int v = lane < nw ? wsum[lane] : 0;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const int y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
-    }
-    wsum[lane] = v;
-  }
-  __syncthreads();
-  const int excl = x - s + (warp > 0 ? wsum[warp - 1] : 0);
-  const int total = wsum[nw - 1];
-  if (i0 < n) a[i0] = excl;
-  if (i1 < n) a[i1] = excl + v0;
-  __syncthreads();
-  return total;
 }
 
 // Tile plan from counts/offsets: each expert with count c gets ceil(c/TT)

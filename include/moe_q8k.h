@@ -105,6 +105,13 @@ typedef struct {
   size_t hd;       /* float [P, I/256]                                         */
   size_t hbs;      /* int16 [P, I/16]                                          */
   size_t y;        /* float [P, H]     expert outputs, indexed by slot index   */
+  size_t phase_ns; /* uint64 [16] SM clock-cycle stamps (clock64) taken by CTA 0
+                      of the single-launch decode kernel at its phase
+                      boundaries: [0] start, [1] router done, [2] after
+                      barrier 1, [9] top-k done, [10] counts and scan,
+                      [11] bucket positions, [3] tile plan done, [4] gate/up
+                      done, [5] after barrier 2, [6] down done, [7] after
+                      barrier 3, [8] combine done                             */
   size_t total;    /* bytes required                                           */
 } moe_ws_layout;
 
@@ -198,6 +205,34 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table,
                       const float* residual, float* out, int32_t T, int32_t* ids_out,
                       float* gates_out, void* ws, size_t ws_bytes, void* stream);
 
+/* The pointers of one layer of a stack (see moe_stack_forward); the same
+ * meaning and rules as the arguments of moe_layer_forward. */
+typedef struct {
+  const moe_expert_ptrs* table; /* device array of E + n_shared records      */
+  const float* w_router;        /* [E, H]                                     */
+  const float* router_bias;     /* [E] or NULL                                */
+  const float* x;               /* [T, H]; may be a previous layer's out      */
+  const float* residual;        /* [T, H] or NULL; may alias out              */
+  float* out;                   /* [T, H]                                     */
+  int32_t* ids_out;             /* [T, k] or NULL                             */
+  float* gates_out;             /* [T, k] or NULL                             */
+} moe_layer_ptrs;
+
+/* A stack of n_layers MoE layers of the same shape, run in order in ONE
+ * launch: layer l+1 starts after layer l's output is complete, so a layer's
+ * x may point at the previous layer's out (a decode step through the
+ * stack).  `layers` is a DEVICE array of n_layers records.  Only the
+ * single-launch decode shapes are accepted: T <= 16, T*top_k <= 256, and
+ * the layer's staging fits in shared memory; otherwise MOE_ERR_UNSUPPORTED
+ * (run moe_layer_forward per layer instead).  ws: one workspace of
+ * moe_layer_workspace_size(desc) bytes, shared by the layers (its
+ * intermediates hold the last layer's).  While layer l computes its down
+ * projection, the next layer's router rows and shared-expert gate/up weights
+ * are prefetched into L2.  Source: Strata summary (the per-token layer loop
+ * run as captured, replayed work with no allocation on the token path). */
+int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
+                      void* ws, size_t ws_bytes, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the status word of a
  * workspace written by moe_layer_forward, moe_bucket or moe_expert_ffn.
  * Returns MOE_OK, a device-recorded error, or MOE_ERR_CUDA. */
@@ -206,15 +241,19 @@ int moe_get_status(void* ws, void* stream);
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 
-/* Profiling hook.  While set, every expert-FFN launch sequence issued by this
- * host thread (moe_layer_forward, moe_expert_ffn) records the next four
- * unused entries of `events` (cudaEvent_t handles created by the caller with
- * timing enabled) on its stream: immediately before and after the gate/up
- * kernel, and immediately before and after the down kernel.  Records use
+/* Profiling hook.  While set, the expert kernels launched by this host
+ * thread record the next unused entries of `events` (cudaEvent_t handles
+ * created by the caller with timing enabled) on their stream, immediately
+ * before and after each launch: two entries per single-launch decode layer
+ * (moe_layer_forward with T <= 16 and T*top_k <= 256), four per expert-FFN
+ * sequence otherwise (gate/up kernel, then down kernel).  Records use
  * cudaEventRecordExternal, so they also work inside stream capture.  When
  * the array is used up, recording stops.  events = NULL or n_events = 0
  * turns the hook off.  Returns MOE_OK or MOE_ERR_INVALID_ARG. */
 int moe_trace_events(void* const* events, int32_t n_events);
+
+/* Number of entries recorded since the last moe_trace_events call. */
+int32_t moe_trace_used(void);
 
 /* Test hook: the integer sub-block sums of the device dot routine that the
  * expert kernels use, for matrix w [N, K] against q8_K codes q [T, K]:

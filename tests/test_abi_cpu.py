@@ -59,7 +59,7 @@ def test_workspace_layout_regions(lib):
         sizes = dict(status=16, xq=T * H, xd=T * H // 256 * 4, xbs=T * H // 16 * 2, logits=T * E * 4,
                      ids=T * k * 4, gates=T * k * 4, gap=T * 4, counts=(E + S) * 4, offsets=(E + S + 1) * 4,
                      perm=P * 4, inv=P * 4, h=P * I * 4, hq=P * I, hd=P * I // 256 * 4, hbs=P * I // 16 * 2,
-                     y=P * H * 4)
+                     y=P * H * 4, phase_ns=128)
         spans = sorted((getattr(lay, n), getattr(lay, n) + s, n) for n, s in sizes.items())
         for (a0, a1, n0), (b0, b1, n1) in zip(spans, spans[1:]):
             assert a1 <= b0, (n0, n1)

@@ -304,3 +304,41 @@ def test_layer_forward_in_place_residual(moe):
     ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, 0, ex, wr, None, x, residual=x,
                                         forced_ids=ids.cpu().numpy())
     assert_close_rows(xd.cpu().numpy(), ref)
+
+
+@pytest.mark.parametrize("fmt,route,S,T", [(FMT_Q4K, 0, 1, 2), (FMT_Q2K, 1, 0, 5)])
+def test_stack_forward_chained_layers(moe, fmt, route, S, T):
+    """A stack whose layer l+1 reads layer l's output (a decode step through
+    the layers), in one launch; each layer matches the oracle run on the
+    GPU's own input for that layer."""
+    H, I, E, k, L = 512, 256, 16, 4, 3
+    ex = [_experts_host(fmt, E + S, H, I, seed=40 + l, layer=l) for l in range(L)]
+    tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
+    wrs = [synth.router_weight(E, H, 40, l) for l in range(L)]
+    x0 = synth.activations(T, H, 40)
+    xs = [dev(x0)] + [torch.empty((T, H), dtype=torch.float32, device="cuda") for _ in range(L - 1)]
+    outs = xs[1:] + [torch.empty((T, H), dtype=torch.float32, device="cuda")]
+    ids = [torch.empty((T, k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
+            for l in range(L)]
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
+    assert moe.moe_get_status(ws) == 0
+    for l in range(L):
+        xin = xs[l].cpu().numpy()
+        gids = ids[l].cpu().numpy()
+        rl, rids, _, rgap = oracle.route(xin, wrs[l], None, k, route)
+        routing_ok(gids, rids, rgap, rl)
+        ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xin, residual=xin,
+                                            forced_ids=gids)
+        assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
+
+
+def test_stack_forward_rejects_prefill_shapes(moe):
+    desc = dict(H=512, I=256, E=16, top_k=8, n_shared=0, route=0, fmt=FMT_Q4K, T_max=64)
+    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    rows = moe.stack_pointer_table([dict()], device="cuda")
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_stack_forward(desc, rows, 64, ws)
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
