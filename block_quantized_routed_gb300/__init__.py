@@ -21,7 +21,7 @@ __all__ = [
     "MoeError", "LayerDesc", "WsLayout", "FMT_Q4K", "FMT_Q2K", "ROUTE_SOFTMAX", "ROUTE_SIGMOID",
     "load", "lib", "moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_bucket_workspace_size",
     "moe_expert_ffn", "moe_expert_ffn_workspace_size", "moe_combine", "moe_layer_forward",
-    "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "stack_pointer_table", "moe_get_status", "moe_status_string",
+    "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "expert_table", "MoeLayer",
 ]
 
@@ -85,6 +85,7 @@ def load():
         "moe_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P, P]),
         "moe_layer_forward": (ctypes.c_int, [D, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_stack_forward": (ctypes.c_int, [D, I32, P, I32, P, SZ, P]),
+        "moe_layer_forward_noalloc": (ctypes.c_int, [D, P, P, P, P, P, P, I32, P, P, P]),
         "moe_get_status": (ctypes.c_int, [P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_debug_subblock_dots": (ctypes.c_int, [I32, P, I32, I32, P, I32, P, P, P]),
@@ -187,6 +188,16 @@ def moe_layer_forward(desc, table, w_router, router_bias, x, residual, out, ids_
     _check(load().moe_layer_forward(ctypes.byref(_desc(desc)), _ptr(table), _ptr(w_router), _ptr(router_bias),
                                     _ptr(x), _ptr(residual), _ptr(out), T, _ptr(ids_out), _ptr(gates_out), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)), "moe_layer_forward")
+
+
+def moe_layer_forward_noalloc(desc, table, w_router, router_bias, x, residual, out, ids_out=None, gates_out=None,
+                              stream=None):
+    """moe_layer_forward with the library's own fixed scratch (no workspace, no allocation)."""
+    T = x.shape[0]
+    _check(load().moe_layer_forward_noalloc(ctypes.byref(_desc(desc)), _ptr(table), _ptr(w_router),
+                                            _ptr(router_bias), _ptr(x), _ptr(residual), _ptr(out), T,
+                                            _ptr(ids_out), _ptr(gates_out), _stream(stream)),
+           "moe_layer_forward_noalloc")
 
 
 def moe_stack_forward(desc, layers, T, ws, stream=None):

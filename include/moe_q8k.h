@@ -233,6 +233,37 @@ typedef struct {
 int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* Largest workspace, in bytes, that moe_layer_forward_noalloc can serve. */
+#define MOE_NOALLOC_MAX_WORKSPACE ((size_t)16 << 20)
+
+/* moe_layer_forward without a workspace argument and without any memory
+ * allocation.  (No counterpart on the pages: this is a convenience of this
+ * library.)  It is meant for callers that cannot call cudaMalloc where they
+ * run the layer: an engine whose memory planner gives the whole device to
+ * its own pool, a plugin that only receives the tensors it reads and writes,
+ * or a token loop that must not allocate because allocating can synchronise
+ * the device mid-step.  The caller still passes every input and output; the
+ * intermediates live in a 16 MiB array that is part of the library (every
+ * GPU that loads the library holds it until the process exits).
+ *   - Arguments and results are those of moe_layer_forward.
+ *   - Descriptors whose moe_layer_workspace_size exceeds
+ *     MOE_NOALLOC_MAX_WORKSPACE are rejected with MOE_ERR_WORKSPACE (decode
+ *     shapes fit: e.g. H=6144, I=2048, 192 experts, top-8, 16 tokens needs
+ *     about 5 MB).
+ *   - The first call on a device looks up the array's device address for
+ *     that device (with it current); make that first call before any stream
+ *     capture.
+ *   - All calls share the one array and it keeps the last call's contents;
+ *     each call clears the parts that must start at zero.  Calls that
+ *     overlap on the GPU (other streams, other host threads) race on it:
+ *     order them.
+ *   - Device-side errors are not reported (there is no workspace to read
+ *     with moe_get_status); use moe_layer_forward for that. */
+int moe_layer_forward_noalloc(const moe_layer_desc* desc, const moe_expert_ptrs* table,
+                              const float* w_router, const float* router_bias, const float* x,
+                              const float* residual, float* out, int32_t T, int32_t* ids_out,
+                              float* gates_out, void* stream);
+
 /* Synchronizes `stream`, then reads and clears the status word of a
  * workspace written by moe_layer_forward, moe_bucket or moe_expert_ffn.
  * Returns MOE_OK, a device-recorded error, or MOE_ERR_CUDA. */
