@@ -372,13 +372,18 @@ def run_ours(args, wl, T):
     phases = None
     phase_ws = ws if stacked else layers[-1].ws
     st = moe.MoeLayer.ws_view_of(phase_ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,)).cpu().numpy()
-    order = [0, 1, 2, 9, 10, 11, 3, 4, 5, 6, 7, 8]
-    names = ["router+quant", "barrier1", "topk+stage", "counts+scan", "positions", "tile_plan", "gate_up",
-             "barrier2", "down", "barrier3", "combine"]
+    if st[15] == 2:   # pipelined schedule: one stage
+        order = [0, 3, 4, 6, 1, 8, 12]
+        names = ["stage_x", "gate_up", "down_prev", "router_next2", "combine_prev2", "wait_route_next+prefetch"]
+    else:
+        order = [0, 1, 2, 9, 10, 11, 3, 4, 5, 6, 7, 8]
+        names = ["router+quant", "barrier1", "topk+stage", "counts+scan", "positions", "tile_plan", "gate_up",
+                 "barrier2", "down", "barrier3", "combine"]
     seq = st[order].astype(np.float64)
     if seq[0] > 0 and (np.diff(seq) >= 0).all():
         mhz = clock_info.get("sm_mhz") or 2070.0
         phases = {n: round(float(v) / mhz, 3) for n, v in zip(names, np.diff(seq))}
+        phases["schedule"] = "pipelined" if st[15] == 2 else "sequential"
 
     # bytes
     gu_bytes = synth.layout.matrix_bytes(wl.fmt, wl.I, wl.H)

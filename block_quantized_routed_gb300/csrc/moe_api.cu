@@ -78,6 +78,23 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
   p.chunk_cnt = c.take((size_t)(p.n_chunks > 0 ? p.n_chunks : 1) * EpS * 4);
   p.phase_ns = c.take(16 * 8);
   p.pub.phase_ns = p.phase_ns;
+  // the pipelined decode schedule of a stack keeps several layers in flight:
+  // 3 copies of q8_K(x), 2 of logits, h and y (only for decode shapes)
+  p.xq_b[0] = p.pub.xq; p.xd_b[0] = p.pub.xd; p.xbs_b[0] = p.pub.xbs;
+  p.logits_b[0] = p.pub.logits; p.h_b[0] = p.pub.h; p.y_b[0] = p.pub.y;
+  p.pipeline = d.T_max <= kDecodeMaxT;
+  if (p.pipeline) {
+    for (int i = 1; i < 3; ++i) {
+      p.xq_b[i] = c.take(T * H);
+      p.xd_b[i] = c.take(T * (H / 256) * 4);
+      p.xbs_b[i] = c.take(T * (H / 16) * 2);
+    }
+    p.logits_b[1] = c.take(T * E * 4);
+    p.h_b[1] = c.take(P * I * 4);
+    p.y_b[1] = c.take(P * H * 4);
+    p.route_pub = c.take(4 * decode_route_bytes((int)T, (int)k, (int)S));
+    p.route_flag = c.take(8);
+  }
   p.total = c.off;
   p.pub.total = p.total;
   return p;
@@ -292,10 +309,10 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
       d.x = x;
       d.residual = residual;
       d.out = out;
-      d.xq = xq;
-      d.xd = xd;
-      d.xbs = xbs;
-      d.logits = logits;
+      d.xq[0] = xq;
+      d.xd[0] = xd;
+      d.xbs[0] = xbs;
+      d.logits[0] = logits;
       d.gap = gap;
       d.ids = ids;
       d.gates = gates;
@@ -303,11 +320,11 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
       d.offsets = offsets;
       d.perm = perm;
       d.inv = inv;
-      d.h = static_cast<float*>(at(p.pub.h));
+      d.h[0] = static_cast<float*>(at(p.pub.h));
       d.hq = static_cast<int8_t*>(at(p.pub.hq));
       d.hd = static_cast<float*>(at(p.pub.hd));
       d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
-      d.y = static_cast<float*>(at(p.pub.y));
+      d.y[0] = static_cast<float*>(at(p.pub.y));
       d.bar = static_cast<unsigned long long*>(at(p.bar));
       d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
       d.status = status;
@@ -391,10 +408,19 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   d.S = S;
   d.route = desc->route;
   d.T = T;
-  d.xq = static_cast<int8_t*>(at(p.pub.xq));
-  d.xd = static_cast<float*>(at(p.pub.xd));
-  d.xbs = static_cast<int16_t*>(at(p.pub.xbs));
-  d.logits = static_cast<float*>(at(p.pub.logits));
+  for (int i = 0; i < 3; ++i) {
+    d.xq[i] = static_cast<int8_t*>(at(p.xq_b[i]));
+    d.xd[i] = static_cast<float*>(at(p.xd_b[i]));
+    d.xbs[i] = static_cast<int16_t*>(at(p.xbs_b[i]));
+  }
+  for (int i = 0; i < 2; ++i) {
+    d.logits[i] = static_cast<float*>(at(p.logits_b[i]));
+    d.h[i] = static_cast<float*>(at(p.h_b[i]));
+    d.y[i] = static_cast<float*>(at(p.y_b[i]));
+  }
+  d.pipeline_ok = p.pipeline ? 1 : 0;
+  d.route_pub = p.pipeline ? static_cast<uint8_t*>(at(p.route_pub)) : nullptr;
+  d.route_flag = p.pipeline ? static_cast<unsigned long long*>(at(p.route_flag)) : nullptr;
   d.gap = static_cast<float*>(at(p.pub.gap));
   d.ids = static_cast<int32_t*>(at(p.pub.ids));
   d.gates = static_cast<float*>(at(p.pub.gates));
@@ -402,11 +428,9 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   d.offsets = static_cast<int32_t*>(at(p.pub.offsets));
   d.perm = static_cast<int32_t*>(at(p.pub.perm));
   d.inv = static_cast<int32_t*>(at(p.pub.inv));
-  d.h = static_cast<float*>(at(p.pub.h));
   d.hq = static_cast<int8_t*>(at(p.pub.hq));
   d.hd = static_cast<float*>(at(p.pub.hd));
   d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
-  d.y = static_cast<float*>(at(p.pub.y));
   d.bar = static_cast<unsigned long long*>(at(p.bar));
   d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
   d.status = static_cast<int*>(at(p.pub.status));

@@ -308,8 +308,9 @@ __device__ __forceinline__ void warp_topk_n(const float* l, int E, int k, int ro
       idx[j] = ti;
     }
   }
-  float sel_v[MOE_MAX_TOPK];
-  int sel_e[MOE_MAX_TOPK];
+  // lane r keeps round r's winner; everything stays in registers
+  float my_v = 0.0f;
+  int my_e = 0;
   float next_v = -INFINITY;
   const int rounds = k < E ? k + 1 : k;
   for (int r = 0; r < rounds; ++r) {
@@ -317,9 +318,9 @@ __device__ __forceinline__ void warp_topk_n(const float* l, int E, int k, int ro
     const uint32_t cand = key[0] == mk ? (uint32_t)idx[0] : 0xFFFFFFFFu;
     const int win = (int)__reduce_min_sync(0xffffffffu, cand);
     if (r < k) {
-      if (r < MOE_MAX_TOPK) {
-        sel_v[r] = key_logit(mk);
-        sel_e[r] = win;
+      if (lane == r) {
+        my_v = key_logit(mk);
+        my_e = win;
       }
       if ((win & 31) == lane) {  // the owner drops its head
 #pragma unroll
@@ -334,20 +335,19 @@ __device__ __forceinline__ void warp_topk_n(const float* l, int E, int k, int ro
       next_v = key_logit(mk);
     }
   }
-  if (lane == 0) {
-    float g[MOE_MAX_TOPK];
-    float z = 0.0f;
-    for (int s = 0; s < k; ++s) {
-      g[s] = route == MOE_ROUTE_SOFTMAX ? expf(sel_v[s] - sel_v[0]) : 1.0f / (1.0f + expf(-sel_v[s]));
-      z += g[s];
-    }
-    const float inv = 1.0f / z;
-    for (int s = 0; s < k; ++s) {
-      ids[s] = sel_e[s];
-      gates[s] = g[s] * inv;
-    }
-    if (gap) *gap = k < E ? sel_v[k - 1] - next_v : INFINITY;
+  // gates over the k selected: lane s holds selection s
+  const float v0 = __shfl_sync(0xffffffffu, my_v, 0);
+  float g = 0.0f;
+  if (lane < k) g = route == MOE_ROUTE_SOFTMAX ? expf(my_v - v0) : 1.0f / (1.0f + expf(-my_v));
+  float z = g;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+  if (lane < k) {
+    ids[lane] = my_e;
+    gates[lane] = g / z;
   }
+  const float vk = __shfl_sync(0xffffffffu, my_v, (k - 1) & 31);
+  if (lane == 0 && gap) *gap = k < E ? vk - next_v : INFINITY;
 }
 
 __device__ __forceinline__ void warp_topk(const float* l, int E, int k, int route, int lane, int32_t* ids,

@@ -29,6 +29,10 @@ struct WsPlan {
   size_t chunk_cnt;   // int32 [n_chunks * (E + S)]
   size_t bar;         // uint64 grid-barrier counter (inside the status block)
   size_t phase_ns;    // uint64 [16]  phase stamps of the single-launch decode kernel
+  // second/third buffers of the pipelined decode schedule (0 when absent)
+  size_t xq_b[3], xd_b[3], xbs_b[3], logits_b[2], h_b[2], y_b[2];
+  size_t route_pub, route_flag;
+  bool pipeline;
   int max_tiles;
   int n_chunks;
   size_t total;
@@ -94,10 +98,14 @@ struct DecodeArgs {
   const float* x;
   const float* residual;
   float* out;
-  int8_t* xq;
-  float* xd;
-  int16_t* xbs;
-  float* logits;
+  // workspace buffers; [0] is the one moe_workspace_layout names, the others
+  // exist only for the pipelined schedule of a stack (pipeline_ok)
+  int8_t* xq[3];
+  float* xd[3];
+  int16_t* xbs[3];
+  float* logits[2];
+  float* h[2];
+  float* y[2];
   float* gap;
   int32_t* ids;
   float* gates;
@@ -105,11 +113,9 @@ struct DecodeArgs {
   int32_t* offsets;
   int32_t* perm;
   int32_t* inv;
-  float* h;
   int8_t* hq;
   float* hd;
   int16_t* hbs;
-  float* y;
   unsigned long long* bar;
   unsigned long long* phase_ns;   // [16] SM-cycle stamps of CTA 0 (nullable)
   int* status;
@@ -117,8 +123,12 @@ struct DecodeArgs {
   float* gates_out;
   int n_layers;                   // layers of this launch (stack); 1 for one layer
   const moe_layer_ptrs* layers;   // device array of n_layers records, or NULL: use the fields above
+  int pipeline_ok;                // the workspace holds the extra buffers of the pipelined schedule
+  uint8_t* route_pub;             // 4 routing states published by the routing CTA (pipelined schedule)
+  unsigned long long* route_flag; // monotonic count of published routing states
 };
 size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S);
+size_t decode_route_bytes(int T, int k, int S);  // one routing state of the decode kernel
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 // largest token count of the single-launch decode path
 constexpr int kDecodeMaxT = 16;

@@ -111,7 +111,13 @@ typedef struct {
                       barrier 1, [9] top-k done, [10] counts and scan,
                       [11] bucket positions, [3] tile plan done, [4] gate/up
                       done, [5] after barrier 2, [6] down done, [7] after
-                      barrier 3, [8] combine done                             */
+                      barrier 3, [8] combine done; [15] = 1 after the
+                      sequential schedule, 2 after the pipelined one (see
+                      moe_stack_forward); a pipelined run stamps, for the stage
+                      holding the gate/up of layer L-2: [0] stage start, [3]
+                      x staged, [4] gate/up, [6] down of the layer before,
+                      [1] router of layer+2, [8] combine, [12] next layer's
+                      routing taken and its experts prefetched             */
   size_t total;    /* bytes required                                           */
 } moe_ws_layout;
 
@@ -218,10 +224,13 @@ typedef struct {
   float* gates_out;             /* [T, k] or NULL                             */
 } moe_layer_ptrs;
 
-/* A stack of n_layers MoE layers of the same shape, run in order in ONE
- * launch: layer l+1 starts after layer l's output is complete, so a layer's
- * x may point at the previous layer's out (a decode step through the
- * stack).  `layers` is a DEVICE array of n_layers records.  Only the
+/* A stack of n_layers MoE layers of the same shape in ONE launch, with the
+ * results of running them one after the other: a layer's x may point at the
+ * previous layer's out (a decode step through the stack).  When no layer's x
+ * overlaps the outputs of the three layers before it (independent inputs),
+ * the kernel pipelines neighbouring layers (one grid barrier per layer
+ * instead of four); otherwise every layer runs after the previous one has
+ * finished.  Both schedules give the same results.  `layers` is a DEVICE array of n_layers records.  Only the
  * single-launch decode shapes are accepted: T <= 16, T*top_k <= 256, and
  * the layer's staging fits in shared memory; otherwise MOE_ERR_UNSUPPORTED
  * (run moe_layer_forward per layer instead).  ws: one workspace of

@@ -325,6 +325,8 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
     ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
     moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
     assert moe.moe_get_status(ws) == 0
+    marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
+    assert int(marker[15]) == 1          # chained layers run one after the other
     for l in range(L):
         xin = xs[l].cpu().numpy()
         gids = ids[l].cpu().numpy()
@@ -333,6 +335,37 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
         ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xin, residual=xin,
                                             forced_ids=gids)
         assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
+
+
+@pytest.mark.parametrize("fmt,route,S,T,L", [(FMT_Q4K, 0, 1, 1, 6), (FMT_Q2K, 1, 1, 4, 5), (FMT_Q4K, 0, 0, 3, 2)])
+def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
+    """Layers with their own inputs: the kernel pipelines neighbouring layers;
+    every layer must still match the oracle (and the schedule must be the
+    pipelined one)."""
+    H, I, E, k = 512, 512, 32, 6
+    ex = [_experts_host(fmt, E + S, H, I, seed=70 + l, layer=l) for l in range(L)]
+    tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
+    wrs = [synth.router_weight(E, H, 70, l) for l in range(L)]
+    xs_h = [synth.activations(T, H, 70, layer=l) for l in range(L)]
+    xs = [dev(x) for x in xs_h]
+    outs = [torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda") for _ in range(L)]
+    ids = [torch.empty((T, k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
+            for l in range(L)]
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    for rep in range(2):
+        moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
+        assert moe.moe_get_status(ws) == 0
+        marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
+        assert int(marker[15]) == 2
+        for l in range(L):
+            gids = ids[l].cpu().numpy()
+            rl, rids, _, rgap = oracle.route(xs_h[l], wrs[l], None, k, route)
+            routing_ok(gids, rids, rgap, rl)
+            ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xs_h[l],
+                                                residual=xs_h[l], forced_ids=gids)
+            assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
 
 
 def test_stack_forward_rejects_prefill_shapes(moe):
