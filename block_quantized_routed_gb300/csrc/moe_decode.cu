@@ -203,9 +203,6 @@ __device__ __forceinline__ LayerView layer_view(const DecodeArgs& a, int l) {
   return v;
 }
 
-// expert of the o-th entry of the tile order: shared experts first
-__device__ __forceinline__ int tile_order_expert(int o, int E, int S) { return o < S ? E + o : o - S; }
-
 // Per-launch constants and the shared-memory view, passed to every phase.
 template <int FMT>
 struct Ctx {
@@ -244,9 +241,30 @@ struct Ctx {
   __device__ void stamp(int i, bool on) const {
     if (on && blockIdx.x == 0 && tid == 0 && a.phase_ns) a.phase_ns[i] = (unsigned long long)clock64();
   }
-  // down items [begin, end) of this CTA for a layer with n_tiles tiles
+  // Down items of a layer with n_tiles tiles: (tile, group of `per` row
+  // groups).  With enough items for every CTA, a warp owns a whole row group
+  // (by_warp: 8 row groups per item, no cross-warp reduction); otherwise the
+  // warps of a CTA split the super-blocks of rg_per row groups.
+  __device__ void down_plan(int n_tiles, int& per, int& ngrp, bool& by_warp) const {
+    const int nblk = (nRGH + kDecWarps - 1) / kDecWarps;
+    by_warp = (long long)n_tiles * nblk >= W && nbI >= 2;
+    per = by_warp ? kDecWarps : rg_per;
+    ngrp = by_warp ? nblk : n_grp;
+  }
+  // down items to keep in flight towards L2 ahead of use (about 192 KB per CTA)
+  __device__ int down_ahead(int n_tiles) const {
+    int per, ngrp;
+    bool bw;
+    down_plan(n_tiles, per, ngrp, bw);
+    const int n = (int)((size_t)(192 * 1024) / ((size_t)per * dn_rg_bytes));
+    return n < 1 ? 1 : n > kDownAhead ? kDownAhead : n;
+  }
+  // down items [begin, end) of this CTA
   __device__ void down_range(int n_tiles, int& begin, int& end) const {
-    const int n3 = n_tiles * n_grp;
+    int per, ngrp;
+    bool bw;
+    down_plan(n_tiles, per, ngrp, bw);
+    const int n3 = n_tiles * ngrp;
     begin = (int)((long long)n3 * blockIdx.x / W);
     end = (int)((long long)n3 * (blockIdx.x + 1) / W);
   }
@@ -346,43 +364,68 @@ __device__ void routing_phase(Ctx<FMT>& c, const LayerView& lv, const float* log
   const DecodeArgs& a = c.a;
   const int T = c.T, E = c.E, k = c.k, S = c.S, EpS = c.EpS, P = c.P, tid = c.tid;
   Smem& sm = c.sm;
+  for (int e = tid; e < EpS; e += kDecThreads) sm.cnt[e] = 0;
   for (int t = c.warp; t < T; t += kDecWarps)
     warp_topk(logits + (size_t)t * E, E, k, a.route, c.lane, R.ids + t * k, R.gates + t * k,
               writer && a.gap ? a.gap + t : nullptr);
-  for (int e = tid; e < EpS; e += kDecThreads) sm.cnt[e] = 0;
   __syncthreads();
   c.stamp(9, stamps);
+  // counts per expert (low 16 bits) and one "used" mark (bit 16): a single
+  // scan then gives every bucket's offset and every tile's index (tiles in
+  // expert order, shared experts last, like the buckets)
   for (int p = tid; p < T * k; p += kDecThreads) atomicAdd(&sm.cnt[R.ids[p]], 1);
   for (int sh = tid; sh < S; sh += kDecThreads) sm.cnt[E + sh] = T;
+  // presence of each slot's expert (one read of the pointer table)
+  for (int p = tid; p < T * k + S; p += kDecThreads) {
+    const int e = p < T * k ? R.ids[p] : E + (p - T * k);
+    R.ok[p] = lv.table[e].gate != nullptr ? 1 : 0;
+  }
   __syncthreads();
-  if (writer)
-    for (int e = tid; e < EpS; e += kDecThreads) a.counts[e] = sm.cnt[e];
+  for (int e = tid; e < EpS; e += kDecThreads) {
+    const int cnt = sm.cnt[e];
+    if (writer) a.counts[e] = cnt;
+    sm.scan[e] = cnt; // keep the counts
+    sm.cnt[e] = cnt | (cnt > 0 ? 1 << 16 : 0);
+  }
   __syncthreads();
-  const int total = block_exclusive_scan(sm.cnt, EpS);  // sm.cnt: offsets
-  if (tid == 0) sm.cnt[EpS] = total;
-  __syncthreads();
+  const int total = block_exclusive_scan(sm.cnt, EpS);
   c.stamp(10, stamps);
   for (int p = tid; p < T * k; p += kDecThreads) {
     const int e = R.ids[p];
     int rank = 0;
     for (int q = 0; q < p; ++q) rank += (R.ids[q] == e);
-    const int pos = sm.cnt[e] + rank;
+    const int pos = (sm.cnt[e] & 0xFFFF) + rank;
     R.tok[pos] = p / k;
     R.slot[pos] = p;
+    if (rank == 0) {  // the expert's tile
+      Tile tl;
+      tl.expert = e;
+      tl.start = sm.cnt[e] & 0xFFFF;
+      tl.count = sm.scan[e];
+      tl.flag = R.ok[p] ? 0 : 1;
+      R.tiles[sm.cnt[e] >> 16] = tl;
+    }
   }
   for (int i = tid; i < S * T; i += kDecThreads) {
-    const int sh = i / T, t = i % T;
-    const int pos = sm.cnt[E + sh] + t;
+    const int sh = i / T, t = i % T, e = E + sh;
+    const int pos = (sm.cnt[e] & 0xFFFF) + t;
     R.tok[pos] = t;
     R.slot[pos] = T * k + sh * T + t;
+    if (t == 0) {
+      Tile tl;
+      tl.expert = e;
+      tl.start = sm.cnt[e] & 0xFFFF;
+      tl.count = T;
+      tl.flag = R.ok[T * k + sh] ? 0 : 1;
+      R.tiles[sm.cnt[e] >> 16] = tl;
+    }
   }
-  for (int p = tid; p < T * k + S; p += kDecThreads) {  // presence of each slot's expert
-    const int e = p < T * k ? R.ids[p] : E + (p - T * k);
-    R.ok[p] = lv.table[e].gate != nullptr ? 1 : 0;
-  }
+  if (tid == 0) *R.n_tiles = total >> 16;
   __syncthreads();
+  c.stamp(11, stamps);
   if (writer) {
-    for (int e = tid; e <= EpS; e += kDecThreads) a.offsets[e] = sm.cnt[e];
+    for (int e = tid; e < EpS; e += kDecThreads) a.offsets[e] = sm.cnt[e] & 0xFFFF;
+    if (tid == 0) a.offsets[EpS] = total & 0xFFFF;
     for (int j = tid; j < P; j += kDecThreads) {
       a.perm[j] = R.slot[j];
       if (a.inv) a.inv[R.slot[j]] = j;
@@ -394,41 +437,21 @@ __device__ void routing_phase(Ctx<FMT>& c, const LayerView& lv, const float* log
       if (lv.gates_out) lv.gates_out[p] = R.gates[p];
     }
   }
-  c.stamp(11, stamps);
-  // tile plan: one tile per expert used (a tile holds up to T <= 16 rows), shared experts first
-  int* order = sm.scan;
-  for (int o = tid; o < EpS; o += kDecThreads) {
-    const int e = tile_order_expert(o, E, S);
-    order[o] = sm.cnt[e + 1] - sm.cnt[e] > 0 ? 1 : 0;
-  }
-  __syncthreads();
-  const int nt = block_exclusive_scan(order, EpS);
-  for (int o = tid; o < EpS; o += kDecThreads) {
-    const int e = tile_order_expert(o, E, S);
-    const int cc = sm.cnt[e + 1] - sm.cnt[e];
-    if (cc > 0) {
-      Tile tl;
-      tl.expert = e;
-      tl.start = sm.cnt[e];
-      tl.count = cc;
-      tl.flag = lv.table[e].gate == nullptr ? 1 : 0;
-      R.tiles[order[o]] = tl;
-    }
-  }
-  if (tid == 0) *R.n_tiles = nt;
-  __syncthreads();
 }
 
 // L2 prefetch of the down weights of this CTA's down items [i0, i1) of a layer
 template <int FMT>
 __device__ void prefetch_down(const Ctx<FMT>& c, const LayerView& lv, const Route& R, int i0, int i1) {
+  int per, ngrp;
+  bool bw;
+  c.down_plan(*R.n_tiles, per, ngrp, bw);
   while (i0 < i1) {
-    const int ti = i0 / c.n_grp;
-    const int last = min(i1, (ti + 1) * c.n_grp);
+    const int ti = i0 / ngrp;
+    const int last = min(i1, (ti + 1) * ngrp);
     const Tile tl = R.tiles[ti];
     if (!tl.flag) {
-      const int rg0 = (i0 % c.n_grp) * c.rg_per;
-      const int rg1 = min(c.nRGH, ((last - 1) % c.n_grp + 1) * c.rg_per);
+      const int rg0 = (i0 % ngrp) * per;
+      const int rg1 = min(c.nRGH, ((last - 1) % ngrp + 1) * per);
       prefetch_l2(static_cast<const uint8_t*>(lv.table[tl.expert].down) + (size_t)rg0 * c.dn_rg_bytes,
                   (uint32_t)((size_t)(rg1 - rg0) * c.dn_rg_bytes));
     }
@@ -456,7 +479,7 @@ __device__ void prefetch_layer_experts(const Ctx<FMT>& c, const LayerView& lv, c
   for (int it = blockIdx.x; it < n2; it += c.W) prefetch_gateup_item(c, lv, R, it);
   int d0, d1;
   c.down_range(*R.n_tiles, d0, d1);
-  prefetch_down(c, lv, R, d0, min(d1, d0 + kDownAhead));
+  prefetch_down(c, lv, R, d0, min(d1, d0 + c.down_ahead(*R.n_tiles)));
 }
 
 // The whole of every expert a layer uses (gate, up and down matrices), from
@@ -522,7 +545,7 @@ __device__ void gateup_phase(Ctx<FMT>& c, const LayerView& lv, const Route& R, f
         if (first) {
           int d0, d1;
           c.down_range(*R.n_tiles, d0, d1);
-          prefetch_down(c, lv, R, d0, min(d1, d0 + kDownAhead));
+          prefetch_down(c, lv, R, d0, min(d1, d0 + c.down_ahead(*R.n_tiles)));
         }
       }
       sb_accum<FMT>(sg, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, accw, lane);
@@ -545,7 +568,7 @@ __device__ void gateup_phase(Ctx<FMT>& c, const LayerView& lv, const Route& R, f
   if (pf_next && first && tid == 0) {
     int d0, d1;
     c.down_range(*R.n_tiles, d0, d1);
-    prefetch_down(c, lv, R, d0, min(d1, d0 + kDownAhead));
+    prefetch_down(c, lv, R, d0, min(d1, d0 + c.down_ahead(*R.n_tiles)));
   }
 }
 
@@ -560,13 +583,17 @@ __device__ void down_phase(Ctx<FMT>& c, const LayerView& lv, const Route& R, con
   c.down_range(*R.n_tiles, d_begin, d_end);
   for (int t = tid; t < T; t += kDecThreads) sm.aoff[t] = t * I;
   __syncthreads();
+  int per, ngrp;
+  bool by_warp;
+  c.down_plan(*R.n_tiles, per, ngrp, by_warp);
+  const int ahead = c.down_ahead(*R.n_tiles);
   int staged = -1;  // tile whose q8_K(h) is in shared memory
   for (int it = d_begin; it < d_end; ++it) {
-    const int ti = it / c.n_grp;
+    const int ti = it / ngrp;
     const Tile tl = R.tiles[ti];
-    const int grp = it % c.n_grp;
-    const int rg0 = grp * c.rg_per, nrg = min(c.rg_per, c.nRGH - rg0);
-    if (tid == 0 && it + kDownAhead < d_end) prefetch_down(c, lv, R, it + kDownAhead, it + kDownAhead + 1);
+    const int grp = it % ngrp;
+    const int rg0 = grp * per, nrg = min(per, c.nRGH - rg0);
+    if (tid == 0 && it + ahead < d_end) prefetch_down(c, lv, R, it + ahead, it + ahead + 1);
     if (tl.flag) continue;
     if (ti != staged) {
       __syncthreads();  // previous readers of the staged rows are done
@@ -592,6 +619,23 @@ __device__ void down_phase(Ctx<FMT>& c, const LayerView& lv, const Route& R, con
     float* accw = sm.red + (size_t)warp * T * 32;
     for (int i = lane; i < tl.count * 32; i += 32) accw[i] = 0.0f;
     __syncwarp();
+    if (by_warp) {
+      // warp w owns row group rg0 + w: all of its super-blocks, two at a time
+      if (warp < nrg) {
+        const uint8_t* rbase = dbase + (size_t)(rg0 + warp) * c.dn_rg_bytes;
+        for (int b = 0; b < nbI; b += 2) {
+          SbRegs<FMT> s0, s1;
+          load_sb<FMT>(rbase + (size_t)b * F::kSlabBytes, lane, s0);
+          if (b + 1 < nbI) load_sb<FMT>(rbase + (size_t)(b + 1) * F::kSlabBytes, lane, s1);
+          sb_accum<FMT>(s0, sm.hq, sm.hbs, sm.hd, sm.aoff, b, tl.count, accw, lane);
+          if (b + 1 < nbI) sb_accum<FMT>(s1, sm.hq, sm.hbs, sm.hd, sm.aoff, b + 1, tl.count, accw, lane);
+        }
+        __syncwarp();
+        for (int t = 0; t < tl.count; ++t)
+          y[(size_t)R.slot[tl.start + t] * H + (rg0 + warp) * 32 + lane] = accw[t * 32 + lane];
+      }
+      continue;  // no cross-warp reduction; the next tile's staging synchronizes
+    }
     // warp -> (row group, super-blocks)
     const int rgl = nbI >= kDecWarps ? 0 : warp / nbI;
     const int b0 = nbI >= kDecWarps ? warp : warp % nbI;
