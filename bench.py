@@ -77,6 +77,18 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense fp16/bf16 tensor peak (TFLOP/s): the sustained cuBLAS bf16 figure (the GEMMs run inside
+    seconds of back-to-back steps); fp16 and bf16 share one rate on tcgen05 kind::f16."""
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["bf16_tflops_sustained"]), "measured (cuBLAS bf16, sustained)"
+    except (OSError, KeyError, ValueError):
+        return 1700.0, "fallback (sustained)"
+
+
 def kernel_source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_routed_gb300", "csrc")
@@ -282,6 +294,7 @@ def run_ours(args, wl, T):
         stacked = False
         layers = [moe.MoeLayer(desc, tables[l], routers[l], biases[l], device=dev) for l in range(L)]
     torch.cuda.synchronize()
+    path = moe.moe_layer_path(desc, T)
 
     def body():
         if stacked:
@@ -312,12 +325,14 @@ def run_ours(args, wl, T):
     use_graph = not args.no_graph
     graph = None
     moe.moe_trace_events(events)
+    n_launch0 = moe.moe_kernel_launch_count()
     if use_graph:
         graph = torch.cuda.CUDAGraph()
         with torch.cuda.graph(graph):
             body()
     else:
         body()
+    launches_per_step = moe.moe_kernel_launch_count() - n_launch0   # this library's kernels in one step
     n_traced = moe.moe_trace_used()
     moe.moe_trace_events(None)
 
@@ -404,7 +419,23 @@ def run_ours(args, wl, T):
                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
                     "traffic": profiled_traffic(wl.name, "decode_fused_kernel"),
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * launch_ms}
-        launches_per_step = 1
+    elif path == moe.PATH_TENSOR_PREFILL:
+        # the tcgen05 gate/up GEMM (+ SwiGLU) is the dominant kernel; a contraction: tensor-bound
+        gu_ms = [events[4 * l].elapsed_time(events[4 * l + 1]) for l in range(L)]
+        dn_ms = [events[4 * l + 2].elapsed_time(events[4 * l + 3]) for l in range(L)]
+        rows = T * (wl.k + wl.S)                      # bucket rows: every expert is present
+        gu_flop = 2.0 * rows * 2 * wl.I * wl.H
+        dn_flop = 2.0 * rows * wl.H * wl.I
+        tpeak, tpeak_src = measured_tensor_peak()
+        gu_tf = gu_flop / (float(np.mean(gu_ms)) * 1e-3) / 1e12
+        dn_tf = dn_flop / (float(np.mean(dn_ms)) * 1e-3) / 1e12
+        roofline = {"bound": "tensor",
+                    "kernel": "prefill_gemm_kernel<gate/up> (tcgen05 kind::f16 grouped GEMM + SwiGLU)",
+                    "achieved": gu_tf, "peak": tpeak, "unit": "TFLOP/s", "frac": gu_tf / tpeak,
+                    "peak_source": tpeak_src, "traffic": profiled_traffic(wl.name, "prefill_gemm_kernel"),
+                    "algorithmic_flops_per_launch": gu_flop, "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
+                    "down_kernel_tflops": dn_tf, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms)),
+                    "down_frac": dn_tf / tpeak}
     else:
         per_layer = n_traced // L
         if per_layer == 2:
@@ -415,7 +446,6 @@ def run_ours(args, wl, T):
                         "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
                         "traffic": profiled_traffic(wl.name, "decode_fused_kernel"),
                         "algorithmic_bytes_per_launch": float(np.mean(alg)), "avg_launch_us": 1e3 * float(np.mean(fz_ms))}
-            launches_per_step = L
         else:
             gu_ms = [events[4 * l].elapsed_time(events[4 * l + 1]) for l in range(L)]
             dn_ms = [events[4 * l + 2].elapsed_time(events[4 * l + 3]) for l in range(L)]
@@ -429,7 +459,6 @@ def run_ours(args, wl, T):
                         "algorithmic_bytes_per_launch": float(np.mean(gu_alg)),
                         "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
                         "down_kernel_gbs": dn_gbs, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms))}
-            launches_per_step = L * (10 if T * wl.k > 256 else 6)
 
     # end to end through the public call with host buffers: pinned H2D of the
     # step's inputs, the layers, D2H of the outputs, every step
@@ -457,14 +486,17 @@ def run_ours(args, wl, T):
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K, "warmup": W,
         "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "int8 x int4/int2 -> int32 (dp4a) + fp32", "data": "synthetic",
+        "dtype": ("int8 codes x (scale*code) as exact fp16 integers on tcgen05 kind::f16 -> fp32"
+                  if path == moe.PATH_TENSOR_PREFILL else "int8 x int4/int2 -> int32 (dp4a) + fp32"),
+        "data": "synthetic",
         "config": {"workload": wl.name, "layers": L, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.k,
                    "n_shared": wl.S, "route": ["softmax", "sigmoid"][wl.route], "fmt": ["q4_k", "q2_k"][wl.fmt],
                    "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct expert weights "
                          "plus %.0f MB of router weights (L2 129 MB)" % (
                              np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
-                   "graph": use_graph, "rotations": R, "single_launch_stack": stacked},
+                   "graph": use_graph, "rotations": R, "single_launch_stack": stacked,
+                   "path": ["decode_fused", "gemv", "tensor_prefill"][path]},
         "clocks": clock_info,
         "us_per_layer": 1e3 * ms_step / L,
         "active_expert_bytes_per_step": active_bytes_total / K,

@@ -22,7 +22,8 @@ __all__ = [
     "load", "lib", "moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_bucket_workspace_size",
     "moe_expert_ffn", "moe_expert_ffn_workspace_size", "moe_combine", "moe_layer_forward",
     "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
-    "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "expert_table", "MoeLayer",
+    "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
+    "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
 ]
 
 FMT_Q4K = 0
@@ -31,6 +32,10 @@ ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID = 1
 SB_BYTES = {FMT_Q4K: 144, FMT_Q2K: 84}
 N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16}
+
+PATH_DECODE_FUSED = 0
+PATH_GEMV = 1
+PATH_TENSOR_PREFILL = 2
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -91,6 +96,8 @@ def load():
         "moe_debug_subblock_dots": (ctypes.c_int, [I32, P, I32, I32, P, I32, P, P, P]),
         "moe_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), I32]),
         "moe_trace_used": (I32, []),
+        "moe_kernel_launch_count": (ctypes.c_ulonglong, []),
+        "moe_layer_path": (ctypes.c_int, [D, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -249,6 +256,17 @@ def moe_trace_events(events):
 
 def moe_trace_used() -> int:
     return int(load().moe_trace_used())
+
+
+def moe_kernel_launch_count() -> int:
+    return int(load().moe_kernel_launch_count())
+
+
+def moe_layer_path(desc, T) -> int:
+    rc = int(load().moe_layer_path(ctypes.byref(_desc(desc)), T))
+    if rc < 0:
+        raise MoeError(rc, "moe_layer_path")
+    return rc
 
 
 def moe_debug_subblock_dots(fmt, w, N, K, q, isum, bsum, stream=None):

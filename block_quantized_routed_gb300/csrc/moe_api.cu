@@ -1,6 +1,7 @@
 // C ABI of the block-quantized MoE layer: argument validation, workspace
 // plans and the launch sequences.  Every entry point validates on the host
 // before it touches the GPU, so a rejected call launches nothing.
+#include <atomic>
 #include <cstdint>
 #include <cstring>
 
@@ -95,6 +96,11 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
     p.route_pub = c.take(4 * decode_route_bytes((int)T, (int)k, (int)S));
     p.route_flag = c.take(8);
   }
+  if (prefill_path(d.T_max, d.top_k, d.E)) {
+    p.max_pitems = (int)prefill_item_capacity((int64_t)P, d.E, d.n_shared, d.H, d.I);
+    p.pitems = c.take((size_t)p.max_pitems * sizeof(PItem));
+    p.n_pitems = c.take(16);
+  }
   p.total = c.off;
   p.pub.total = p.total;
   return p;
@@ -105,6 +111,12 @@ thread_local void* const* g_trace_events = nullptr;
 thread_local int g_trace_n = 0;
 thread_local int g_trace_next = 0;
 }  // namespace
+
+namespace {
+std::atomic<unsigned long long> g_launches{0};
+}  // namespace
+
+void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 void trace_record(cudaStream_t s) {
   if (!g_trace_events || g_trace_next >= g_trace_n) return;
@@ -342,7 +354,38 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
   }
   if (launch_q8k_quantize(x, T, H, xq, xd, xbs, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_router(x, w_router, router_bias, T, H, E, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if ((int64_t)T * k <= kSmallPairs) {
+  if (prefill_path(T, k, E)) {
+    // prefill chunk: top-k, bucketing, then the tcgen05 grouped GEMMs
+    if (launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    PrefillArgs a{};
+    a.fmt = desc->fmt;
+    a.H = H;
+    a.I = desc->I;
+    a.E = E;
+    a.S = S;
+    a.T = T;
+    a.k = k;
+    a.P = (int64_t)T * (k + S);
+    a.table = table;
+    a.xq = xq;
+    a.xd = xd;
+    a.xbs = xbs;
+    a.counts = counts;
+    a.offsets = offsets;
+    a.perm = perm;
+    a.h = static_cast<float*>(at(p.pub.h));
+    a.hq = static_cast<int8_t*>(at(p.pub.hq));
+    a.hd = static_cast<float*>(at(p.pub.hd));
+    a.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+    a.y = static_cast<float*>(at(p.pub.y));
+    a.items = static_cast<PItem*>(at(p.pitems));
+    a.n_items = static_cast<int32_t*>(at(p.n_pitems));
+    a.max_items = p.max_pitems;
+    a.status = status;
+    if (launch_prefill_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  } else if ((int64_t)T * k <= kSmallPairs) {
     if (launch_route_bucket_small(logits, T, E, k, desc->route, S, ids, gates, gap, counts, offsets, perm, inv, table,
                                   TT, nIB, tiles, n_tiles, req_cnt, status, s) != cudaSuccess)
       return MOE_ERR_CUDA;
@@ -353,30 +396,33 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
     if (launch_plan(counts, offsets, E + S, table, TT, nIB, tiles, n_tiles, req_cnt, s) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  FfnArgs a{};
-  a.fmt = desc->fmt;
-  a.H = H;
-  a.I = desc->I;
-  a.T = T;
-  a.k = k;
-  a.TT = TT;
-  a.table = table;
-  a.xq = xq;
-  a.xd = xd;
-  a.xbs = xbs;
-  a.perm = perm;
-  a.tiles = tiles;
-  a.n_tiles = n_tiles;
-  a.max_tiles = p.max_tiles;
-  a.h = static_cast<float*>(at(p.pub.h));
-  a.hq = static_cast<int8_t*>(at(p.pub.hq));
-  a.hd = static_cast<float*>(at(p.pub.hd));
-  a.hbs = static_cast<int16_t*>(at(p.pub.hbs));
-  a.req_cnt = req_cnt;
-  a.y = static_cast<float*>(at(p.pub.y));
-  a.status = status;
-  if (launch_expert_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_combine(a.y, gates, T, H, k, S, residual, out, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!prefill_path(T, k, E)) {
+    FfnArgs a{};
+    a.fmt = desc->fmt;
+    a.H = H;
+    a.I = desc->I;
+    a.T = T;
+    a.k = k;
+    a.TT = TT;
+    a.table = table;
+    a.xq = xq;
+    a.xd = xd;
+    a.xbs = xbs;
+    a.perm = perm;
+    a.tiles = tiles;
+    a.n_tiles = n_tiles;
+    a.max_tiles = p.max_tiles;
+    a.h = static_cast<float*>(at(p.pub.h));
+    a.hq = static_cast<int8_t*>(at(p.pub.hq));
+    a.hd = static_cast<float*>(at(p.pub.hd));
+    a.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+    a.req_cnt = req_cnt;
+    a.y = static_cast<float*>(at(p.pub.y));
+    a.status = status;
+    if (launch_expert_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (launch_combine(static_cast<float*>(at(p.pub.y)), gates, T, H, k, S, residual, out, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (ids_out && cudaMemcpyAsync(ids_out, ids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (gates_out &&
@@ -477,6 +523,19 @@ int moe_trace_events(void* const* events, int32_t n_events) {
   g_trace_n = n_events;
   g_trace_next = 0;
   return MOE_OK;
+}
+
+unsigned long long moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (T < 0 || T > desc->T_max) return MOE_ERR_INVALID_ARG;
+  const int k = desc->top_k;
+  if (T <= kDecodeMaxT && (int64_t)T * k <= kSmallPairs &&
+      decode_smem_bytes(T, desc->H, desc->I, desc->E, k, desc->n_shared) <= kDecodeSmemMax)
+    return MOE_PATH_DECODE_FUSED;
+  return prefill_path(T, k, desc->E) ? MOE_PATH_TENSOR_PREFILL : MOE_PATH_GEMV;
 }
 
 int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }

@@ -849,6 +849,7 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   const int grid = num_sms() * std::min(per_sm, 2);
   DecodeArgs args = a;
   void* params[] = {&args};
+  note_launch();
   return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kDecThreads), params,
                                      smem, s);
 }

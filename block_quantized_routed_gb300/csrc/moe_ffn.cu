@@ -271,6 +271,7 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
     const int64_t max_items = (int64_t)a.max_tiles * (a.I / 32);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_items, (int64_t)std::max(per_sm, 1) * sms));
     trace_record(s);
+    note_launch();
     kern<<<grid, kThreads, smem, s>>>(a);
     err = cudaGetLastError();
     trace_record(s);
@@ -285,6 +286,7 @@ cudaError_t launch_ffn_t(const FfnArgs& a, cudaStream_t s) {
     const int64_t max_items = (int64_t)a.max_tiles * (a.H / 128);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(max_items, (int64_t)std::max(per_sm, 1) * sms));
     trace_record(s);
+    note_launch();
     kern<<<grid, kThreads, smem, s>>>(a);
     err = cudaGetLastError();
     trace_record(s);
@@ -309,6 +311,7 @@ cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int
                            float* out, cudaStream_t s) {
   const int64_t n = (int64_t)T * (H / 4);
   if (n == 0) return cudaSuccess;
+  note_launch();
   combine_kernel<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(y, gates, T, H, k, S, residual, out);
   return cudaGetLastError();
 }
@@ -316,6 +319,7 @@ cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int
 cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t* q, int T, int32_t* isum,
                               int32_t* bsum, cudaStream_t s) {
   const int blocks = (N / 32) * (K / 256);
+  note_launch();
   if (fmt == kQ4K)
     debug_dots_kernel<kQ4K><<<blocks, 32, 0, s>>>(static_cast<const uint8_t*>(w), N, K, q, T, isum, bsum);
   else

@@ -33,6 +33,9 @@ struct WsPlan {
   size_t xq_b[3], xd_b[3], xbs_b[3], logits_b[2], h_b[2], y_b[2];
   size_t route_pub, route_flag;
   bool pipeline;
+  // work items of the tensor-core prefill path (0 when the shape never takes it)
+  size_t pitems, n_pitems;
+  int max_pitems;
   int max_tiles;
   int n_chunks;
   size_t total;
@@ -88,6 +91,8 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 
 // profiling hook state (per host thread): records the next event if tracing
 void trace_record(cudaStream_t s);
+// counts every kernel launch the library issues (moe_kernel_launch_count)
+void note_launch();
 
 // Single-launch decode layer (cooperative kernel); see moe_decode.cu.
 struct DecodeArgs {
@@ -132,6 +137,43 @@ size_t decode_route_bytes(int T, int k, int S);  // one routing state of the dec
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 // largest token count of the single-launch decode path
 constexpr int kDecodeMaxT = 16;
+
+// ---- tensor-core prefill path (moe_prefill.cu) ------------------------------
+// Experts must average at least this many routed tokens for the tcgen05
+// grouped GEMM to beat the dp4a GEMV kernels.
+constexpr int kPrefillMinTokensPerExpert = 16;
+inline bool prefill_path(int64_t T, int k, int E) {
+  return T * k > kSmallPairs && T * k >= (int64_t)kPrefillMinTokensPerExpert * E;
+}
+// one unit of prefill GEMM work: a token tile of one expert x a weight tile
+struct PItem {
+  int expert;  // expert index (routed, then shared)
+  int start;   // first bucket position of the token tile
+  int count;   // tokens in the tile (<= 128)
+  int wtile;   // gate/up: 64-row group of I (its gate and up rows); down: 128-row group of H
+};
+size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I);
+struct PrefillArgs {
+  int fmt, H, I, E, S, T, k;
+  int64_t P;                     // bucket positions = T * (k + S)
+  const moe_expert_ptrs* table;
+  const int8_t* xq;
+  const float* xd;
+  const int16_t* xbs;
+  const int32_t* counts;
+  const int32_t* offsets;
+  const int32_t* perm;
+  float* h;                      // [P, I] bucket order
+  int8_t* hq;
+  float* hd;
+  int16_t* hbs;
+  float* y;                      // slot-indexed [P, H]
+  PItem* items;
+  int32_t* n_items;
+  int max_items;
+  int* status;
+};
+cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s);
 
 cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S,
                            const float* residual, float* out, cudaStream_t s);

@@ -73,6 +73,85 @@ __global__ void __launch_bounds__(128) router_kernel(const float* __restrict__ x
   }
 }
 
+// Router logits of many tokens: logits[T, E] = x[T, H] * W[E, H]^T + bias, an
+// fp32 GEMM (the gate stays in fp32: top-k picks are decided on these values).
+// Tile 128 tokens x 128 experts per CTA, K steps of 16 staged in shared
+// memory (double-buffered), 256 threads each holding an 8 x 8 register tile
+// (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise): every thread
+// reads float4 pairs from shared memory per k and issues 64 FMAs.
+constexpr int kRgTile = 128, kRgK = 16, kRgPad = 4;
+// token count from which the tiled GEMM replaces the per-expert GEMV
+constexpr int kRouterGemmMinT = 64;
+
+__global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restrict__ x, const float* __restrict__ w,
+                                                          const float* __restrict__ bias, int T, int H, int E,
+                                                          float* __restrict__ logits) {
+  __shared__ __align__(16) float sx[2][kRgK][kRgTile + kRgPad];
+  __shared__ __align__(16) float sw[2][kRgK][kRgTile + kRgPad];
+  const int tid = threadIdx.x, tx = tid & 15, ty = tid >> 4;
+  const int t0 = blockIdx.y * kRgTile, e0 = blockIdx.x * kRgTile;
+  // loader: rows lr and lr + 64 of each tile, k quad lk (4 floats)
+  const int lr = tid >> 2, lk = (tid & 3) * 4;
+  const float* xr0 = t0 + lr < T ? x + (int64_t)(t0 + lr) * H : nullptr;
+  const float* xr1 = t0 + lr + 64 < T ? x + (int64_t)(t0 + lr + 64) * H : nullptr;
+  const float* wr0 = e0 + lr < E ? w + (int64_t)(e0 + lr) * H : nullptr;
+  const float* wr1 = e0 + lr + 64 < E ? w + (int64_t)(e0 + lr + 64) * H : nullptr;
+  const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+  auto fetch = [&](int k0, float4 (&v)[4]) {
+    v[0] = xr0 ? __ldg(reinterpret_cast<const float4*>(xr0 + k0 + lk)) : z;
+    v[1] = xr1 ? __ldg(reinterpret_cast<const float4*>(xr1 + k0 + lk)) : z;
+    v[2] = wr0 ? __ldg(reinterpret_cast<const float4*>(wr0 + k0 + lk)) : z;
+    v[3] = wr1 ? __ldg(reinterpret_cast<const float4*>(wr1 + k0 + lk)) : z;
+  };
+  auto stash = [&](int buf, const float4 (&v)[4]) {
+    sx[buf][lk + 0][lr] = v[0].x; sx[buf][lk + 1][lr] = v[0].y; sx[buf][lk + 2][lr] = v[0].z; sx[buf][lk + 3][lr] = v[0].w;
+    sx[buf][lk + 0][lr + 64] = v[1].x; sx[buf][lk + 1][lr + 64] = v[1].y;
+    sx[buf][lk + 2][lr + 64] = v[1].z; sx[buf][lk + 3][lr + 64] = v[1].w;
+    sw[buf][lk + 0][lr] = v[2].x; sw[buf][lk + 1][lr] = v[2].y; sw[buf][lk + 2][lr] = v[2].z; sw[buf][lk + 3][lr] = v[2].w;
+    sw[buf][lk + 0][lr + 64] = v[3].x; sw[buf][lk + 1][lr + 64] = v[3].y;
+    sw[buf][lk + 2][lr + 64] = v[3].z; sw[buf][lk + 3][lr + 64] = v[3].w;
+  };
+  float acc[8][8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[i][j] = 0.0f;
+  float4 v[4];
+  fetch(0, v);
+  stash(0, v);
+  __syncthreads();
+  const int nk = H / kRgK;
+  for (int kt = 0; kt < nk; ++kt) {
+    const int buf = kt & 1;
+    if (kt + 1 < nk) fetch((kt + 1) * kRgK, v);
+#pragma unroll
+    for (int kk = 0; kk < kRgK; ++kk) {
+      const float4 a0 = *reinterpret_cast<const float4*>(&sx[buf][kk][ty * 4]);
+      const float4 a1 = *reinterpret_cast<const float4*>(&sx[buf][kk][64 + ty * 4]);
+      const float4 b0 = *reinterpret_cast<const float4*>(&sw[buf][kk][tx * 4]);
+      const float4 b1 = *reinterpret_cast<const float4*>(&sw[buf][kk][64 + tx * 4]);
+      const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+      const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc[i][j] = fmaf(av[i], bv[j], acc[i][j]);
+    }
+    if (kt + 1 < nk) stash(buf ^ 1, v);
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + (i < 4 ? ty * 4 + i : 64 + ty * 4 + i - 4);
+    if (t >= T) continue;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      const int e = e0 + (j < 4 ? tx * 4 + j : 64 + tx * 4 + j - 4);
+      if (e < E) logits[(int64_t)t * E + e] = acc[i][j] + (bias ? __ldg(bias + e) : 0.0f);
+    }
+  }
+}
+
 // ---------------------------------------------------------------- top-k
 __global__ void __launch_bounds__(128) topk_kernel(const float* __restrict__ logits, int T, int E, int k,
                                                    int route, int32_t* __restrict__ ids,
@@ -263,6 +342,7 @@ cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q,
   const int64_t nblocks = T * (K / 256);
   if (nblocks == 0) return cudaSuccess;
   const int per = 8;  // warps (blocks of 256 elements) per CTA
+  note_launch();
   q8k_quantize_kernel<<<(unsigned)((nblocks + per - 1) / per), 32 * per, 0, s>>>(x, nblocks, q, d, bs);
   return cudaGetLastError();
 }
@@ -270,8 +350,15 @@ cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q,
 cudaError_t launch_router(const float* x, const float* w, const float* bias, int T, int H, int E, float* logits,
                           cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  if (T >= kRouterGemmMinT) {
+    const dim3 grid((E + kRgTile - 1) / kRgTile, (T + kRgTile - 1) / kRgTile);
+    note_launch();
+    router_gemm_kernel<<<grid, 256, 0, s>>>(x, w, bias, T, H, E, logits);
+    return cudaGetLastError();
+  }
   const int warps = 2;                       // rows per CTA: spread the rows over many SMs
   int grid = (E + warps - 1) / warps;
+  note_launch();
   router_kernel<<<grid, 32 * warps, 0, s>>>(x, w, bias, T, H, E, logits);
   return cudaGetLastError();
 }
@@ -279,6 +366,7 @@ cudaError_t launch_router(const float* x, const float* w, const float* bias, int
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int route, int32_t* ids, float* gates,
                         float* gap, cudaStream_t s) {
   if (T == 0) return cudaSuccess;
+  note_launch();
   topk_kernel<<<(T + 3) / 4, 128, 0, s>>>(logits, T, E, k, route, ids, gates, gap);
   return cudaGetLastError();
 }
@@ -287,6 +375,7 @@ cudaError_t launch_route_bucket_small(const float* logits, int T, int E, int k, 
                                       float* gates, float* gap, int32_t* counts, int32_t* offsets, int32_t* perm,
                                       int32_t* inv, const moe_expert_ptrs* table, int TT, int nIB, Tile* tiles,
                                       int32_t* n_tiles, int32_t* req_cnt, int* status, cudaStream_t s) {
+  note_launch();
   route_bucket_small_kernel<<<1, 1024, 0, s>>>(logits, T, E, k, route, S, ids, gates, gap, counts, offsets, perm,
                                                 inv, table, TT, nIB, tiles, n_tiles, req_cnt, status);
   return cudaGetLastError();
@@ -297,13 +386,16 @@ cudaError_t launch_bucket_large(const int32_t* ids, int T, int k, int E, int S, 
   const int P = T * k;
   const int n_chunks = (P + kBucketChunk - 1) / kBucketChunk;
   if (n_chunks > 0) {
+    note_launch();
     bucket_count_kernel<<<n_chunks, 1024, 0, s>>>(ids, P, E, E + S, chunk_cnt, status);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
   }
+  note_launch();
   bucket_scan_kernel<<<1, 1024, 0, s>>>(chunk_cnt, n_chunks, T, E, S, counts, offsets);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
+  note_launch();
   bucket_scatter_kernel<<<n_chunks > 0 ? n_chunks : 1, 1024, 0, s>>>(ids, T, k, E, S, chunk_cnt, offsets, perm,
                                                                      inv);
   return cudaGetLastError();
@@ -311,6 +403,7 @@ cudaError_t launch_bucket_large(const int32_t* ids, int T, int k, int E, int S, 
 
 cudaError_t launch_plan(const int32_t* counts, const int32_t* offsets, int EpS, const moe_expert_ptrs* table,
                         int TT, int nIB, Tile* tiles, int32_t* n_tiles, int32_t* req_cnt, cudaStream_t s) {
+  note_launch();
   plan_kernel<<<1, 1024, 0, s>>>(counts, offsets, EpS, table, TT, nIB, tiles, n_tiles, req_cnt);
   return cudaGetLastError();
 }

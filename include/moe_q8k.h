@@ -295,6 +295,28 @@ int moe_trace_events(void* const* events, int32_t n_events);
 /* Number of entries recorded since the last moe_trace_events call. */
 int32_t moe_trace_used(void);
 
+/* Total number of kernel launches this library has issued in the process
+ * (all host threads, all devices), including launches recorded into a CUDA
+ * graph during stream capture.  The difference across one call counts that
+ * call's kernels.  This library has no other side effect to observe. */
+unsigned long long moe_kernel_launch_count(void);
+
+/* Which implementation moe_layer_forward uses for T tokens of `desc`
+ * (no device work):
+ *   MOE_PATH_DECODE_FUSED   one cooperative launch (T <= 16, T*top_k <= 256
+ *                           and the routing state fits the kernel's shared
+ *                           memory; if the device cannot make the grid
+ *                           co-resident the call falls back to the GEMV path)
+ *   MOE_PATH_GEMV           separate routing / bucketing / dp4a GEMV kernels
+ *   MOE_PATH_TENSOR_PREFILL tcgen05 grouped GEMMs over the expert buckets
+ *                           (T*top_k > 256 and T*top_k >= 16 * E: experts
+ *                           average at least 16 routed tokens)
+ * Returns one of them, or a negative status for an invalid descriptor or T. */
+#define MOE_PATH_DECODE_FUSED 0
+#define MOE_PATH_GEMV 1
+#define MOE_PATH_TENSOR_PREFILL 2
+int moe_layer_path(const moe_layer_desc* desc, int32_t T);
+
 /* Test hook: the integer sub-block sums of the device dot routine that the
  * expert kernels use, for matrix w [N, K] against q8_K codes q [T, K]:
  *   isum int32 [T, N, K/256, n_sub] = sum over sub-block j of q_w * q_a,

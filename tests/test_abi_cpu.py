@@ -103,3 +103,30 @@ def test_host_validation_rejects_before_launch(lib):
     assert L.moe_get_status(None, None) == moe.MOE_ERR_INVALID_ARG
     assert moe.moe_bucket_workspace_size(8192, 10, 512, 1) >= 80 * 513 * 4
     assert moe.moe_expert_ffn_workspace_size(d, 5) == 0
+
+
+def test_layer_path_selection(lib):
+    assert moe.moe_layer_path(desc(), 1) == moe.PATH_DECODE_FUSED
+    # 40 tokens x 10 of 40 experts: 400 pairs, 10 per expert -> GEMV kernels
+    assert moe.moe_layer_path(desc(H=512, I=256, E=40, top_k=10, T_max=40), 40) == moe.PATH_GEMV
+    d = desc(H=4096, I=1024, E=512, top_k=10, T_max=8192)
+    assert moe.moe_layer_path(d, 8192) == moe.PATH_TENSOR_PREFILL
+    assert moe.moe_layer_path(d, 820) == moe.PATH_TENSOR_PREFILL      # 8200 pairs >= 16 * 512
+    assert moe.moe_layer_path(d, 819) == moe.PATH_GEMV
+    assert moe.moe_layer_path(d, 16) == moe.PATH_DECODE_FUSED
+    assert moe.moe_layer_path(d, 26) == moe.PATH_GEMV                 # 260 pairs: beyond the single-CTA routing
+    with pytest.raises(moe.MoeError):
+        moe.moe_layer_path(d, 8193)
+    with pytest.raises(moe.MoeError):
+        moe.moe_layer_path(desc(H=300), 1)
+    # the prefill work-item region exists only where the path can be taken
+    assert moe.moe_layer_workspace_size(desc(H=4096, I=1024, E=512, top_k=10, T_max=819)) < \
+        moe.moe_layer_workspace_size(desc(H=4096, I=1024, E=512, top_k=10, T_max=820)) - 16 * 1000
+
+
+def test_kernel_launch_count_is_monotonic(lib):
+    a = moe.moe_kernel_launch_count()
+    L = moe.load()
+    fake = ctypes.c_void_p(0x10000)
+    assert L.moe_q8k_quantize(fake, 0, 256, fake, fake, None, None) == moe.MOE_OK   # T = 0: nothing launched
+    assert moe.moe_kernel_launch_count() == a >= 0

@@ -105,7 +105,9 @@ def test_subblock_dots_extreme_codes(moe):
 
 @pytest.mark.parametrize("route", [0, 1])
 @pytest.mark.parametrize("T,H,E,k,bias", [(1, 2048, 256, 8, False), (4, 4096, 512, 10, False),
-                                          (16, 6144, 192, 8, True), (37, 512, 16, 2, False), (5, 256, 4, 4, False)])
+                                          (16, 6144, 192, 8, True), (37, 512, 16, 2, False), (5, 256, 4, 4, False),
+                                          # tiled router GEMM: ragged token and expert tiles
+                                          (200, 1024, 300, 6, True), (640, 4096, 512, 10, False)])
 def test_route_topk(moe, route, T, H, E, k, bias):
     x = synth.activations(T, H, 11)
     wr = synth.router_weight(E, H, 11)
@@ -226,6 +228,10 @@ CASES = [
     (FMT_Q2K, 0, 256, 256, 8, 8, 1, 3, False),       # k = E
     (FMT_Q4K, 1, 256, 768, 1, 1, 0, 7, False),       # one expert
     (FMT_Q4K, 1, 512, 256, 40, 10, 1, 40, False),    # more than the single-CTA bucket (400 pairs)
+    # prefill chunks (tensor-core grouped GEMM): several 128-token tiles per expert, ragged tails
+    (FMT_Q4K, 0, 512, 256, 8, 2, 1, 512, False),
+    (FMT_Q2K, 1, 768, 512, 16, 4, 0, 300, True),     # skewed router: some experts far above 128 tokens
+    (FMT_Q4K, 1, 1024, 256, 4, 1, 2, 257, False),    # two shared experts, one routed slot per token
 ]
 
 
@@ -274,8 +280,9 @@ def test_layer_forward_is_deterministic(moe):
     np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
-def test_layer_forward_null_expert_is_not_mine(moe):
-    fmt, H, I, E, k, S, T = FMT_Q4K, 512, 256, 8, 2, 1, 6
+@pytest.mark.parametrize("T", [6, 512])
+def test_layer_forward_null_expert_is_not_mine(moe, T):
+    fmt, H, I, E, k, S = FMT_Q4K, 512, 256, 8, 2, 1
     ex = _experts_host(fmt, E + S, H, I, 8)
     wr = synth.router_weight(E, H, 8)
     x = synth.activations(T, H, 8)
