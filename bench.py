@@ -387,6 +387,15 @@ def run_ours(args, wl, T):
     phases = None
     phase_ws = ws if stacked else layers[-1].ws
     st = moe.MoeLayer.ws_view_of(phase_ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,)).cpu().numpy()
+    if path == moe.PATH_TENSOR_PREFILL:
+        # wait statistics of the GEMMs' CTA 0 (SM cycles): per role, then the CTA's total
+        mhz = clock_info.get("sm_mhz") or 2070.0
+        names = ["producer_wait_raw_slot", "producer_wait_act_slot", "expander_wait_raw", "expander_wait_slot",
+                 "mma_wait_accum", "mma_wait_operands", "epilogue_wait_accum", "cta_total"]
+        phases = {"schedule": "prefill_gemm_waits",
+                  "gate_up": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[0:8])},
+                  "down": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[8:16])}}
+        st = np.zeros(16, np.int64)
     if st[15] == 2:   # pipelined schedule: one stage
         order = [0, 3, 4, 6, 1, 8, 12]
         names = ["stage_x", "gate_up", "down_prev", "router_next2", "combine_prev2", "wait_route_next+prefetch"]

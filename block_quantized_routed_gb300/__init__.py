@@ -49,7 +49,10 @@ MOE_ERR_DEVICE_TIMEOUT = -6
 class MoeError(RuntimeError):
     def __init__(self, status: int, where: str):
         self.status = status
-        super().__init__(f"{where}: {moe_status_string(status)} ({status})")
+        extra = ""
+        if status == MOE_ERR_CUDA:
+            extra = f", cudaError {int(load().moe_last_cuda_error())}"
+        super().__init__(f"{where}: {moe_status_string(status)} ({status}{extra})")
 
 
 class LayerDesc(ctypes.Structure):
@@ -97,6 +100,7 @@ def load():
         "moe_trace_events": (ctypes.c_int, [ctypes.POINTER(ctypes.c_void_p), I32]),
         "moe_trace_used": (I32, []),
         "moe_kernel_launch_count": (ctypes.c_ulonglong, []),
+        "moe_last_cuda_error": (ctypes.c_int, []),
         "moe_layer_path": (ctypes.c_int, [D, I32]),
     }
     for name, (res, args) in sig.items():

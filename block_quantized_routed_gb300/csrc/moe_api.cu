@@ -1,6 +1,7 @@
 // C ABI of the block-quantized MoE layer: argument validation, workspace
 // plans and the launch sequences.  Every entry point validates on the host
 // before it touches the GPU, so a rejected call launches nothing.
+#include <algorithm>
 #include <atomic>
 #include <cstdint>
 #include <cstring>
@@ -29,7 +30,7 @@ struct Carve {
 
 cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
 
-int check(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+int check(cudaError_t e) { return record_error(e) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
 }  // namespace
 
@@ -96,10 +97,14 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
     p.route_pub = c.take(4 * decode_route_bytes((int)T, (int)k, (int)S));
     p.route_flag = c.take(8);
   }
-  if (prefill_path(d.T_max, d.top_k, d.E)) {
+  if (prefill_path(d.T_max, d.top_k, d.E) && prefill_fits(d.T_max, d)) {
     p.max_pitems = (int)prefill_item_capacity((int64_t)P, d.E, d.n_shared, d.H, d.I);
     p.pitems = c.take((size_t)p.max_pitems * sizeof(PItem));
     p.n_pitems = c.take(16);
+    const size_t Kmax = std::max(H, I);
+    p.pxg = c.take(P * Kmax * 2);
+    p.psg = c.take((Kmax / 256) * 2 * P * 16);
+    p.pdg = c.take((Kmax / 256) * P * 4);
   }
   p.total = c.off;
   p.pub.total = p.total;
@@ -114,7 +119,14 @@ thread_local int g_trace_next = 0;
 
 namespace {
 std::atomic<unsigned long long> g_launches{0};
+thread_local int g_last_error = 0;
 }  // namespace
+
+cudaError_t record_error(cudaError_t e) {
+  if (e != cudaSuccess) g_last_error = (int)e;
+  return e;
+}
+int last_error() { return g_last_error; }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
@@ -168,7 +180,7 @@ int moe_route_topk(const float* x, const float* w_router, const float* bias, int
   if (!aligned(x, 16) || !aligned(w_router, 16)) return MOE_ERR_INVALID_ARG;
   cudaStream_t s = as_stream(stream);
   cudaError_t e = launch_router(x, w_router, bias, T, H, E, logits, s);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_error(e) != cudaSuccess) return MOE_ERR_CUDA;
   return check(launch_topk(logits, T, E, k, route, ids, gates, gap, s));
 }
 
@@ -236,7 +248,7 @@ int moe_expert_ffn(const moe_layer_desc* desc, const moe_expert_ptrs* table, con
   const int TT = pick_tile_tokens(T, desc->H);
   const int EpS = desc->E + desc->n_shared;
   int32_t* n_tiles = status + 1;
-  if (launch_plan(counts, offsets, EpS, table, TT, desc->I / 256, tiles, n_tiles, req_cnt, s) != cudaSuccess)
+  if (record_error(launch_plan(counts, offsets, EpS, table, TT, desc->I / 256, tiles, n_tiles, req_cnt, s)) != cudaSuccess)
     return MOE_ERR_CUDA;
   a.fmt = desc->fmt;
   a.H = desc->H;
@@ -345,19 +357,20 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
       d.n_layers = 1;
       d.layers = nullptr;
       trace_record(s);
-      const cudaError_t err = launch_decode_fused(d, s);
+      const cudaError_t err = record_error(launch_decode_fused(d, s));
       trace_record(s);
       if (err == cudaSuccess) return MOE_OK;
       if (err != cudaErrorCooperativeLaunchTooLarge) return MOE_ERR_CUDA;
       cudaGetLastError();  // not co-resident on this device: use the multi-kernel path
     }
   }
-  if (launch_q8k_quantize(x, T, H, xq, xd, xbs, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_router(x, w_router, router_bias, T, H, E, logits, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (prefill_path(T, k, E)) {
+  if (record_error(launch_q8k_quantize(x, T, H, xq, xd, xbs, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_error(launch_router(x, w_router, router_bias, T, H, E, logits, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  const bool use_prefill = prefill_path(T, k, E) && prefill_fits(desc->T_max, *desc);  // buffers sized by T_max
+  if (use_prefill) {
     // prefill chunk: top-k, bucketing, then the tcgen05 grouped GEMMs
-    if (launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s) != cudaSuccess)
+    if (record_error(launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (record_error(launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s)) != cudaSuccess)
       return MOE_ERR_CUDA;
     PrefillArgs a{};
     a.fmt = desc->fmt;
@@ -380,23 +393,27 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
     a.hd = static_cast<float*>(at(p.pub.hd));
     a.hbs = static_cast<int16_t*>(at(p.pub.hbs));
     a.y = static_cast<float*>(at(p.pub.y));
+    a.xg = at(p.pxg);
+    a.sg = at(p.psg);
+    a.dg = static_cast<float*>(at(p.pdg));
     a.items = static_cast<PItem*>(at(p.pitems));
     a.n_items = static_cast<int32_t*>(at(p.n_pitems));
     a.max_items = p.max_pitems;
     a.status = status;
-    if (launch_prefill_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+    a.stats = static_cast<unsigned long long*>(at(p.phase_ns));
+    if (record_error(launch_prefill_ffn(a, s)) != cudaSuccess) return MOE_ERR_CUDA;
   } else if ((int64_t)T * k <= kSmallPairs) {
-    if (launch_route_bucket_small(logits, T, E, k, desc->route, S, ids, gates, gap, counts, offsets, perm, inv, table,
-                                  TT, nIB, tiles, n_tiles, req_cnt, status, s) != cudaSuccess)
+    if (record_error(launch_route_bucket_small(logits, T, E, k, desc->route, S, ids, gates, gap, counts, offsets, perm, inv, table,
+                                  TT, nIB, tiles, n_tiles, req_cnt, status, s)) != cudaSuccess)
       return MOE_ERR_CUDA;
   } else {
-    if (launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s) != cudaSuccess) return MOE_ERR_CUDA;
-    if (launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s) != cudaSuccess)
+    if (record_error(launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (record_error(launch_bucket_large(ids, T, k, E, S, counts, offsets, perm, inv, chunk_cnt, status, s)) != cudaSuccess)
       return MOE_ERR_CUDA;
-    if (launch_plan(counts, offsets, E + S, table, TT, nIB, tiles, n_tiles, req_cnt, s) != cudaSuccess)
+    if (record_error(launch_plan(counts, offsets, E + S, table, TT, nIB, tiles, n_tiles, req_cnt, s)) != cudaSuccess)
       return MOE_ERR_CUDA;
   }
-  if (!prefill_path(T, k, E)) {
+  if (!use_prefill) {
     FfnArgs a{};
     a.fmt = desc->fmt;
     a.H = H;
@@ -419,9 +436,9 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
     a.req_cnt = req_cnt;
     a.y = static_cast<float*>(at(p.pub.y));
     a.status = status;
-    if (launch_expert_ffn(a, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (record_error(launch_expert_ffn(a, s)) != cudaSuccess) return MOE_ERR_CUDA;
   }
-  if (launch_combine(static_cast<float*>(at(p.pub.y)), gates, T, H, k, S, residual, out, s) != cudaSuccess)
+  if (record_error(launch_combine(static_cast<float*>(at(p.pub.y)), gates, T, H, k, S, residual, out, s)) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (ids_out && cudaMemcpyAsync(ids_out, ids, sizeof(int32_t) * T * k, cudaMemcpyDeviceToDevice, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -484,7 +501,7 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   d.layers = layers;
   cudaStream_t s = as_stream(stream);
   trace_record(s);
-  const cudaError_t err = launch_decode_fused(d, s);
+  const cudaError_t err = record_error(launch_decode_fused(d, s));
   trace_record(s);
   if (err == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();
@@ -495,9 +512,9 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
 
 int moe_get_status(void* ws, void* stream) {
   if (!ws) return MOE_ERR_INVALID_ARG;
-  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_error(cudaStreamSynchronize(as_stream(stream))) != cudaSuccess) return MOE_ERR_CUDA;
   int v = 0;
-  if (cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_error(cudaMemcpy(&v, ws, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess) return MOE_ERR_CUDA;
   // clear the status block (status word, tile count and the grid-barrier
   // counter, which a timed-out barrier leaves out of step)
   if (v != 0 && cudaMemset(ws, 0, 16) != cudaSuccess) return MOE_ERR_CUDA;
@@ -525,6 +542,8 @@ int moe_trace_events(void* const* events, int32_t n_events) {
   return MOE_OK;
 }
 
+int moe_last_cuda_error(void) { return last_error(); }
+
 unsigned long long moe_kernel_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
@@ -535,7 +554,7 @@ int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
   if (T <= kDecodeMaxT && (int64_t)T * k <= kSmallPairs &&
       decode_smem_bytes(T, desc->H, desc->I, desc->E, k, desc->n_shared) <= kDecodeSmemMax)
     return MOE_PATH_DECODE_FUSED;
-  return prefill_path(T, k, desc->E) ? MOE_PATH_TENSOR_PREFILL : MOE_PATH_GEMV;
+  return prefill_path(T, k, desc->E) && prefill_fits(desc->T_max, *desc) ? MOE_PATH_TENSOR_PREFILL : MOE_PATH_GEMV;
 }
 
 int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }

@@ -34,7 +34,7 @@ struct WsPlan {
   size_t route_pub, route_flag;
   bool pipeline;
   // work items of the tensor-core prefill path (0 when the shape never takes it)
-  size_t pitems, n_pitems;
+  size_t pitems, n_pitems, pxg, psg, pdg;
   int max_pitems;
   int max_tiles;
   int n_chunks;
@@ -93,6 +93,8 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s);
 void trace_record(cudaStream_t s);
 // counts every kernel launch the library issues (moe_kernel_launch_count)
 void note_launch();
+// remembers a failed CUDA call of this host thread (moe_last_cuda_error); returns e
+cudaError_t record_error(cudaError_t e);
 
 // Single-launch decode layer (cooperative kernel); see moe_decode.cu.
 struct DecodeArgs {
@@ -145,6 +147,12 @@ constexpr int kPrefillMinTokensPerExpert = 16;
 inline bool prefill_path(int64_t T, int k, int E) {
   return T * k > kSmallPairs && T * k >= (int64_t)kPrefillMinTokensPerExpert * E;
 }
+// TMA coordinates are 32-bit: the code-sum plane has (max(H, I)/256) * 2 * P rows
+inline bool prefill_fits(int64_t T, const moe_layer_desc& d) {
+  const int64_t P = T * (d.top_k + d.n_shared);
+  const int64_t K = d.H > d.I ? d.H : d.I;
+  return (K / 256) * 2 * P + 256 < ((int64_t)1 << 31);
+}
 // one unit of prefill GEMM work: a token tile of one expert x a weight tile
 struct PItem {
   int expert;  // expert index (routed, then shared)
@@ -168,10 +176,14 @@ struct PrefillArgs {
   float* hd;
   int16_t* hbs;
   float* y;                      // slot-indexed [P, H]
+  void* xg;                      // fp16 [P, max(H, I)] activation codes in bucket order
+  void* sg;                      // fp16 [max(H, I)/256][2][P][8] code sums
+  float* dg;                     // fp32 [max(H, I)/256][P] block scales
   PItem* items;
   int32_t* n_items;
   int max_items;
   int* status;
+  unsigned long long* stats;     // [16] wait statistics of the GEMMs' CTA 0 (the phase_ns region)
 };
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s);
 

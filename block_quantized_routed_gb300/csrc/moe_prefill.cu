@@ -1,34 +1,58 @@
 // Prefill expert FFNs on the 5th-generation tensor cores (tcgen05).
 //
-// For a prefill chunk every expert sees on average tens to hundreds of
-// tokens, so gate/up and down are real dense contractions.  The weights stay
-// block-quantized in HBM; each CTA expands one super-block column of a
-// 128-row weight tile into shared memory as fp16 values sc_j * q (integers
-// <= 945, exact in fp16) and the tokens' q8_K codes as fp16 (exact), and
-// issues tcgen05.mma kind::f16 with fp32 accumulation in TMEM.  Every
-// partial sum inside one 256-wide super-block is an integer below 2^24, so
-// the accumulator holds the exact integer S = sum_j sc_j * isum_j.  The min
-// term M = sum_j mn_j * bsum_j is one more K=16 MMA per super-block (Q4_K:
-// bsum = 64*hi + lo split into two exact halves against mn and 64*mn; Q2_K:
-// |bsum| <= 2032 is exact as is).  The epilogue warps (TMEM lane = weight
-// row) read S and M and accumulate d_a * (d_w * S - dmin * M) in fp32.
+// In a prefill chunk each expert receives tens to hundreds of tokens, so its
+// gate/up and down products are dense contractions.  The weights stay
+// block-quantized in HBM and are expanded on chip; the arithmetic is exact
+// integer arithmetic carried by fp16 operands:
 //
-//   D[weight row m, token n] = sum_b d_a[n,b] * (d_w[m,b] * S[m,n,b] - dmin[m,b] * M[m,n,b])
+//   A (weights)     sc_j * q  for each weight of sub-block j   (<= 945: exact in fp16)
+//   B (activations) the q8_K codes of the tokens               (|q| <= 127: exact)
+//   S[m, n, b] = sum over the 256 columns of super-block b of A * B
 //
-// gate/up: a 128-row tile is 64 gate rows + the same 64 up rows, so one CTA
-// holds G and U of the same (row, token) and applies SwiGLU; h goes to
-// global memory in bucket order.  down: a tile is 128 rows of H; y goes to
-// the slot buffer.  h is re-quantized to q8_K between the two (the q8_K
-// quantizer kernel, one row per bucket position).
+// tcgen05.mma kind::f16 accumulates in fp32 in tensor memory (TMEM); the
+// integer partial sums stay below 2^24 (Q4_K: |S| <= 63*15*127*256 fits
+// except in contrived all-extreme blocks, where fp32 rounding is the only
+// deviation; Q2_K always fits), so S is the integer sub-block sum.  The
+// min term M[m, n, b] = sum_j mn_j * bsum_j(n) is one extra K=16 MMA per
+// super-block on the tokens' code sums (Q4_K: bsum = 64*hi + lo against
+// mn and 64*mn, both halves exact; Q2_K: |bsum16| <= 2032 as is).  The
+// epilogue rescales per super-block in fp32 registers:
 //
-// The pages' design does this with int8 MMA (mma.m16n8k32, "mmq-style
-// grouped MoE that unpacks each expert super-block to shared memory once per
-// prefill chunk and rescales per quant block in registers": Pulsar README,
-// "What it does today"; Strata, 长提示 0.1.13: MMQ int8 tensor-core expert
-// GEMM).  tcgen05 has no int8 kind on sm_103a, hence the exact-integer fp16
-// operands.
+//   D[m, n] = sum_b d_a[n, b] * (d_w[m, b] * S[m, n, b] - dmin[m, b] * M[m, n, b])
+//
+// This is the same contraction the GEMV kernels compute with dp4a; the
+// pages' prefill design reaches it with int8 MMA (Pulsar README, "What it
+// does today"; Strata, 0.1.13 prefill notes: grouped int8 tensor-core expert
+// GEMM that unpacks super-blocks to shared memory and rescales per block).
+// tcgen05 offers no int8 kind on sm_103a, hence exact-integer fp16.
+//
+// Kernel organisation (one persistent CTA per SM, 448 threads, warp roles):
+//   warp 12      producer: cp.async.bulk of the raw weight slabs and TMA
+//                tiles of the activation codes / code sums into rings
+//   warps 8-11   expanders: raw slab -> fp16 sc*q tile (one weight row per
+//                thread), mins tile for the min MMA
+//   warp 13      MMA issuer (one thread): 8 MMAs per half super-block into a
+//                double-buffered TMEM accumulator, the min MMA with the last
+//                half; commits are grouped (a commit costs the issuing
+//                thread several hundred cycles, so each group carries 8+ MMAs)
+//   warps 0-7    epilogue: TMEM -> registers, per-block rescale, output
+// Rings: 3 activation stages and 2 expanded-weight stages of 128 K each
+// (two 128-byte swizzle atoms), 2 raw stages of one super-block column.
+// A work item is (expert, token tile of <= 128 bucket rows, weight tile of
+// 128 rows); the items of a launch are laid out by a plan kernel.
+//   gate/up: the 128 rows interleave 64 gate rows and the same 64 up rows
+//            (even tile row: gate, odd: up), so a lane pair of the epilogue
+//            holds G and U of one (row, token): SwiGLU is a shuffle, and h is
+//            written in bucket order.
+//   down:    128 rows of H; y goes to the (token, slot) rows of the slot buffer.
+// Activations are first gathered into bucket order as fp16 codes (and the
+// code sums and block scales into TMA-friendly planes) by a small kernel, so
+// a token tile is a plain 2-D box for TMA.
 #include <algorithm>
 #include <cmath>
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <mutex>
 
 #include "moe_device.cuh"
 #include "moe_internal.h"
@@ -36,33 +60,70 @@
 namespace moe {
 namespace {
 
-constexpr int kPThreads = 256;
-constexpr int kTileM = 128;      // weight rows per tile (MMA M)
-constexpr int kTileN = 128;      // tokens per tile (MMA N, rounded to 16)
-constexpr long long kWaitCycles = 2000000000ll;  // ~1 s at 2 GHz: a wait that long has failed
+constexpr int kTileM = 128;                          // weight rows per tile (MMA M)
+constexpr int kTileN = 128;                          // tokens per tile (MMA N <= 128)
+constexpr int kStageK = 128;                         // K of one A or B stage: half a super-block
+constexpr int kAtomK = 64;                           // K of one 128-byte swizzle atom (fp16)
+constexpr int kStagesA = 2;                          // expanded-weight stages
+constexpr int kStagesB = 3;                          // activation stages
+constexpr int kRaw = 2;                              // raw stages (one super-block column each)
+constexpr int kBoxRows = 32;                         // token rows per TMA box
+constexpr int kEpiWarps = 8, kExpWarps = 4;         // expanders: one thread per tile row
+constexpr int kWarpProducer = kEpiWarps + kExpWarps; // 12
+constexpr int kWarpMma = kWarpProducer + 1;          // 13
+constexpr int kPThreads = 32 * (kWarpMma + 1);       // 448
+constexpr long long kWaitCycles = 2000000000ll;      // ~1 s at 2 GHz: a wait that long has failed
+
+// shared memory (offsets from a 1024-byte aligned base).  A stage holds two
+// swizzle atoms of 128 rows x 64 fp16 (16 KB each), K-major, 128-byte swizzle.
+constexpr int kAtomBytes = 128 * 128;
+constexpr int kBStage = 2 * kAtomBytes;              // 32 KB: 128 token rows x 128 codes
+constexpr int kAStage = 2 * kAtomBytes;              // 32 KB: 128 weight rows x 128 (sc * q)
+constexpr int kRawBytes = 4 * 4608;                  // four slabs (Q4_K size; Q2_K uses less)
+constexpr int kSmB = 0;
+constexpr int kSmA = kSmB + kStagesB * kBStage;
+constexpr int kSmRaw = kSmA + kStagesA * kAStage;
+constexpr int kSmA2 = kSmRaw + kRaw * kRawBytes;     // mins tile [128 rows][16] per raw stage
+constexpr int kSmB2 = kSmA2 + kRaw * 4096;           // code-sum tile [128 tokens][16] per raw stage
+constexpr int kSmDa = kSmB2 + kRaw * 4096;           // per epilogue warp: the block scales of its 64 tokens
+constexpr int kSmBar = kSmDa + kEpiWarps * 64 * 4;
+constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 * kRaw + 4;
+constexpr int kSmMisc = kSmBar + 8 * 32;
+constexpr int kSmUsed = kSmMisc + 16;
+constexpr int kSmAlloc = kSmUsed + 1024;             // slack for aligning the base
+static_assert(kNumBars <= 32, "barrier area");
+static_assert(kSmAlloc <= 232448, "shared memory per CTA");
 
 // ---------------------------------------------------------------- PTX helpers
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
 
-// Shared-memory matrix descriptor of a K-major operand without swizzle:
-// core matrices of 8 rows x 16 bytes; lbo = byte distance of core matrices
-// adjacent along K, sbo = along M/N.
-__device__ __forceinline__ uint64_t smem_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
-  uint64_t d = 0;
-  d |= (uint64_t)((addr & 0x3FFFF) >> 4);
+// Shared-memory matrix descriptor, K-major, no swizzle: core matrices of 8
+// rows x 16 bytes; lbo = byte distance of core matrices adjacent along K,
+// sbo = along M/N.
+__device__ __forceinline__ uint64_t desc_plain(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
   d |= (uint64_t)((lbo & 0x3FFFF) >> 4) << 16;
   d |= (uint64_t)((sbo & 0x3FFFF) >> 4) << 32;
-  d |= (uint64_t)1 << 46;  // fixed 0b001 in bits 46..48
-  return d;                // base offset 0, no swizzle
+  d |= (uint64_t)1 << 46;  // fixed 0b001
+  return d;
+}
+// K-major, 128-byte swizzle (the layout TMA writes with CU_TENSOR_MAP_SWIZZLE_128B):
+// 8-row groups 1024 bytes apart; the start may advance by 32-byte K steps inside the atom.
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(1024 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
 }
 
-// Instruction descriptor: kind::f16, A and B fp16, D fp32, K-major A and B.
+// Instruction descriptor: kind::f16, A and B fp16, D fp32, both K-major.
 __device__ __forceinline__ uint32_t idesc_f16(int M, int N) {
   uint32_t d = 0;
-  d |= 1u << 4;                       // D format: f32
-  // A format bits 7..9 = 0 (f16), B format bits 10..12 = 0 (f16)
+  d |= 1u << 4;                 // D format f32 (A/B format fields 0 = f16)
   d |= (uint32_t)(N >> 3) << 17;
   d |= (uint32_t)(M >> 4) << 24;
   return d;
@@ -74,34 +135,101 @@ __device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t adesc, uint64_
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"((int)acc));
 }
-
-__device__ __forceinline__ void mma_commit(uint32_t mbar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(mbar) : "memory");
+// The four K=16 MMAs of one 64-wide stage: descriptors advance by 32 bytes
+// (2 in the start-address field) per step; `acc` = accumulate the first one.
+__device__ __forceinline__ void mma_stage4(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %11, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %5, %9, p;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %2, %6, %9, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %3, %7, %9, 1;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %4, %8, %9, 1;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(adesc + 2), "l"(adesc + 4), "l"(adesc + 6), "l"(bdesc), "l"(bdesc + 2), "l"(bdesc + 4),
+      "l"(bdesc + 6), "r"(idesc), "r"(0), "r"((int)acc));
+}
+__device__ __forceinline__ void mma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar) : "memory");
 }
 
-__device__ __forceinline__ void mbar_init(uint32_t mbar, int count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(mbar), "r"(count) : "memory");
+__device__ __forceinline__ void mbar_init(uint32_t bar, int count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
-// Bounded wait for phase `parity` of an mbarrier: false once about a second
-// of SM clock has passed without the phase completing.
-__device__ __forceinline__ bool mbar_wait(uint32_t mbar, uint32_t parity) {
-  const long long t0 = clock64();
-  while (true) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(mbar), "r"(parity)
-        : "memory");
-    if (ok) return true;
-    if (clock64() - t0 > kWaitCycles) return false;
+// Bounded wait for phase `parity`.  Gives up when another role has aborted,
+// or after about a second, recording a timeout; false = abort.
+// `spent` accumulates the cycles waited (per-role wait statistics).
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                         long long& spent) {
+  const long long t0 = clock64();  // before the first try: try_wait itself may suspend the thread
+  while (!mbar_try(bar, parity)) {
+    if (*abort_flag) return false;
+    if (clock64() - t0 > kWaitCycles) {
+      *abort_flag = 1;
+      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
   }
+  spent += clock64() - t0;
+  return true;
+}
+
+// The same, taken by lane 0 for its whole (converged) warp: every lane gets
+// the same answer, so the warp stays converged for .sync.aligned operations.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
+                                          long long& spent) {
+  bool ok = true;
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status, spent);
+  ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+  __syncwarp();  // orders the other lanes after lane 0's acquire
+  return ok;
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::
+          "r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
+
+// packed fp32 pairs (one rounding per lane, as the scalar operations)
+__device__ __forceinline__ unsigned long long f2_pack(float x, float y) {
+  return (unsigned long long)__float_as_uint(x) | ((unsigned long long)__float_as_uint(y) << 32);
+}
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
 
 // 32 lanes x 16 consecutive fp32 columns of TMEM into 16 registers of each lane
 __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
@@ -117,10 +245,17 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// byte offset of element (row, k) in a K-major canonical tile with kc core
-// matrices along K (16-bit elements): core (row/8, k/8), 8 rows x 16 bytes each
+// byte offset of element (row, k) in a K-major canonical tile without
+// swizzle, kc core matrices along K (16-bit elements)
 __device__ __forceinline__ uint32_t canon_off(int row, int k, int kc) {
   return (uint32_t)(((row >> 3) * kc + (k >> 3)) * 128 + (row & 7) * 16 + (k & 7) * 2);
+}
+
+// byte offset of element (row, k), k < 128, in a stage of two 128-byte
+// swizzled K-major atoms (k / 64 selects the atom): row r at 128*r, its
+// 16-byte chunk c stored at chunk c ^ (r % 8)
+__device__ __forceinline__ uint32_t sw128_off(int row, int k) {
+  return (uint32_t)((k >> 6) * kAtomBytes + row * 128 + (((((k & 63) >> 3) ^ (row & 7)) & 7) << 4) + (k & 7) * 2);
 }
 
 __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
@@ -128,9 +263,28 @@ __device__ __forceinline__ uint32_t pack_h2(float a, float b) {
   return *reinterpret_cast<const uint32_t*>(&h);
 }
 
-// ---------------------------------------------------------------- work items
-// One CTA: per expert with tokens and a present gate pointer, its token tiles x
-// weight tiles, expert by expert.
+// Two small unsigned codes (bytes `sel` = 0x4140: bytes 0,1; 0x4342: bytes
+// 2,3 of w) times the sub-block scale, as an exact fp16 pair:
+// 0x64XX is the fp16 number 1024 + XX, and one fused multiply-add
+// (1024 + q) * sc - 1024 * sc rounds only the exact result q * sc.
+__device__ __forceinline__ uint32_t scaled_pair(uint32_t w, uint32_t sel, __half2 sc2, __half2 off2) {
+  const uint32_t v = __byte_perm(w, 0x64u, sel);
+  const __half2 h = __hfma2(*reinterpret_cast<const __half2*>(&v), sc2, off2);
+  return *reinterpret_cast<const uint32_t*>(&h);
+}
+// eight codes (bytes of w0, then w1) -> 16 bytes of fp16 sc*q
+__device__ __forceinline__ uint4 scaled8(uint32_t w0, uint32_t w1, __half2 sc2, __half2 off2) {
+  uint4 o;
+  o.x = scaled_pair(w0, 0x4140u, sc2, off2);
+  o.y = scaled_pair(w0, 0x4342u, sc2, off2);
+  o.z = scaled_pair(w1, 0x4140u, sc2, off2);
+  o.w = scaled_pair(w1, 0x4342u, sc2, off2);
+  return o;
+}
+
+// ---------------------------------------------------------------- planning
+// One CTA: per expert with tokens and a present gate pointer, its token tiles
+// (ceil(c/128) tiles of balanced size) x weight tiles, expert by expert.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* counts, const int32_t* offsets, int EpS,
                                                             const moe_expert_ptrs* table, int n_wtiles, PItem* items,
                                                             int32_t* n_items, int max_items) {
@@ -144,14 +298,16 @@ __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* count
   for (int e = threadIdx.x; e < EpS; e += blockDim.x) {
     const int c = counts[e];
     if (c <= 0 || table[e].gate == nullptr) continue;
+    const int nt = (c + kTileN - 1) / kTileN;
+    const int per = (c + nt - 1) / nt;
     int idx = s_n[e];
-    for (int t0 = 0; t0 < c; t0 += kTileN)
+    for (int t0 = 0; t0 < c; t0 += per)
       for (int w = 0; w < n_wtiles; ++w, ++idx) {
         if (idx >= max_items) continue;
         PItem it;
         it.expert = e;
         it.start = offsets[e] + t0;
-        it.count = min(kTileN, c - t0);
+        it.count = min(per, c - t0);
         it.wtile = w;
         items[idx] = it;
       }
@@ -171,356 +327,562 @@ __global__ void zero_absent_slots_kernel(const int32_t* counts, const int32_t* o
   }
 }
 
+// Bucket-order planes of the activations for the GEMM (one warp per row p):
+//   xg [P][K]          fp16 codes
+//   sg [nb][2][P][8]   fp16 code sums of super-block b, two 8-wide halves:
+//                      Q4_K: the 32-code sums split as lo (0..63) and hi
+//                      (bsum = 64*hi + lo); Q2_K: the 16-code sums 0-7, 8-15
+//   dg [nb][P]         fp32 block scales
+// Row p comes from token row perm ? token_of_slot(perm[p]) : p.
+template <int FMT>
+__global__ void __launch_bounds__(256) prefill_gather_kernel(const int8_t* __restrict__ q,
+                                                             const int16_t* __restrict__ bs,
+                                                             const float* __restrict__ d,
+                                                             const int32_t* __restrict__ perm, int T, int k,
+                                                             int64_t P, int K, __half* __restrict__ xg,
+                                                             __half* __restrict__ sg, float* __restrict__ dg) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int nb = K / 256;
+  for (int64_t p = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < P; p += nw) {
+    const int64_t t = perm ? token_of_slot(perm[p], T, k) : p;
+    const int4* src = reinterpret_cast<const int4*>(q + t * K);
+    uint4* dst = reinterpret_cast<uint4*>(xg + p * K);
+    for (int c = lane; c < K / 16; c += 32) {
+      const int4 v = __ldg(src + c);
+      const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+      for (int hh = 0; hh < 2; ++hh) {
+        const uint32_t a = w[2 * hh], b = w[2 * hh + 1];
+        uint4 o;
+        o.x = pack_h2((float)(int8_t)(a & 0xFF), (float)(int8_t)((a >> 8) & 0xFF));
+        o.y = pack_h2((float)(int8_t)((a >> 16) & 0xFF), (float)(int8_t)(a >> 24));
+        o.z = pack_h2((float)(int8_t)(b & 0xFF), (float)(int8_t)((b >> 8) & 0xFF));
+        o.w = pack_h2((float)(int8_t)((b >> 16) & 0xFF), (float)(int8_t)(b >> 24));
+        dst[2 * c + hh] = o;
+      }
+    }
+    for (int e = lane; e < 2 * nb; e += 32) {
+      const int b = e >> 1, hh = e & 1;
+      const int16_t* s = bs + t * (K / 16) + 16 * b;
+      float v[8];
+      if constexpr (FMT == kQ4K) {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int sum = (int)s[2 * j] + (int)s[2 * j + 1];
+          const int hi = sum >> 6;  // floor
+          v[j] = (float)(hh ? hi : sum - 64 * hi);
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = (float)s[8 * hh + j];
+      }
+      uint4 o;
+      o.x = pack_h2(v[0], v[1]);
+      o.y = pack_h2(v[2], v[3]);
+      o.z = pack_h2(v[4], v[5]);
+      o.w = pack_h2(v[6], v[7]);
+      *reinterpret_cast<uint4*>(sg + ((int64_t)(2 * b + hh) * P + p) * 8) = o;
+    }
+    for (int b = lane; b < nb; b += 32) dg[(int64_t)b * P + p] = d[t * nb + b];
+  }
+}
+
 // ---------------------------------------------------------------- the GEMM
-// Shared memory: A weights [128][256] fp16 canonical (64 KB), B tokens
-// [128][256] fp16 canonical (64 KB), A2 mins [128][16] (4 KB), B2 code sums
-// [128][16] (4 KB), per-row d/dmin, per-token d_a and row index, the
-// mbarrier and the TMEM address.
-constexpr int kSmA = 0;
-constexpr int kSmB = kSmA + kTileM * 256 * 2;
-constexpr int kSmA2 = kSmB + kTileN * 256 * 2;
-constexpr int kSmB2 = kSmA2 + kTileM * 16 * 2;
-constexpr int kSmDw = kSmB2 + kTileN * 16 * 2;
-constexpr int kSmDmin = kSmDw + kTileM * 4;
-constexpr int kSmDa = kSmDmin + kTileM * 4;
-constexpr int kSmRow = kSmDa + kTileN * 4;
-constexpr int kSmBar = kSmRow + kTileN * 4;
-constexpr int kSmTmem = kSmBar + 16;
-constexpr int kSmTotal = kSmTmem + 16;
+struct GemmArgs {
+  CUtensorMap map_x;    // xg [P][K] fp16, box {64, 32}, 128-byte swizzle
+  CUtensorMap map_s;    // sg rows of 8 fp16, box {8, 128}
+  int fmt, H, I, T, k;
+  int64_t P;
+  const moe_expert_ptrs* table;
+  const int32_t* perm;
+  const float* dg;
+  const PItem* items;
+  const int32_t* n_items;
+  float* h;
+  float* y;
+  int* status;
+  unsigned long long* stats;  // [16] wait statistics of CTA 0 (nullable)
+};
 
 template <int FMT, int MODE>  // MODE 0: gate/up + SwiGLU -> h; MODE 1: down -> y
-__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ PrefillArgs a) {
+__global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ GemmArgs a) {
   using F = Fmt<FMT>;
-  extern __shared__ __align__(1024) uint8_t sm[];
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int K = MODE == 0 ? a.H : a.I;          // reduction length
+  const int K = MODE == 0 ? a.H : a.I;
   const int nb = K / 256;
-  const int N_out = MODE == 0 ? a.I : a.H;      // rows of the weight matrices
-  const uint32_t bar = smem_u32(sm + kSmBar);
-  float* s_dw = reinterpret_cast<float*>(sm + kSmDw);
-  float* s_dmin = reinterpret_cast<float*>(sm + kSmDmin);
-  float* s_da = reinterpret_cast<float*>(sm + kSmDa);
-  int* s_row = reinterpret_cast<int*>(sm + kSmRow);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kSmTmem);
+  const int N_out = MODE == 0 ? a.I : a.H;
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + kSmBar;
+  // barrier slots: full_a, empty_a, full_b, empty_b, full_raw, empty_raw, tfull, tempty
+  auto full_a = [&](int s) { return bar0 + 8 * s; };
+  auto empty_a = [&](int s) { return bar0 + 8 * (kStagesA + s); };
+  auto full_b = [&](int s) { return bar0 + 8 * (2 * kStagesA + s); };
+  auto empty_b = [&](int s) { return bar0 + 8 * (2 * kStagesA + kStagesB + s); };
+  auto full_raw = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + s); };
+  auto empty_raw = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + kRaw + s); };
+  auto tfull = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + 2 * kRaw + s); };
+  auto tempty = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + 2 * kRaw + 2 + s); };
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kSmMisc);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmMisc + 4);
 
   if (warp == 0) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(s_tmem)));
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
-  if (tid == 0) {
-    mbar_init(bar, 1);
+  if (tid == 32) {
+    for (int s = 0; s < kStagesA; ++s) {
+      mbar_init(full_a(s), kExpWarps);
+      mbar_init(empty_a(s), 1);
+    }
+    for (int s = 0; s < kStagesB; ++s) {
+      mbar_init(full_b(s), 1);
+      mbar_init(empty_b(s), 1);
+    }
+    for (int s = 0; s < kRaw; ++s) {
+      mbar_init(full_raw(s), 1);
+      mbar_init(empty_raw(s), kExpWarps + 1);
+    }
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(tfull(s), 1);
+      mbar_init(tempty(s), kEpiWarps);
+    }
+    *abort_flag = 0;
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *s_tmem;
-  uint32_t phase = 0;
-  bool failed = false;
-
   const int n_items = *a.n_items;
-  for (int item = blockIdx.x; item < n_items && !failed; item += gridDim.x) {
-    const PItem it = a.items[item];
-    const moe_expert_ptrs ep = a.table[it.expert];
-    const int ntok = it.count;
-    const int N = (ntok + 15) / 16 * 16;  // MMA N
-    // token rows of the tile: gate/up gathers x by the bucket permutation, down reads h in bucket order
-    for (int n = tid; n < kTileN; n += kPThreads) {
-      int row = -1;
-      if (n < ntok) row = MODE == 0 ? token_of_slot(a.perm[it.start + n], a.T, a.k) : it.start + n;
-      s_row[n] = row;
-    }
-    float acc[kTileN];
-#pragma unroll
-    for (int j = 0; j < kTileN; ++j) acc[j] = 0.0f;
-    __syncthreads();
+  const int slab_bytes = F::kSlabBytes;
+  const long long t_start = clock64();
+  long long w0 = 0, w1 = 0;  // cycles this thread waited on its role's two kinds of barrier
 
-    for (int b = 0; b < nb; ++b) {
-      // ---- A: 128 weight rows of super-block b, as fp16 sc*q, and the mins
-      {
-        const int r = tid >> 1, half = tid & 1;  // row r, K half [128*half, +128)
-        const uint8_t* base;
-        int wrow;
-        if (MODE == 0) {
-          const int g = r & 63;
-          wrow = it.wtile * 64 + g;
-          base = static_cast<const uint8_t*>(r < 64 ? ep.gate : ep.up);
-        } else {
-          wrow = it.wtile * 128 + r;
-          base = static_cast<const uint8_t*>(ep.down);
+  if (warp == kWarpProducer) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      uint32_t ri = 0;
+      int bs = 0;
+      uint32_t pb = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const PItem it = a.items[item];
+        const moe_expert_ptrs ep = a.table[it.expert];
+        const int nbox = (it.count + kBoxRows - 1) / kBoxRows;
+        // the four row groups of the tile: gate/up -> gate 2w, 2w+1, up 2w, 2w+1; down -> 4w .. 4w+3
+        const uint8_t* src[4];
+#pragma unroll
+        for (int g = 0; g < 4; ++g) {
+          if (MODE == 0) {
+            const uint8_t* m = static_cast<const uint8_t*>(g < 2 ? ep.gate : ep.up);
+            src[g] = m + (size_t)(it.wtile * 2 + (g & 1)) * nb * slab_bytes;
+          } else {
+            src[g] = static_cast<const uint8_t*>(ep.down) + (size_t)(it.wtile * 4 + g) * nb * slab_bytes;
+          }
         }
-        const uint8_t* slab = base + ((size_t)(wrow >> 5) * nb + b) * F::kSlabBytes;
-        const int lr = wrow & 31;
-        SbRegs<FMT> s;
-        load_sb<FMT>(slab, lr, s);
-        if (half == 0) {
-          s_dw[r] = half_lo(s.dm);
-          s_dmin[r] = half_hi(s.dm);
-        }
-        uint8_t* A = sm + kSmA;
-        if constexpr (FMT == kQ4K) {
-          // sub-blocks 4*half .. 4*half+3 (32 codes each)
+        for (int b = 0; b < nb && ok; ++b) {
+          const int rs = ri % kRaw;
+          if (!(ok = wait_bar(empty_raw(rs), ((ri / kRaw) & 1) ^ 1, abort_flag, a.status, w0))) break;
+          mbar_expect_tx(full_raw(rs), 4 * slab_bytes + 4096);
+          const uint32_t raw = sbase + kSmRaw + rs * kRawBytes;
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const int j = 4 * half + jj;
-            int sc, mn;
-            sb_scale_min<FMT>(s, j, sc, mn);
-            uint32_t lo[4], hi[4];
-            mask_q4k(s.code[j], lo, hi);
-            const float fs = (float)sc;
-            // codes 0..15 of the sub-block are the low nibbles, 16..31 the high ones
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-#pragma unroll
-              for (int hh = 0; hh < 2; ++hh) {
-                const uint32_t v = hh ? hi[w] : lo[w];
-                const int k0 = 32 * j + 16 * hh + 4 * w;  // 4 codes k0..k0+3
-                uint2 pk;
-                pk.x = pack_h2(fs * (float)(v & 0xFF), fs * (float)((v >> 8) & 0xFF));
-                pk.y = pack_h2(fs * (float)((v >> 16) & 0xFF), fs * (float)(v >> 24));
-                *reinterpret_cast<uint2*>(A + canon_off(r, k0, 32)) = pk;
-              }
-            }
+          for (int g = 0; g < 4; ++g)
+            bulk_load(raw + g * slab_bytes, src[g] + (size_t)b * slab_bytes, slab_bytes, full_raw(rs));
+          const uint32_t b2 = sbase + kSmB2 + rs * 4096;
+          tma_load_2d(b2, &a.map_s, 0, (int)((2 * b) * a.P + it.start), full_raw(rs));
+          tma_load_2d(b2 + 2048, &a.map_s, 0, (int)((2 * b + 1) * a.P + it.start), full_raw(rs));
+          ++ri;
+          for (int c = 0; c < 256 / kStageK && ok; ++c) {
+            if (!(ok = wait_bar(empty_b(bs), pb ^ 1, abort_flag, a.status, w1))) break;
+            mbar_expect_tx(full_b(bs), 2 * nbox * kBoxRows * 128);
+            const uint32_t bdst = sbase + kSmB + bs * kBStage;
+            for (int at = 0; at < 2; ++at)
+              for (int i = 0; i < nbox; ++i)
+                tma_load_2d(bdst + at * kAtomBytes + i * kBoxRows * 128, &a.map_x, 256 * b + kStageK * c + kAtomK * at,
+                            it.start + kBoxRows * i, full_b(bs));
+            if (++bs == kStagesB) { bs = 0; pb ^= 1; }
           }
-          if (half == 0) {
-            // A2 row r: [mn_0..7, 64*mn_0..7]
-            int mnv[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              int sc;
-              sb_scale_min<FMT>(s, j, sc, mnv[j]);
-            }
-            uint4 c0, c1;
-            c0.x = pack_h2((float)mnv[0], (float)mnv[1]);
-            c0.y = pack_h2((float)mnv[2], (float)mnv[3]);
-            c0.z = pack_h2((float)mnv[4], (float)mnv[5]);
-            c0.w = pack_h2((float)mnv[6], (float)mnv[7]);
-            c1.x = pack_h2(64.f * mnv[0], 64.f * mnv[1]);
-            c1.y = pack_h2(64.f * mnv[2], 64.f * mnv[3]);
-            c1.z = pack_h2(64.f * mnv[4], 64.f * mnv[5]);
-            c1.w = pack_h2(64.f * mnv[6], 64.f * mnv[7]);
-            *reinterpret_cast<uint4*>(sm + kSmA2 + canon_off(r, 0, 2)) = c0;
-            *reinterpret_cast<uint4*>(sm + kSmA2 + canon_off(r, 8, 2)) = c1;
-          }
-        } else {
-          // sub-blocks 8*half .. 8*half+7 (16 codes each)
-#pragma unroll
-          for (int jj = 0; jj < 8; ++jj) {
-            const int j = 8 * half + jj;
-            int sc, mn;
-            sb_scale_min<FMT>(s, j, sc, mn);
-            uint32_t w[4];
-            mask_q2k(s.code[j >> 2], j, w);
-            const float fs = (float)sc;
-#pragma unroll
-            for (int p = 0; p < 4; ++p) {
-              const int k0 = 16 * j + 4 * p;
-              uint2 pk;
-              pk.x = pack_h2(fs * (float)(w[p] & 0xFF), fs * (float)((w[p] >> 8) & 0xFF));
-              pk.y = pack_h2(fs * (float)((w[p] >> 16) & 0xFF), fs * (float)(w[p] >> 24));
-              *reinterpret_cast<uint2*>(A + canon_off(r, k0, 32)) = pk;
-            }
-          }
-          // A2 row r: mins of the 16 sub-blocks (|bsum| <= 2032 is exact in fp16)
-          uint4 c;
-          int m0, m1, sc;
-          uint32_t pk[4];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            sb_scale_min<FMT>(s, 8 * half + 2 * q, sc, m0);
-            sb_scale_min<FMT>(s, 8 * half + 2 * q + 1, sc, m1);
-            pk[q] = pack_h2((float)m0, (float)m1);
-          }
-          c.x = pk[0]; c.y = pk[1]; c.z = pk[2]; c.w = pk[3];
-          *reinterpret_cast<uint4*>(sm + kSmA2 + canon_off(r, 8 * half, 2)) = c;
         }
       }
-      // ---- B: the tile's token rows of block b as fp16 codes, and their code sums
-      {
-        const int n = tid >> 1, half = tid & 1;
-        uint8_t* B = sm + kSmB;
-        const int row = s_row[n];
-        const int8_t* q = MODE == 0 ? a.xq : a.hq;
-        const int16_t* bs = MODE == 0 ? a.xbs : a.hbs;
-        const float* dq = MODE == 0 ? a.xd : a.hd;
-        if (row >= 0) {
-          const int4* src = reinterpret_cast<const int4*>(q + (size_t)row * K + 256 * b + 128 * half);
+    }
+  } else if (warp >= kEpiWarps && warp < kWarpProducer) {
+    // ------------------------------------------------------------ expanders
+    // tile row r: gate/up interleaved (even r: gate row r/2 of the 64-row
+    // group, odd r: the same row of up), down: row r of the 128-row group.
+    // Two threads per row: `hx` picks the 64-wide atom of each stage.
+    const int r = tid - 32 * kEpiWarps;
+    const int g = MODE == 0 ? ((r & 1) * 2 + (r >> 6)) : (r >> 5);  // slab of the raw stage
+    const int lr = MODE == 0 ? ((r >> 1) & 31) : (r & 31);         // row inside the slab
+    uint32_t ri = 0;
+    int as = 0;
+    uint32_t pa = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      for (int b = 0; b < nb && ok; ++b) {
+        const int rs = ri % kRaw;
+        if (!(ok = warp_wait(full_raw(rs), (ri / kRaw) & 1, abort_flag, a.status, w0))) break;
+        const uint8_t* slab = sm + kSmRaw + rs * kRawBytes + g * slab_bytes;
+        uint8_t* a2 = sm + kSmA2 + rs * 4096;
+        // scales and mins, extracted on demand (no per-thread arrays)
+        uint64_t sm_lo, sm_hi;
+        if constexpr (FMT == kQ4K) {
+          // 96-bit string: scale j = bits 6j.., min j = bits 48 + 6j..
+          const uint32_t* smw = reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * lr);
+          sm_lo = (uint64_t)smw[0] | ((uint64_t)smw[1] << 32);
+          sm_hi = (uint64_t)(smw[1] >> 16) | ((uint64_t)smw[2] << 16);
+        } else {
+          // byte j = scale_j | min_j << 4
+          const uint4 v = *reinterpret_cast<const uint4*>(slab + F::kSmOff + 16 * lr);
+          sm_lo = (uint64_t)v.x | ((uint64_t)v.y << 32);
+          sm_hi = (uint64_t)v.z | ((uint64_t)v.w << 32);
+        }
+        auto scale_of = [&](int j) -> int {
+          if constexpr (FMT == kQ4K) return (int)((sm_lo >> (6 * j)) & 63);
+          else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7))) & 15);
+        };
+        auto min_of = [&](int j) -> int {
+          if constexpr (FMT == kQ4K) return (int)((sm_hi >> (6 * j)) & 63);
+          else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7) + 4)) & 15);
+        };
 #pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const int4 v = __ldcg(src + c);
-            const uint32_t w4[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+        for (int hx = 0; hx < 2; ++hx) {
+          // A2 row r, K 8*hx .. 8*hx+7: Q4_K [mn_0..7 | 64 * mn_0..7], Q2_K mn_0..15
+          float f[8];
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              uint4 pk;
-              const uint32_t wa = w4[2 * hh], wb = w4[2 * hh + 1];
-              pk.x = pack_h2((float)(int8_t)(wa & 0xFF), (float)(int8_t)((wa >> 8) & 0xFF));
-              pk.y = pack_h2((float)(int8_t)((wa >> 16) & 0xFF), (float)(int8_t)(wa >> 24));
-              pk.z = pack_h2((float)(int8_t)(wb & 0xFF), (float)(int8_t)((wb >> 8) & 0xFF));
-              pk.w = pack_h2((float)(int8_t)((wb >> 16) & 0xFF), (float)(int8_t)(wb >> 24));
-              *reinterpret_cast<uint4*>(B + canon_off(n, 128 * half + 16 * c + 8 * hh, 32)) = pk;
-            }
-          }
-          const int16_t* bsp = bs + (size_t)row * (K / 16) + 16 * b;
+          for (int i = 0; i < 8; ++i)
+            f[i] = FMT == kQ4K ? (hx ? 64.f : 1.f) * (float)min_of(i) : (float)min_of(8 * hx + i);
+          uint4 c0;
+          c0.x = pack_h2(f[0], f[1]);
+          c0.y = pack_h2(f[2], f[3]);
+          c0.z = pack_h2(f[4], f[5]);
+          c0.w = pack_h2(f[6], f[7]);
+          *reinterpret_cast<uint4*>(a2 + canon_off(r, 8 * hx, 2)) = c0;
+        }
+#pragma unroll
+        for (int c = 0; c < 256 / kStageK; ++c) {
+          if (!(ok = warp_wait(empty_a(as), pa ^ 1, abort_flag, a.status, w1))) break;
+          uint8_t* A = sm + kSmA + as * kAStage;
+#pragma unroll
+          for (int hx = 0; hx < 2; ++hx) {
           if constexpr (FMT == kQ4K) {
-            if (half == 0) {
-              // 32-code sums bsum_j = 64*hi + lo, lo in [0, 64)
-              float lo[8], hi[8];
 #pragma unroll
-              for (int j = 0; j < 8; ++j) {
-                const int v = (int)__ldcg(bsp + 2 * j) + (int)__ldcg(bsp + 2 * j + 1);
-                const int h = v >> 6;  // floor division
-                lo[j] = (float)(v - 64 * h);
-                hi[j] = (float)h;
-              }
-              uint4 c0, c1;
-              c0.x = pack_h2(lo[0], lo[1]); c0.y = pack_h2(lo[2], lo[3]);
-              c0.z = pack_h2(lo[4], lo[5]); c0.w = pack_h2(lo[6], lo[7]);
-              c1.x = pack_h2(hi[0], hi[1]); c1.y = pack_h2(hi[2], hi[3]);
-              c1.z = pack_h2(hi[4], hi[5]); c1.w = pack_h2(hi[6], hi[7]);
-              *reinterpret_cast<uint4*>(sm + kSmB2 + canon_off(n, 0, 2)) = c0;
-              *reinterpret_cast<uint4*>(sm + kSmB2 + canon_off(n, 8, 2)) = c1;
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 4 * c + 2 * hx + jj;  // sub-block of 32 codes
+              const uint4 cw = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * j + 16 * lr);
+              uint32_t lo4[4], hi4[4];
+              mask_q4k(cw, lo4, hi4);
+              const float scf = (float)scale_of(j);
+              const __half2 sc2 = __float2half2_rn(scf);
+              const __half2 off2 = __float2half2_rn(-1024.0f * scf);
+              const int k0 = 64 * hx + 32 * jj;  // K offset inside the stage
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0)) = scaled8(lo4[0], lo4[1], sc2, off2);
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 8)) = scaled8(lo4[2], lo4[3], sc2, off2);
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 16)) = scaled8(hi4[0], hi4[1], sc2, off2);
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 24)) = scaled8(hi4[2], hi4[3], sc2, off2);
             }
           } else {
-            uint4 c;
-            c.x = pack_h2((float)__ldcg(bsp + 8 * half + 0), (float)__ldcg(bsp + 8 * half + 1));
-            c.y = pack_h2((float)__ldcg(bsp + 8 * half + 2), (float)__ldcg(bsp + 8 * half + 3));
-            c.z = pack_h2((float)__ldcg(bsp + 8 * half + 4), (float)__ldcg(bsp + 8 * half + 5));
-            c.w = pack_h2((float)__ldcg(bsp + 8 * half + 6), (float)__ldcg(bsp + 8 * half + 7));
-            *reinterpret_cast<uint4*>(sm + kSmB2 + canon_off(n, 8 * half, 2)) = c;
-          }
-          if (half == 0) s_da[n] = __ldcg(dq + (size_t)row * nb + b);
-        } else {
-          // padding token: zero codes and sums
-          const uint4 z = make_uint4(0, 0, 0, 0);
+            const uint4 line = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * (2 * c + hx) + 16 * lr);
 #pragma unroll
-          for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(B + canon_off(n, 128 * half + 8 * c, 32)) = z;
-          *reinterpret_cast<uint4*>(sm + kSmB2 + canon_off(n, 8 * half, 2)) = z;
-          if (half == 0) s_da[n] = 0.0f;
+            for (int q = 0; q < 4; ++q) {
+              const int j = 8 * c + 4 * hx + q;  // sub-block of 16 codes
+              uint32_t w[4];
+              mask_q2k(line, q, w);
+              const float scf = (float)scale_of(j);
+              const __half2 sc2 = __float2half2_rn(scf);
+              const __half2 off2 = __float2half2_rn(-1024.0f * scf);
+              const int k0 = 64 * hx + 16 * q;
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0)) = scaled8(w[0], w[1], sc2, off2);
+              *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 8)) = scaled8(w[2], w[3], sc2, off2);
+            }
+          }
+          }
+          fence_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(full_a(as));
+          if (++as == kStagesA) { as = 0; pa ^= 1; }
+        }
+        if (!ok) break;
+        __syncwarp();
+        if (lane == 0) mbar_arrive(empty_raw(rs));
+        ++ri;
+      }
+    }
+  } else if (warp == kWarpMma) {
+    // ------------------------------------------------------------ MMA issuer
+    // Per block: stage 0 (8 MMAs, one commit group), stage 1 (8 MMAs + the
+    // min MMA, one commit group).  The first commit after a run of MMAs
+    // costs the issuing thread a few hundred cycles, so commits are grouped
+    // behind as much MMA work as possible.
+    if (lane == 0) {
+      const uint64_t dA0 = desc_sw128(sbase + kSmA), dB0 = desc_sw128(sbase + kSmB);
+      const uint64_t dA2 = desc_plain(sbase + kSmA2, 128, 256), dB2 = desc_plain(sbase + kSmB2, 2048, 128);
+      uint32_t ri = 0, tb = 0;
+      int as = 0, bs = 0;
+      uint32_t pa = 0, pb = 0;
+      bool ok = true;
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const PItem it = a.items[item];
+        const int N = (it.count + 15) / 16 * 16;
+        const uint32_t idesc = idesc_f16(kTileM, N);
+        for (int b = 0; b < nb && ok; ++b) {
+          const int ab = tb & 1;
+          if (!(ok = wait_bar(tempty(ab), ((tb >> 1) & 1) ^ 1, abort_flag, a.status, w0))) break;
+          tc_fence_after();
+          const uint32_t dS = tmem + ab * 256, dM = dS + 128;
+          const int rs = ri % kRaw;
+          for (int c = 0; c < 256 / kStageK && ok; ++c) {
+            if (!(ok = wait_bar(full_a(as), pa, abort_flag, a.status, w1))) break;
+            if (!(ok = wait_bar(full_b(bs), pb, abort_flag, a.status, w1))) break;
+            const bool last = c == 256 / kStageK - 1;
+            if (last && !(ok = wait_bar(full_raw(rs), (ri / kRaw) & 1, abort_flag, a.status, w1))) break;
+            tc_fence_after();
+            const uint64_t da = dA0 + (uint64_t)((as * kAStage) >> 4), db = dB0 + (uint64_t)((bs * kBStage) >> 4);
+            mma_stage4(dS, da, db, idesc, c > 0);
+            mma_stage4(dS, da + (kAtomBytes >> 4), db + (kAtomBytes >> 4), idesc, true);
+            if (last) mma_f16(dM, dA2 + (uint64_t)((rs * 4096) >> 4), dB2 + (uint64_t)((rs * 4096) >> 4), idesc, false);
+            mma_commit(empty_a(as));
+            mma_commit(empty_b(bs));
+            if (last) {
+              mma_commit(empty_raw(rs));
+              mma_commit(tfull(ab));
+            }
+            if (++as == kStagesA) { as = 0; pa ^= 1; }
+            if (++bs == kStagesB) { bs = 0; pb ^= 1; }
+          }
+          ++ri;
+          ++tb;
         }
       }
-      fence_async_smem();
-      tc_fence_before();
-      __syncthreads();
-      // ---- MMAs: S into TMEM columns [0, N), the min term into [128, 128+N)
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc = idesc_f16(kTileM, N);
-        const uint32_t a0 = smem_u32(sm + kSmA), b0 = smem_u32(sm + kSmB);
-        // K-major, 32 core matrices along K: lbo = 128 B, sbo = 32 * 128 B
-#pragma unroll 1
-        for (int s = 0; s < 16; ++s)
-          mma_f16(tmem, smem_desc(a0 + s * 256, 128, 4096), smem_desc(b0 + s * 256, 128, 4096), idesc, s > 0);
-        mma_f16(tmem + 128, smem_desc(smem_u32(sm + kSmA2), 128, 256), smem_desc(smem_u32(sm + kSmB2), 128, 256),
-                idesc, false);
-        mma_commit(bar);
+    }
+  } else {
+    // ------------------------------------------------------------ epilogue (warps 0-7)
+    // Warp (qd, cg) owns TMEM lanes 32*qd.. (tile rows) and the 16-token
+    // chunks cg, cg+2, cg+4, cg+6 (local token index 16*kl + j is token
+    // 16*(2*kl + cg) + j), so both column groups share short tiles evenly.
+    const int qd = warp & 3, cg = warp >> 2;
+    const int m = 32 * qd + lane;             // tile row
+    float* s_da = reinterpret_cast<float*>(sm + kSmDa) + 64 * warp;
+    uint32_t tb = 0;
+    bool ok = true;
+    for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+      const PItem it = a.items[item];
+      const moe_expert_ptrs ep = a.table[it.expert];
+      const int ntok = it.count;
+      const int N = (ntok + 15) / 16 * 16;
+      const uint8_t* hdr;  // d/dmin word of this row's super-block 0
+      if (MODE == 0) {
+        const int i = it.wtile * 64 + (m >> 1);
+        hdr = static_cast<const uint8_t*>((m & 1) ? ep.up : ep.gate) + (size_t)(i >> 5) * nb * slab_bytes + 4 * (i & 31);
+      } else {
+        const int i = it.wtile * 128 + m;
+        hdr = static_cast<const uint8_t*>(ep.down) + (size_t)(i >> 5) * nb * slab_bytes + 4 * (i & 31);
       }
-      const bool done = mbar_wait(bar, phase);
-      phase ^= 1;
-      if (__syncthreads_or(!done)) {  // uniform: every thread leaves together
-        if (tid == 0) set_status(a.status, MOE_ERR_DEVICE_TIMEOUT);
-        mbar_wait(bar, phase ^ 1);    // one more bounded wait for the MMAs in flight before TMEM is freed
-        failed = true;
-        break;
-      }
-      tc_fence_after();
-      // ---- epilogue: lane m of warps 0..3 = weight row m
-      if (warp < 4) {
-        const int m = 32 * warp + lane;
-        const float dw = s_dw[m], dmin = s_dmin[m];
-        const uint32_t tbase = tmem + ((uint32_t)(32 * warp) << 16);
+      unsigned long long acc[32];  // pairs of local tokens (2i, 2i+1)
 #pragma unroll
-        for (int c = 0; c < kTileN / 16; ++c) {
-          if (16 * c < N) {  // N is a multiple of 16 and warp-uniform
+      for (int j = 0; j < 32; ++j) acc[j] = 0ull;
+      // tokens of this lane's two prefetched scales: local l and 32 + l
+      const int tk0 = 16 * (2 * (lane >> 4) + cg) + (lane & 15), tk1 = tk0 + 64;
+      const float* dgp = a.dg + it.start;
+      const bool v0 = tk0 < ntok, v1 = tk1 < ntok;
+      // down: the slot rows of the same tokens, for the output
+      int slot0 = 0, slot1 = 0;
+      if (MODE == 1) {
+        slot0 = v0 ? __ldg(a.perm + it.start + tk0) : 0;
+        slot1 = v1 ? __ldg(a.perm + it.start + tk1) : 0;
+      }
+      // the scales of block b + 1 are loaded while block b is processed
+      uint32_t dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr));
+      float da0_n = v0 ? __ldg(dgp + tk0) : 0.0f, da1_n = v1 ? __ldg(dgp + tk1) : 0.0f;
+      for (int b = 0; b < nb; ++b) {
+        const int ab = tb & 1;
+        const uint32_t dm = dm_n;
+        const float da0 = da0_n, da1 = da1_n;
+        if (b + 1 < nb) {
+          dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr + (size_t)(b + 1) * slab_bytes));
+          const float* dgb = dgp + (int64_t)(b + 1) * a.P;
+          da0_n = v0 ? __ldg(dgb + tk0) : 0.0f;
+          da1_n = v1 ? __ldg(dgb + tk1) : 0.0f;
+        }
+        if (!(ok = warp_wait(tfull(ab), (tb >> 1) & 1, abort_flag, a.status, w0))) break;
+        tc_fence_after();
+        s_da[lane] = da0;
+        s_da[32 + lane] = da1;
+        __syncwarp();
+        const float dw = half_lo(dm), dmin = half_hi(dm);
+        const unsigned long long dw2 = f2_pack(dw, dw), ndm2 = f2_pack(-dmin, -dmin);
+        const uint32_t tS = tmem + ((uint32_t)(32 * qd) << 16) + ab * 256;
+#pragma unroll
+        for (int kl = 0; kl < 4; ++kl) {
+          const int c = 2 * kl + cg;  // chunk of 16 tokens
+          if (16 * c < N) {
             float Sv[16], Mv[16];
-            tmem_ld16(tbase + 16 * c, Sv);
-            tmem_ld16(tbase + 128 + 16 * c, Mv);
+            tmem_ld16(tS + 16 * c, Sv);
+            tmem_ld16(tS + 128 + 16 * c, Mv);
             tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 16; ++j) acc[16 * c + j] += s_da[16 * c + j] * fmaf(dw, Sv[j], -dmin * Mv[j]);
+            for (int j = 0; j < 8; ++j) {
+              const float2 da = *reinterpret_cast<const float2*>(s_da + 16 * kl + 2 * j);
+              const unsigned long long t =
+                  f2_fma(dw2, f2_pack(Sv[2 * j], Sv[2 * j + 1]), f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
+              acc[8 * kl + j] = f2_fma(f2_pack(da.x, da.y), t, acc[8 * kl + j]);
+            }
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty(ab));
+        ++tb;
       }
-      tc_fence_before();
-      __syncthreads();
-    }
-    if (failed) break;
-    // ---- output
-    if (MODE == 0) {
-      // warps 2,3 hold U of rows 0..63 (lanes 64..127): pass them to warps 0,1 through shared memory
-      float* s_u = reinterpret_cast<float*>(sm + kSmA);  // [64][128]
-      if (warp == 2 || warp == 3) {
-        const int g = 32 * warp + lane - 64;
+      if (!ok) break;
 #pragma unroll
-        for (int j = 0; j < kTileN; ++j) s_u[j * 64 + g] = acc[j];
-      }
-      __syncthreads();
-      if (warp < 2) {
-        const int g = 32 * warp + lane;
-        const int col = it.wtile * 64 + g;
-#pragma unroll
-        for (int j = 0; j < kTileN; ++j)
-          if (j < ntok) {
-            const float Gv = acc[j], Uv = s_u[j * 64 + g];
-            a.h[(size_t)(it.start + j) * N_out + col] = Gv / (1.0f + expf(-Gv)) * Uv;
+      for (int p = 0; p < 32; ++p) {
+        const int kl = p >> 3, j = 2 * (p & 7);
+        const int tok = 16 * (2 * kl + cg) + j;  // tokens tok, tok + 1 (local 16*kl + j, + 1)
+        const float lo = __uint_as_float((uint32_t)acc[p]), hi = __uint_as_float((uint32_t)(acc[p] >> 32));
+        if (MODE == 0) {
+          // lane pairs hold gate (even lane) and up (odd lane) of one row: SwiGLU in registers
+          const float G0 = __shfl_sync(0xffffffffu, lo, lane & ~1), G1 = __shfl_sync(0xffffffffu, hi, lane & ~1);
+          float* hcol = a.h + (int64_t)(it.start + tok) * N_out + it.wtile * 64 + (m >> 1);
+          if (lane & 1) {
+            if (tok < ntok) hcol[0] = __fdividef(G0, 1.0f + __expf(-G0)) * lo;
+            if (tok + 1 < ntok) hcol[N_out] = __fdividef(G1, 1.0f + __expf(-G1)) * hi;
           }
+        } else {
+          // local token index l = 16*kl + j lives in lane l % 32 of slot0 (l < 32) or slot1
+          const int l = 16 * kl + j;
+          const int s0 = __shfl_sync(0xffffffffu, l < 32 ? slot0 : slot1, l & 31);
+          const int s1 = __shfl_sync(0xffffffffu, l + 1 < 32 ? slot0 : slot1, (l + 1) & 31);
+          const int col = it.wtile * 128 + m;
+          if (tok < ntok) a.y[(int64_t)s0 * N_out + col] = lo;
+          if (tok + 1 < ntok) a.y[(int64_t)s1 * N_out + col] = hi;
+        }
       }
-      __syncthreads();
-    } else {
-      if (warp < 4) {
-        const int m = 32 * warp + lane;
-        const int col = it.wtile * 128 + m;
-#pragma unroll
-        for (int j = 0; j < kTileN; ++j)
-          if (j < ntok) a.y[(size_t)a.perm[it.start + j] * N_out + col] = acc[j];
-      }
-      __syncthreads();
     }
+  }
+  // wait statistics of CTA 0, one thread per role (SM cycles):
+  //   [0] producer: raw slot free   [1] producer: activation slot free
+  //   [2] expander: raw data        [3] expander: weight slot free
+  //   [4] MMA: accumulator free     [5] MMA: operands ready
+  //   [6] epilogue: accumulator     [7] total cycles of the CTA
+  if (a.stats && blockIdx.x == 0) {
+    unsigned long long* st = a.stats + 8 * MODE;
+    if (tid == 32 * kWarpProducer) { st[0] = w0; st[1] = w1; }
+    if (tid == 32 * kEpiWarps) { st[2] = w0; st[3] = w1; }
+    if (tid == 32 * kWarpMma) { st[4] = w0; st[5] = w1; }
+    if (tid == 0) st[6] = w0;
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  if (a.stats && blockIdx.x == 0 && tid == 0) a.stats[8 * MODE + 7] = clock64() - t_start;
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 512;" ::"r"(tmem));
+  }
+}
+
+// ---------------------------------------------------------------- host side
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D fp16 tensor map: `inner` elements per row, `rows` rows, box {box_inner, box_rows}
+bool make_map(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+              uint32_t box_rows, bool swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 2};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int FMT, int MODE>
-cudaError_t launch_gemm_t(const PrefillArgs& a, int max_items, cudaStream_t s) {
+cudaError_t launch_gemm_t(const GemmArgs& g, int max_items, cudaStream_t s) {
   auto kern = prefill_gemm_kernel<FMT, MODE>;
   static bool opted = false;
   if (!opted) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmTotal);
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmAlloc);
     if (err != cudaSuccess) return err;
     opted = true;
   }
   const int grid = std::max(1, std::min(max_items, num_sms()));
   note_launch();
-  kern<<<grid, kPThreads, kSmTotal, s>>>(a);
+  kern<<<grid, kPThreads, kSmAlloc, s>>>(g);
   return cudaGetLastError();
 }
 
 template <int FMT>
-cudaError_t launch_prefill_fmt(const PrefillArgs& a0, cudaStream_t s) {
-  PrefillArgs a = a0;
+cudaError_t launch_gather(const int8_t* q, const int16_t* bs, const float* d, const int32_t* perm, int T, int k,
+                          int64_t P, int K, __half* xg, __half* sg, float* dg, cudaStream_t s) {
+  const int64_t blocks = std::max<int64_t>(1, std::min<int64_t>((P + 7) / 8, 16 * num_sms()));
+  note_launch();
+  prefill_gather_kernel<FMT><<<(unsigned)blocks, 256, 0, s>>>(q, bs, d, perm, T, k, P, K, xg, sg, dg);
+  return cudaGetLastError();
+}
+
+template <int FMT>
+cudaError_t launch_prefill_fmt(const PrefillArgs& a, cudaStream_t s) {
   const int EpS = a.E + a.S;
-  // gate/up
+  GemmArgs g{};
+  g.fmt = a.fmt;
+  g.H = a.H;
+  g.I = a.I;
+  g.T = a.T;
+  g.k = a.k;
+  g.P = a.P;
+  g.table = a.table;
+  g.perm = a.perm;
+  g.dg = a.dg;
+  g.items = a.items;
+  g.n_items = a.n_items;
+  g.h = a.h;
+  g.y = a.y;
+  g.status = a.status;
+  g.stats = a.stats;
+  // ---- gate/up: x codes gathered into bucket order
+  __half* xg = static_cast<__half*>(a.xg);
+  __half* sg = static_cast<__half*>(a.sg);
+  cudaError_t err = launch_gather<FMT>(a.xq, a.xbs, a.xd, a.perm, a.T, a.k, a.P, a.H, xg, sg, a.dg, s);
+  if (err != cudaSuccess) return err;
+  if (!make_map(&g.map_x, a.xg, (uint64_t)a.H, (uint64_t)a.P, 64, kBoxRows, true) ||
+      !make_map(&g.map_s, a.sg, 8, (uint64_t)(a.H / 256) * 2 * a.P, 8, 128, false))
+    return cudaErrorInvalidValue;
   int max_items = (int)std::min<int64_t>((a.P / kTileN + EpS) * (a.I / 64), a.max_items);
   note_launch();
   prefill_plan_kernel<<<1, 1024, 0, s>>>(a.counts, a.offsets, EpS, a.table, a.I / 64, a.items, a.n_items, max_items);
-  cudaError_t err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   trace_record(s);
-  err = launch_gemm_t<FMT, 0>(a, max_items, s);
+  err = launch_gemm_t<FMT, 0>(g, max_items, s);
   trace_record(s);
   if (err != cudaSuccess) return err;
-  // q8_K of h, one row per bucket position
-  err = launch_q8k_quantize(a.h, a.P, a.I, a.hq, a.hd, a.hbs, s);
-  if (err != cudaSuccess) return err;
-  // down
+  // ---- q8_K of h (bucket order), its gathered planes, down
+  if ((err = launch_q8k_quantize(a.h, a.P, a.I, a.hq, a.hd, a.hbs, s)) != cudaSuccess) return err;
+  if ((err = launch_gather<FMT>(a.hq, a.hbs, a.hd, nullptr, a.T, a.k, a.P, a.I, xg, sg, a.dg, s)) != cudaSuccess)
+    return err;
+  if (!make_map(&g.map_x, a.xg, (uint64_t)a.I, (uint64_t)a.P, 64, kBoxRows, true) ||
+      !make_map(&g.map_s, a.sg, 8, (uint64_t)(a.I / 256) * 2 * a.P, 8, 128, false))
+    return cudaErrorInvalidValue;
   max_items = (int)std::min<int64_t>((a.P / kTileN + EpS) * (a.H / 128), a.max_items);
   note_launch();
   prefill_plan_kernel<<<1, 1024, 0, s>>>(a.counts, a.offsets, EpS, a.table, a.H / 128, a.items, a.n_items, max_items);
-  err = cudaGetLastError();
-  if (err != cudaSuccess) return err;
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
   trace_record(s);
-  err = launch_gemm_t<FMT, 1>(a, max_items, s);
+  err = launch_gemm_t<FMT, 1>(g, max_items, s);
   trace_record(s);
   if (err != cudaSuccess) return err;
   note_launch();

@@ -278,6 +278,10 @@ int moe_layer_forward_noalloc(const moe_layer_desc* desc, const moe_expert_ptrs*
  * Returns MOE_OK, a device-recorded error, or MOE_ERR_CUDA. */
 int moe_get_status(void* ws, void* stream);
 
+/* The cudaError_t code of the last failed CUDA call made by this library on
+ * the calling host thread (0 if none).  Explains an MOE_ERR_CUDA status. */
+int moe_last_cuda_error(void);
+
 /* Human-readable name of a status code (static string). */
 const char* moe_status_string(int status);
 

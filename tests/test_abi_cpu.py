@@ -130,3 +130,12 @@ def test_kernel_launch_count_is_monotonic(lib):
     fake = ctypes.c_void_p(0x10000)
     assert L.moe_q8k_quantize(fake, 0, 256, fake, fake, None, None) == moe.MOE_OK   # T = 0: nothing launched
     assert moe.moe_kernel_launch_count() == a >= 0
+
+
+def test_prefill_parity_cases_take_the_tensor_path(lib):
+    # the whole-layer parity cases meant for the tcgen05 GEMMs really reach them
+    for fmt, route, H, I, E, k, S, T in [(0, 0, 512, 256, 8, 2, 1, 512), (1, 1, 768, 512, 16, 4, 0, 300),
+                                         (0, 1, 1024, 256, 4, 1, 2, 257), (0, 0, 512, 256, 8, 2, 1, 512),
+                                         (0, 1, 4096, 1024, 512, 10, 1, 8192)]:
+        d = desc(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+        assert moe.moe_layer_path(d, T) == moe.PATH_TENSOR_PREFILL
