@@ -89,12 +89,18 @@ def measured_tensor_peak():
         return 1700.0, "fallback (sustained)"
 
 
-def kernel_source_hash():
+# translation unit defining each profiled kernel (plus the shared headers)
+KERNEL_SOURCES = {"decode_fused_kernel": "moe_decode.cu", "prefill_gemm_kernel": "moe_prefill.cu",
+                  "gateup_kernel": "moe_ffn.cu"}
+
+
+def kernel_source_hash(kernel):
+    """Hash of the sources a kernel is built from, to tell whether a profile still applies."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_routed_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh", ".h")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in [KERNEL_SOURCES[kernel], "moe_device.cuh", "moe_internal.h"]:
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    h.update(open(os.path.join(ROOT, "include", "moe_q8k.h"), "rb").read())
     return h.hexdigest()[:16]
 
 
@@ -104,7 +110,7 @@ def profiled_traffic(workload_name, kernel):
     pdir = os.path.join(ROOT, "profiles")
     if not os.path.isdir(pdir):
         return None
-    want = kernel_source_hash()
+    want = kernel_source_hash(kernel)
     for f in sorted(os.listdir(pdir)):
         if not f.endswith(".md"):
             continue
@@ -176,16 +182,30 @@ def host_inputs(wl, T, R):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_layers(wl, T, x_rl, layers, nthreads):
-    """Run the oracle on the given layers of one rotation (x_rl [L, T, H]);
-    experts are generated on the host for the routed ones only.  Returns
-    (outputs {layer: fp64 [T, H]}, seconds spent in the oracle)."""
+# Tokens are independent through a layer (routing, expert FFNs and combine
+# are per token), so the oracle may run a subset of a chunk's tokens and the
+# result rows are exactly the chunk's rows for those tokens.
+ORACLE_MAX_TOKENS = 64
+
+
+def token_sample(T):
+    """All tokens of small chunks; for large ones 64 tokens spread over the chunk (first and last included)."""
+    if T <= ORACLE_MAX_TOKENS:
+        return np.arange(T)
+    return np.unique(np.linspace(0, T - 1, ORACLE_MAX_TOKENS).round().astype(np.int64))
+
+
+def oracle_layers(wl, T, x_rl, layers, nthreads, tokens=None):
+    """Run the oracle on the given layers of one rotation (x_rl [L, T, H]),
+    on the rows `tokens` (default all); experts are generated on the host
+    for the routed ones only.  Returns (outputs {layer: fp64 [len(tokens), H]},
+    seconds spent in the oracle)."""
     import oracle
     outs, spent = {}, 0.0
     for l in layers:
         wr = synth.router_weight(wl.E, wl.H, wl.seed, l)
         bias = synth.router_bias(wl.E, wl.bias_std, wl.seed, l) if wl.bias_std > 0 else None
-        x = x_rl[l]
+        x = x_rl[l] if tokens is None else np.ascontiguousarray(x_rl[l][tokens])
         _, ids, _, _ = oracle.route(x, wr, bias, wl.k, wl.route)
         need = sorted(set(ids.reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
         experts = [None] * (wl.E + wl.S)
@@ -204,18 +224,19 @@ def oracle_layers(wl, T, x_rl, layers, nthreads):
 def cpu_baseline(wl, T, x_host, budget_s):
     import oracle
     nthreads = oracle.default_threads()
+    tokens = token_sample(T)
     done, spent = 0, 0.0
     layers = []
     while spent < budget_s and done < wl.layers * 4:
         l = done % wl.layers
-        _, s = oracle_layers(wl, T, x_host[0], [l], nthreads)
+        _, s = oracle_layers(wl, T, x_host[0], [l], nthreads, tokens)
         spent += s
         layers.append(l)
         done += 1
-    tok_s = (done / wl.layers) * T / spent
+    tok_s = (done / wl.layers) * len(tokens) / spent
     return {"value": tok_s, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{done} of {wl.layers} layers x {T} token(s) of rotation 0 ({spent:.1f} s of oracle time); "
-                      f"tokens/s = layers done / layers per step * tokens / seconds"}
+            "sample": f"{done} of {wl.layers} layers x {len(tokens)} of {T} token(s) of rotation 0 "
+                      f"({spent:.1f} s of oracle time); tokens/s = layers done / layers per step * tokens / seconds"}
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -230,23 +251,26 @@ def run_reference(args, wl, T):
     W = max(args.warmup if args.warmup is not None else 1, 0)
     x_host = host_inputs(wl, T, 1)
     nthreads = oracle.default_threads()
+    tokens = token_sample(T)
     # size each step's sample so that the whole run stays within ~2 minutes
-    _, t_layer = oracle_layers(wl, T, x_host[0], [0], nthreads)
+    _, t_layer = oracle_layers(wl, T, x_host[0], [0], nthreads, tokens)
     per_step = max(1, min(wl.layers, int(120.0 / max(K + W, 1) / max(t_layer, 1e-3))))
     for i in range(W):
-        oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads)
+        oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads, tokens)
     spent = 0.0
     for i in range(K):
-        _, s = oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads)
+        _, s = oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads,
+                             tokens)
         spent += s
-    tok_s = (K * per_step / wl.layers) * T / spent
+    tok_s = (K * per_step / wl.layers) * len(tokens) / spent
     line = {
         "impl": "reference", "metric": METRIC, "value": tok_s, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": 1e3 * spent / K, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64 (int64 sub-block sums)", "data": "synthetic",
         "config": {"workload": wl.name, "layers": wl.layers, "T": T, "sample_layers_per_step": per_step},
         "cpu_baseline": {"kind": "oracle", "cores": nthreads, "value": tok_s, "unit": "tokens/s",
-                         "sample": f"{per_step} of {wl.layers} layers per step, {T} token(s) per layer"},
+                         "sample": f"{per_step} of {wl.layers} layers per step, {len(tokens)} of {T} token(s) "
+                                   f"per layer"},
         "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -522,12 +546,13 @@ def run_ours(args, wl, T):
         line["cpu_baseline"] = cpu_baseline(wl, T, x_host, args.cpu_budget_s)
         # parity spot check of the bench's own launch configuration on the first layers
         import oracle
-        outs, _ = oracle_layers(wl, T, x_host[0], [0, L - 1], oracle.default_threads())
+        tokens = token_sample(T)
+        outs, _ = oracle_layers(wl, T, x_host[0], sorted({0, L - 1}), oracle.default_threads(), tokens)
         worst = 0.0
         for l, ref in outs.items():
-            err = np.abs(out_r0[l] - ref) / (1e-4 + 1e-3 * np.linalg.norm(ref, axis=1, keepdims=True))
+            err = np.abs(out_r0[l][tokens] - ref) / (1e-4 + 1e-3 * np.linalg.norm(ref, axis=1, keepdims=True))
             worst = max(worst, float(err.max()))
-        line["parity_spot_check"] = {"layers": sorted(outs), "worst_err_over_tol": worst}
+        line["parity_spot_check"] = {"layers": sorted(outs), "tokens": int(len(tokens)), "worst_err_over_tol": worst}
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

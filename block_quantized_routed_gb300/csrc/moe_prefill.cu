@@ -26,16 +26,18 @@
 // GEMM that unpacks super-blocks to shared memory and rescales per block).
 // tcgen05 offers no int8 kind on sm_103a, hence exact-integer fp16.
 //
-// Kernel organisation (one persistent CTA per SM, 448 threads, warp roles):
-//   warp 12      producer: cp.async.bulk of the raw weight slabs and TMA
+// Kernel organisation (one persistent CTA per SM, 832 threads, warp roles):
+//   warp 24      producer: cp.async.bulk of the raw weight slabs and TMA
 //                tiles of the activation codes / code sums into rings
-//   warps 8-11   expanders: raw slab -> fp16 sc*q tile (one weight row per
-//                thread), mins tile for the min MMA
-//   warp 13      MMA issuer (one thread): 8 MMAs per half super-block into a
+//   warps 16-23  expanders: raw slab -> fp16 sc*q tile (two threads per
+//                weight row, one swizzle atom each), mins tile for the min MMA
+//   warp 25      MMA issuer (one thread): 8 MMAs per half super-block into a
 //                double-buffered TMEM accumulator, the min MMA with the last
 //                half; commits are grouped (a commit costs the issuing
 //                thread several hundred cycles, so each group carries 8+ MMAs)
-//   warps 0-7    epilogue: TMEM -> registers, per-block rescale, output
+//   warps 0-15   epilogue: TMEM -> registers, per-block rescale, output
+// (26 warps at 72 registers: the register file is split between the SM's
+// four sub-partitions, so the warp count bounds the registers per thread.)
 // Rings: 3 activation stages and 2 expanded-weight stages of 128 K each
 // (two 128-byte swizzle atoms), 2 raw stages of one super-block column.
 // A work item is (expert, token tile of <= 128 bucket rows, weight tile of
@@ -68,10 +70,10 @@ constexpr int kStagesA = 2;                          // expanded-weight stages
 constexpr int kStagesB = 3;                          // activation stages
 constexpr int kRaw = 2;                              // raw stages (one super-block column each)
 constexpr int kBoxRows = 32;                         // token rows per TMA box
-constexpr int kEpiWarps = 8, kExpWarps = 4;         // expanders: one thread per tile row
-constexpr int kWarpProducer = kEpiWarps + kExpWarps; // 12
-constexpr int kWarpMma = kWarpProducer + 1;          // 13
-constexpr int kPThreads = 32 * (kWarpMma + 1);       // 448
+constexpr int kEpiWarps = 16, kExpWarps = 8;        // epilogue: 32 tokens per warp; expanders: two threads per row
+constexpr int kWarpProducer = kEpiWarps + kExpWarps; // 24
+constexpr int kWarpMma = kWarpProducer + 1;          // 25
+constexpr int kPThreads = 32 * (kWarpMma + 1);       // 832
 constexpr long long kWaitCycles = 2000000000ll;      // ~1 s at 2 GHz: a wait that long has failed
 
 // shared memory (offsets from a 1024-byte aligned base).  A stage holds two
@@ -85,8 +87,8 @@ constexpr int kSmA = kSmB + kStagesB * kBStage;
 constexpr int kSmRaw = kSmA + kStagesA * kAStage;
 constexpr int kSmA2 = kSmRaw + kRaw * kRawBytes;     // mins tile [128 rows][16] per raw stage
 constexpr int kSmB2 = kSmA2 + kRaw * 4096;           // code-sum tile [128 tokens][16] per raw stage
-constexpr int kSmDa = kSmB2 + kRaw * 4096;           // per epilogue warp: the block scales of its 64 tokens
-constexpr int kSmBar = kSmDa + kEpiWarps * 64 * 4;
+constexpr int kSmDa = kSmB2 + kRaw * 4096;           // per epilogue warp: the block scales of its 32 tokens
+constexpr int kSmBar = kSmDa + kEpiWarps * 32 * 4;
 constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 * kRaw + 4;
 constexpr int kSmMisc = kSmBar + 8 * 32;
 constexpr int kSmUsed = kSmMisc + 16;
@@ -242,6 +244,14 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
       : "r"(taddr));
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
@@ -513,7 +523,8 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     // tile row r: gate/up interleaved (even r: gate row r/2 of the 64-row
     // group, odd r: the same row of up), down: row r of the 128-row group.
     // Two threads per row: `hx` picks the 64-wide atom of each stage.
-    const int r = tid - 32 * kEpiWarps;
+    const int x = tid - 32 * kEpiWarps;
+    const int r = x & 127, hx = x >> 7;
     const int g = MODE == 0 ? ((r & 1) * 2 + (r >> 6)) : (r >> 5);  // slab of the raw stage
     const int lr = MODE == 0 ? ((r >> 1) & 31) : (r & 31);         // row inside the slab
     uint32_t ri = 0;
@@ -547,8 +558,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           if constexpr (FMT == kQ4K) return (int)((sm_hi >> (6 * j)) & 63);
           else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7) + 4)) & 15);
         };
-#pragma unroll
-        for (int hx = 0; hx < 2; ++hx) {
+        {
           // A2 row r, K 8*hx .. 8*hx+7: Q4_K [mn_0..7 | 64 * mn_0..7], Q2_K mn_0..15
           float f[8];
 #pragma unroll
@@ -565,8 +575,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         for (int c = 0; c < 256 / kStageK; ++c) {
           if (!(ok = warp_wait(empty_a(as), pa ^ 1, abort_flag, a.status, w1))) break;
           uint8_t* A = sm + kSmA + as * kAStage;
-#pragma unroll
-          for (int hx = 0; hx < 2; ++hx) {
           if constexpr (FMT == kQ4K) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
@@ -597,7 +605,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
               *reinterpret_cast<uint4*>(A + sw128_off(r, k0)) = scaled8(w[0], w[1], sc2, off2);
               *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 8)) = scaled8(w[2], w[3], sc2, off2);
             }
-          }
           }
           fence_async_smem();
           __syncwarp();
@@ -658,13 +665,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       }
     }
   } else {
-    // ------------------------------------------------------------ epilogue (warps 0-7)
+    // ------------------------------------------------------------ epilogue (warps 0-15)
     // Warp (qd, cg) owns TMEM lanes 32*qd.. (tile rows) and the 16-token
-    // chunks cg, cg+2, cg+4, cg+6 (local token index 16*kl + j is token
-    // 16*(2*kl + cg) + j), so both column groups share short tiles evenly.
+    // chunks cg and cg + 4 (local token index 16*kl + j is token
+    // 16*(4*kl + cg) + j), so the four column groups share short tiles evenly.
     const int qd = warp & 3, cg = warp >> 2;
     const int m = 32 * qd + lane;             // tile row
-    float* s_da = reinterpret_cast<float*>(sm + kSmDa) + 64 * warp;
+    float* s_da = reinterpret_cast<float*>(sm + kSmDa) + 32 * warp;
     uint32_t tb = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
@@ -680,54 +687,49 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         const int i = it.wtile * 128 + m;
         hdr = static_cast<const uint8_t*>(ep.down) + (size_t)(i >> 5) * nb * slab_bytes + 4 * (i & 31);
       }
-      unsigned long long acc[32];  // pairs of local tokens (2i, 2i+1)
+      unsigned long long acc[16];  // pairs of local tokens (2i, 2i+1)
 #pragma unroll
-      for (int j = 0; j < 32; ++j) acc[j] = 0ull;
-      // tokens of this lane's two prefetched scales: local l and 32 + l
-      const int tk0 = 16 * (2 * (lane >> 4) + cg) + (lane & 15), tk1 = tk0 + 64;
-      const float* dgp = a.dg + it.start;
-      const bool v0 = tk0 < ntok, v1 = tk1 < ntok;
-      // down: the slot rows of the same tokens, for the output
-      int slot0 = 0, slot1 = 0;
-      if (MODE == 1) {
-        slot0 = v0 ? __ldg(a.perm + it.start + tk0) : 0;
-        slot1 = v1 ? __ldg(a.perm + it.start + tk1) : 0;
-      }
+      for (int j = 0; j < 16; ++j) acc[j] = 0ull;
+      // this lane's token: local index `lane`
+      const int tk = 16 * (4 * (lane >> 4) + cg) + (lane & 15);
+      const bool vt = tk < ntok;
+      const int slot = (MODE == 1 && vt) ? __ldg(a.perm + it.start + tk) : 0;  // down: its slot row
+      const float* dgp = a.dg + it.start + tk;
       // the scales of block b + 1 are loaded while block b is processed
       uint32_t dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr));
-      float da0_n = v0 ? __ldg(dgp + tk0) : 0.0f, da1_n = v1 ? __ldg(dgp + tk1) : 0.0f;
+      float da_n = vt ? __ldg(dgp) : 0.0f;
       for (int b = 0; b < nb; ++b) {
         const int ab = tb & 1;
         const uint32_t dm = dm_n;
-        const float da0 = da0_n, da1 = da1_n;
+        const float da = da_n;
         if (b + 1 < nb) {
           dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr + (size_t)(b + 1) * slab_bytes));
-          const float* dgb = dgp + (int64_t)(b + 1) * a.P;
-          da0_n = v0 ? __ldg(dgb + tk0) : 0.0f;
-          da1_n = v1 ? __ldg(dgb + tk1) : 0.0f;
+          da_n = vt ? __ldg(dgp + (int64_t)(b + 1) * a.P) : 0.0f;
         }
         if (!(ok = warp_wait(tfull(ab), (tb >> 1) & 1, abort_flag, a.status, w0))) break;
         tc_fence_after();
-        s_da[lane] = da0;
-        s_da[32 + lane] = da1;
+        s_da[lane] = da;
         __syncwarp();
         const float dw = half_lo(dm), dmin = half_hi(dm);
         const unsigned long long dw2 = f2_pack(dw, dw), ndm2 = f2_pack(-dmin, -dmin);
         const uint32_t tS = tmem + ((uint32_t)(32 * qd) << 16) + ab * 256;
 #pragma unroll
-        for (int kl = 0; kl < 4; ++kl) {
-          const int c = 2 * kl + cg;  // chunk of 16 tokens
+        for (int kl = 0; kl < 2; ++kl) {
+          const int c = 4 * kl + cg;  // chunk of 16 tokens
           if (16 * c < N) {
-            float Sv[16], Mv[16];
-            tmem_ld16(tS + 16 * c, Sv);
-            tmem_ld16(tS + 128 + 16 * c, Mv);
-            tmem_wait_ld();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              const float2 da = *reinterpret_cast<const float2*>(s_da + 16 * kl + 2 * j);
-              const unsigned long long t =
-                  f2_fma(dw2, f2_pack(Sv[2 * j], Sv[2 * j + 1]), f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
-              acc[8 * kl + j] = f2_fma(f2_pack(da.x, da.y), t, acc[8 * kl + j]);
+            for (int hh = 0; hh < 2; ++hh) {
+              float Sv[8], Mv[8];
+              tmem_ld8(tS + 16 * c + 8 * hh, Sv);
+              tmem_ld8(tS + 128 + 16 * c + 8 * hh, Mv);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const float2 d2 = *reinterpret_cast<const float2*>(s_da + 16 * kl + 8 * hh + 2 * j);
+                const unsigned long long t =
+                    f2_fma(dw2, f2_pack(Sv[2 * j], Sv[2 * j + 1]), f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
+                acc[8 * kl + 4 * hh + j] = f2_fma(f2_pack(d2.x, d2.y), t, acc[8 * kl + 4 * hh + j]);
+              }
             }
           }
         }
@@ -738,9 +740,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       }
       if (!ok) break;
 #pragma unroll
-      for (int p = 0; p < 32; ++p) {
+      for (int p = 0; p < 16; ++p) {
         const int kl = p >> 3, j = 2 * (p & 7);
-        const int tok = 16 * (2 * kl + cg) + j;  // tokens tok, tok + 1 (local 16*kl + j, + 1)
+        const int l = 16 * kl + j;                // local index of tokens tok, tok + 1
+        const int tok = 16 * (4 * kl + cg) + j;
         const float lo = __uint_as_float((uint32_t)acc[p]), hi = __uint_as_float((uint32_t)(acc[p] >> 32));
         if (MODE == 0) {
           // lane pairs hold gate (even lane) and up (odd lane) of one row: SwiGLU in registers
@@ -751,10 +754,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             if (tok + 1 < ntok) hcol[N_out] = __fdividef(G1, 1.0f + __expf(-G1)) * hi;
           }
         } else {
-          // local token index l = 16*kl + j lives in lane l % 32 of slot0 (l < 32) or slot1
-          const int l = 16 * kl + j;
-          const int s0 = __shfl_sync(0xffffffffu, l < 32 ? slot0 : slot1, l & 31);
-          const int s1 = __shfl_sync(0xffffffffu, l + 1 < 32 ? slot0 : slot1, (l + 1) & 31);
+          const int s0 = __shfl_sync(0xffffffffu, slot, l), s1 = __shfl_sync(0xffffffffu, slot, l + 1);
           const int col = it.wtile * 128 + m;
           if (tok < ntok) a.y[(int64_t)s0 * N_out + col] = lo;
           if (tok + 1 < ntok) a.y[(int64_t)s1 * N_out + col] = hi;
