@@ -67,6 +67,24 @@ def dist_env():
     return world, rank, local
 
 
+def rank_barrier():
+    """Barrier across the ranks of an initialised process group (no-op for one process)."""
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized() and dist.get_world_size() > 1:
+        dist.barrier()
+
+
+def max_over_ranks(value, device=None):
+    """The largest `value` of all ranks (every rank gets it); `value` itself for one process."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return value
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return type(value)(t.item())
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -381,14 +399,10 @@ def run_ours(args, wl, T):
     torch.cuda.synchronize()
     t_step = (time.perf_counter() - t0) / 5
     K = args.steps if args.steps is not None else int(min(20000, max(20, 3.0 / max(t_step, 1e-6))))
-
-    def barrier():
-        if world > 1:
-            import torch.distributed as dist
-            dist.barrier()
+    K = max_over_ranks(K, dev)          # every rank times the same number of steps
 
     clocks = ClockSampler(local)
-    barrier()
+    rank_barrier()
     torch.cuda.synchronize()
     clocks.start()
     ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -398,13 +412,8 @@ def run_ours(args, wl, T):
     ev1.record(stream)
     torch.cuda.synchronize()
     clock_info = clocks.stop()
-    barrier()
-    ms_total = ev0.elapsed_time(ev1)
-    if world > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([ms_total], device=dev)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        ms_total = float(tt.item())
+    rank_barrier()
+    ms_total = max_over_ranks(ev0.elapsed_time(ev1), dev)
     ms_step = ms_total / K
 
     # phase stamps (SM cycles of CTA 0) of the single-launch kernel's last layer
