@@ -53,6 +53,8 @@ def parse_args():
                     help="layers (overrides the workload's; smaller cases for profiling captures)")
     ap.add_argument("--rotations", type=int, default=16, help="distinct input sets cycled through the steps")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--chained", action="store_true",
+                    help="layer l reads layer l-1's output (a decode step through the stack) instead of its own input")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
     return ap.parse_args()
@@ -108,7 +110,8 @@ def measured_tensor_peak():
 
 
 # translation unit defining each profiled kernel (plus the shared headers)
-KERNEL_SOURCES = {"decode_fused_kernel": "moe_decode.cu", "prefill_gemm_kernel": "moe_prefill.cu",
+KERNEL_SOURCES = {"decode_fused_kernel": "moe_decode.cu", "decode_stack_kernel": "moe_decode.cu",
+                  "prefill_gemm_kernel": "moe_prefill.cu",
                   "gateup_kernel": "moe_ffn.cu"}
 
 
@@ -321,8 +324,12 @@ def run_ours(args, wl, T):
     out = torch.empty((L, T, H), dtype=torch.float32, device=dev)
     ids_buf = torch.empty((L, T, wl.k), dtype=torch.int32, device=dev)
     desc = wl.desc(T)
-    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device=dev)
-    rows = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=x_static[l], residual=x_static[l],
+    ws = torch.zeros(max(moe.moe_layer_workspace_size(desc), moe.moe_stack_workspace_size(desc, L)),
+                     dtype=torch.uint8, device=dev)
+    def xin(l):  # layer l's input (and residual)
+        return out[l - 1] if args.chained and l > 0 else x_static[l]
+
+    rows = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=xin(l), residual=xin(l),
                  out=out[l], ids_out=ids_buf[l]) for l in range(L)]
     stack = moe.stack_pointer_table(rows, device=dev)
     # the single-launch stack serves decode shapes; other shapes run layer by layer
@@ -343,7 +350,7 @@ def run_ours(args, wl, T):
             moe.moe_stack_forward(desc, stack, T, ws)
         else:
             for l in range(L):
-                layers[l].forward(x_static[l], residual=x_static[l], out=out[l], ids_out=ids_buf[l])
+                layers[l].forward(xin(l), residual=xin(l), out=out[l], ids_out=ids_buf[l])
 
     # unique active experts per layer for every rotation (counted from the routing)
     union = np.zeros((R, L), np.int64)
@@ -429,6 +436,19 @@ def run_ours(args, wl, T):
                   "gate_up": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[0:8])},
                   "down": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[8:16])}}
         st = np.zeros(16, np.int64)
+    if stacked and path == moe.PATH_DECODE_FUSED:
+        # per item kind of the stack kernel, summed over CTAs: work and wait cycles, items
+        mhz = clock_info.get("sm_mhz") or 2070.0
+        kinds = ["router", "routing", "gate_up", "down", "combine"]
+        G_ = int(torch.cuda.get_device_properties(dev).multi_processor_count) * 2
+        us = lambda v: round(float(v) / mhz, 1)
+        phases = {"schedule": "stack_items_" + ("overlapped" if st[15] == 2 else "chained"),
+                  "cta_us_summed_over_ctas": {**{f"work_{n}": us(st[k_]) for k_, n in enumerate(kinds)},
+                                              **{f"wait_{n}": us(st[5 + k_]) for k_, n in enumerate(kinds)},
+                                              "prologue": us(st[10]), "before_first_item": us(st[11]),
+                                              "between_items": us(st[12])},
+                  "items": int(st[13]), "ctas_assumed": G_}
+        st = np.zeros(16, np.int64)
     if st[15] == 2:   # pipelined schedule: one stage
         order = [0, 3, 4, 6, 1, 8, 12]
         names = ["stage_x", "gate_up", "down_prev", "router_next2", "combine_prev2", "wait_route_next+prefetch"]
@@ -457,9 +477,9 @@ def run_ours(args, wl, T):
         launch_ms = events[0].elapsed_time(events[1])
         alg = float(union[last_r].sum() * exp_bytes + L * router_bytes)
         gbs = alg / (launch_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "decode_fused_kernel (all layers of a step, one cooperative launch)",
+        roofline = {"bound": "hbm", "kernel": "decode_stack_kernel (all layers of a step, one cooperative launch)",
                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
-                    "traffic": profiled_traffic(wl.name, "decode_fused_kernel"),
+                    "traffic": profiled_traffic(wl.name, "decode_stack_kernel"),
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * launch_ms}
     elif path == moe.PATH_TENSOR_PREFILL:
         # the tcgen05 gate/up GEMM (+ SwiGLU) is the dominant kernel; a contraction: tensor-bound
@@ -538,6 +558,7 @@ def run_ours(args, wl, T):
                          "plus %.0f MB of router weights (L2 129 MB)" % (
                              np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
                    "graph": use_graph, "rotations": R, "single_launch_stack": stacked,
+                   "layer_inputs": "chained" if args.chained else "independent",
                    "path": ["decode_fused", "gemv", "tensor_prefill"][path]},
         "clocks": clock_info,
         "us_per_layer": 1e3 * ms_step / L,
@@ -556,7 +577,9 @@ def run_ours(args, wl, T):
         # parity spot check of the bench's own launch configuration on the first layers
         import oracle
         tokens = token_sample(T)
-        outs, _ = oracle_layers(wl, T, x_host[0], sorted({0, L - 1}), oracle.default_threads(), tokens)
+        # a chained stack's later layers read GPU outputs: check the layer whose input is known
+        check = [0] if args.chained else sorted({0, L - 1})
+        outs, _ = oracle_layers(wl, T, x_host[0], check, oracle.default_threads(), tokens)
         worst = 0.0
         for l, ref in outs.items():
             err = np.abs(out_r0[l][tokens] - ref) / (1e-4 + 1e-3 * np.linalg.norm(ref, axis=1, keepdims=True))

@@ -21,7 +21,7 @@ __all__ = [
     "MoeError", "LayerDesc", "WsLayout", "FMT_Q4K", "FMT_Q2K", "ROUTE_SOFTMAX", "ROUTE_SIGMOID",
     "load", "lib", "moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_bucket_workspace_size",
     "moe_expert_ffn", "moe_expert_ffn_workspace_size", "moe_combine", "moe_layer_forward",
-    "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
+    "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "moe_stack_workspace_size", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
     "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
 ]
@@ -93,6 +93,7 @@ def load():
         "moe_combine": (ctypes.c_int, [P, P, I32, I32, I32, I32, P, P, P]),
         "moe_layer_forward": (ctypes.c_int, [D, P, P, P, P, P, P, I32, P, P, P, SZ, P]),
         "moe_stack_forward": (ctypes.c_int, [D, I32, P, I32, P, SZ, P]),
+        "moe_stack_workspace_size": (SZ, [D, I32]),
         "moe_layer_forward_noalloc": (ctypes.c_int, [D, P, P, P, P, P, P, I32, P, P, P]),
         "moe_get_status": (ctypes.c_int, [P, P]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
@@ -209,6 +210,10 @@ def moe_layer_forward_noalloc(desc, table, w_router, router_bias, x, residual, o
                                             _ptr(router_bias), _ptr(x), _ptr(residual), _ptr(out), T,
                                             _ptr(ids_out), _ptr(gates_out), _stream(stream)),
            "moe_layer_forward_noalloc")
+
+
+def moe_stack_workspace_size(desc, n_layers) -> int:
+    return int(load().moe_stack_workspace_size(ctypes.byref(_desc(desc)), n_layers))
 
 
 def moe_stack_forward(desc, layers, T, ws, stream=None):

@@ -448,6 +448,12 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
   return MOE_OK;
 }
 
+size_t moe_stack_workspace_size(const moe_layer_desc* desc, int32_t n_layers) {
+  int why;
+  if (!desc_valid(desc, &why) || n_layers < 1) return 0;
+  return (plan_workspace(*desc).total + 255) / 256 * 256 + stack_plan(*desc, n_layers).total;
+}
+
 int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
                       void* ws, size_t ws_bytes, void* stream) {
   int why;
@@ -458,8 +464,13 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   const int H = desc->H, E = desc->E, k = desc->top_k, S = desc->n_shared;
   if (T > kDecodeMaxT || (int64_t)T * k > kSmallPairs || decode_smem_bytes(T, H, desc->I, E, k, S) > kDecodeSmemMax)
     return MOE_ERR_UNSUPPORTED;
+  // the per-layer buffers are sized by the call's T (T_max only bounds it)
+  moe_layer_desc dT = *desc;
+  dT.T_max = T;
   const WsPlan p = plan_workspace(*desc);
-  if (ws_bytes < p.total) return MOE_ERR_WORKSPACE;
+  const size_t ext = (p.total + 255) / 256 * 256;
+  const StackPlan sp = stack_plan(dT, n_layers);
+  if (ws_bytes < ext + sp.total) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
   DecodeArgs d{};
@@ -471,19 +482,6 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   d.S = S;
   d.route = desc->route;
   d.T = T;
-  for (int i = 0; i < 3; ++i) {
-    d.xq[i] = static_cast<int8_t*>(at(p.xq_b[i]));
-    d.xd[i] = static_cast<float*>(at(p.xd_b[i]));
-    d.xbs[i] = static_cast<int16_t*>(at(p.xbs_b[i]));
-  }
-  for (int i = 0; i < 2; ++i) {
-    d.logits[i] = static_cast<float*>(at(p.logits_b[i]));
-    d.h[i] = static_cast<float*>(at(p.h_b[i]));
-    d.y[i] = static_cast<float*>(at(p.y_b[i]));
-  }
-  d.pipeline_ok = p.pipeline ? 1 : 0;
-  d.route_pub = p.pipeline ? static_cast<uint8_t*>(at(p.route_pub)) : nullptr;
-  d.route_flag = p.pipeline ? static_cast<unsigned long long*>(at(p.route_flag)) : nullptr;
   d.gap = static_cast<float*>(at(p.pub.gap));
   d.ids = static_cast<int32_t*>(at(p.pub.ids));
   d.gates = static_cast<float*>(at(p.pub.gates));
@@ -491,17 +489,16 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   d.offsets = static_cast<int32_t*>(at(p.pub.offsets));
   d.perm = static_cast<int32_t*>(at(p.pub.perm));
   d.inv = static_cast<int32_t*>(at(p.pub.inv));
-  d.hq = static_cast<int8_t*>(at(p.pub.hq));
-  d.hd = static_cast<float*>(at(p.pub.hd));
-  d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
   d.bar = static_cast<unsigned long long*>(at(p.bar));
   d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
   d.status = static_cast<int*>(at(p.pub.status));
   d.n_layers = n_layers;
   d.layers = layers;
+  d.stk = static_cast<uint8_t*>(at(ext));
+  d.sp = sp;
   cudaStream_t s = as_stream(stream);
   trace_record(s);
-  const cudaError_t err = record_error(launch_decode_fused(d, s));
+  const cudaError_t err = record_error(launch_decode_stack(d, s));
   trace_record(s);
   if (err == cudaErrorCooperativeLaunchTooLarge) {
     cudaGetLastError();

@@ -360,7 +360,7 @@ __device__ void prefetch_shared_gateup(const Ctx<FMT>& c, const LayerView& lv) {
 // ids_out / gates_out).
 template <int FMT>
 __device__ void routing_phase(Ctx<FMT>& c, const LayerView& lv, const float* logits, const Route& R, bool stamps,
-                              bool writer) {
+                              bool writer, bool write_out) {
   const DecodeArgs& a = c.a;
   const int T = c.T, E = c.E, k = c.k, S = c.S, EpS = c.EpS, P = c.P, tid = c.tid;
   Smem& sm = c.sm;
@@ -433,10 +433,13 @@ __device__ void routing_phase(Ctx<FMT>& c, const LayerView& lv, const float* log
     for (int p = tid; p < T * k; p += kDecThreads) {
       a.ids[p] = R.ids[p];
       a.gates[p] = R.gates[p];
+    }
+  }
+  if (write_out)
+    for (int p = tid; p < T * k; p += kDecThreads) {
       if (lv.ids_out) lv.ids_out[p] = R.ids[p];
       if (lv.gates_out) lv.gates_out[p] = R.gates[p];
     }
-  }
 }
 
 // L2 prefetch of the down weights of this CTA's down items [i0, i1) of a layer
@@ -733,7 +736,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
       if (!grid_barrier(a.bar, a.status)) return;
       c.stamp(2, st);
       stage_x(c, a.xq[0], a.xd[0], a.xbs[0]);
-      routing_phase(c, lv, a.logits[0], R, st, blockIdx.x == 0);
+      routing_phase(c, lv, a.logits[0], R, st, blockIdx.x == 0, blockIdx.x == 0);
       c.stamp(3, st);
       gateup_phase(c, lv, R, a.h[0], true);
       c.stamp(4, st);
@@ -774,7 +777,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
     if (router_cta) {
       if (s + 1 >= 0 && s + 1 < L) {
         const LayerView lv = layer_view(a, s + 1);
-        routing_phase(c, lv, a.logits[(s + 1) & 1], c.route((s + 1) & 3), false, true);
+        routing_phase(c, lv, a.logits[(s + 1) & 1], c.route((s + 1) & 3), false, true, true);
         const int4* src = reinterpret_cast<const int4*>(c.sm.rbase + (size_t)((s + 1) & 3) * rbytes);
         int4* dst = reinterpret_cast<int4*>(a.route_pub + (size_t)((s + 1) & 3) * rbytes);
         for (size_t i = c.tid; i < rbytes / 16; i += kDecThreads) dst[i] = src[i];
@@ -832,6 +835,545 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
   }
 }
 
+// ---------------------------------------------------------------- dataflow stack
+// moe_stack_forward: the stack as one sequence of small work items, handed
+// out round-robin (item i to CTA i % G, each CTA in increasing order), with
+// per-layer counters instead of grid barriers.  Item kinds of layer l:
+//   R   8 router rows (one warp each)                          -> logits_l
+//   Q   q8_K of x_l, top-k, bucketing, tile plan               -> route_l
+//   GU  (tile, 32-row group) of gate and up, SwiGLU            -> h_l
+//   D   (tile, 8 row groups) of down, on q8_K(h) of the tile   -> y_l by slot
+//   C   a chunk of out_l = residual + sum gate * y (fixed order)
+// An item waits (bounded) for the counters of what it reads: Q for all R of
+// its layer, GU for Q, D for the GU items of its tile, C for all D; in a
+// chained stack the R items of layer l also wait for all C of layer l-1.
+// Every item increments its counter, also when it has nothing to do (a
+// tile slot beyond the layer's tiles), so the targets are fixed counts; the
+// counters are zeroed at the start of the launch (one grid barrier).  Waits
+// point only at earlier items, and each CTA takes its items in order, so
+// every wait ends.
+// Item order: a stack whose layers neither read nor write each other's
+// buffers runs stage by stage, stage s holding R of layer s, Q of s-2, GU of
+// s-4, D of s-6 and C of s-8 (two stages of slack between an item and what
+// it waits for), so several layers overlap with no grid barrier; otherwise
+// layer by layer.  Each layer owns its buffers, so no
+// layer's data is overwritten while another still reads it.
+constexpr int kRouterRows = kDecWarps;  // router rows per R item
+constexpr int kCombineVec = 1024;       // float4 elements per C item
+constexpr int kDownRG = kDecWarps;      // row groups per D item (one per warp)
+
+__device__ __forceinline__ unsigned long long* stk_cnt(const DecodeArgs& a, int l, int j) {
+  return reinterpret_cast<unsigned long long*>(a.stk + a.sp.cnt) + (size_t)l * a.sp.n_cnt + j;
+}
+__device__ __forceinline__ uint8_t* stk_layer(const DecodeArgs& a, int l) {
+  return a.stk + a.sp.layer0 + (size_t)l * a.sp.layer_bytes;
+}
+
+__device__ __forceinline__ Route stk_route(const DecodeArgs& a, int l) {
+  return route_at(stk_layer(a, l) + a.sp.route, a.T, a.k, a.S);
+}
+__device__ __forceinline__ Tile ld_tile(const Tile* p) {
+  const int4 v = __ldcg(reinterpret_cast<const int4*>(p));
+  Tile t;
+  t.expert = v.x;
+  t.start = v.y;
+  t.count = v.z;
+  t.flag = v.w;
+  return t;
+}
+
+__device__ __forceinline__ moe_expert_ptrs ld_ptrs(const moe_expert_ptrs* p) {
+  const unsigned long long* q = reinterpret_cast<const unsigned long long*>(p);
+  moe_expert_ptrs e;
+  e.gate = reinterpret_cast<const void*>(__ldcg(q));
+  e.up = reinterpret_cast<const void*>(__ldcg(q + 1));
+  e.down = reinterpret_cast<const void*>(__ldcg(q + 2));
+  return e;
+}
+
+// Thread 0 waits (bounded) until *p >= target; every thread gets the answer.
+// Data behind the counter is then read through L2 (ld.global.cg).
+// While thread 0 polls, thread 32 runs `side` (the next item's L2 prefetch).
+template <typename Side>
+__device__ bool wait_count(const unsigned long long* p, unsigned long long target, int* status, Side side) {
+  __shared__ int s_ok;
+  __syncthreads();
+  if (threadIdx.x == 32) side();
+  if (threadIdx.x == 0) {
+    int ok = 1;
+    long long spins = 0;
+    while (ld_acquire_u64(p) < target) {
+      if (++spins > kSpinLimit) {
+        set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+        ok = 0;
+        break;
+      }
+      __nanosleep(32);
+    }
+    s_ok = ok;
+  }
+  __syncthreads();
+  return s_ok != 0;
+}
+// All of this CTA's writes of the item are done: count the item.
+__device__ void signal_count(unsigned long long* p) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(p, 1ull);
+  }
+}
+
+// The item sequence of one launch.
+struct StackSeq {
+  int L, nR, nGU, nD, nC, per_stage, n_stages;
+  int gpi, grp_g;  // gate/up: row groups per item, items per tile
+  int dpi, grp_d;  // down: row groups per warp (8 dpi per item), items per tile
+  bool overlap;
+  enum { kR = 0, kQ = 1, kGU = 2, kD = 3, kC = 4 };
+  static constexpr int kLag = 2;  // stages between an item kind and the kind it waits for (overlapped order)
+  // item i -> (kind, layer, index within the layer's items of that kind); layer < 0 or >= L: none
+  __device__ void item(long long i, int& kind, int& l, int& idx) const {
+    const int s = (int)(i / per_stage);
+    int j = (int)(i % per_stage);
+    if (j < nR) { kind = kR; idx = j; l = s; return; }
+    j -= nR;
+    if (j < 1) { kind = kQ; idx = 0; l = overlap ? s - kLag : s; return; }
+    j -= 1;
+    if (j < nGU) { kind = kGU; idx = j; l = overlap ? s - 2 * kLag : s; return; }
+    j -= nGU;
+    if (j < nD) { kind = kD; idx = j; l = overlap ? s - 3 * kLag : s; return; }
+    j -= nD;
+    kind = kC; idx = j; l = overlap ? s - 4 * kLag : s;
+  }
+  __device__ long long count() const { return (long long)n_stages * per_stage; }
+};
+
+// Do the layers share no buffer except a layer's residual with its own out?
+// (x, residual, out of every layer against out of every other layer.)
+__device__ bool stack_disjoint(const DecodeArgs& a, int L) {
+  __shared__ int s_clash;
+  if (threadIdx.x == 0) s_clash = 0;
+  __syncthreads();
+  const size_t bytes = (size_t)a.T * a.H * sizeof(float);
+  auto hit = [&](const void* p, const void* q) {
+    const char* x = static_cast<const char*>(p);
+    const char* o = static_cast<const char*>(q);
+    return x && o && x < o + bytes && o < x + bytes;
+  };
+  int clash = 0;
+  for (int pq = threadIdx.x; pq < L * L; pq += blockDim.x) {
+    const int i = pq / L, j = pq % L;
+    if (i == j) continue;
+    const moe_layer_ptrs li = a.layers[i], lj = a.layers[j];
+    if (hit(li.out, lj.x) || hit(li.out, lj.residual) || hit(li.out, lj.out)) clash = 1;
+  }
+  if (clash) atomicOr(&s_clash, 1);
+  __syncthreads();
+  return s_clash == 0;
+}
+
+// L2 prefetch of the weights item i will read (when already known)
+template <int FMT>
+__device__ void stack_prefetch(const Ctx<FMT>& c, const StackSeq& q, long long i, unsigned long long ep1) {
+  if (i >= q.count()) return;
+  const DecodeArgs& a = c.a;
+  int kind, l, idx;
+  q.item(i, kind, l, idx);
+  if (l < 0 || l >= q.L) return;
+  const LayerView lv = layer_view(a, l);
+  if (kind == StackSeq::kR) {
+    const int e0 = idx * kRouterRows, n = min(kRouterRows, c.E - e0);
+    if (n > 0) prefetch_l2(lv.w_router + (size_t)e0 * c.H, (uint32_t)((size_t)n * c.H * 4));
+    return;
+  }
+  if (kind != StackSeq::kGU && kind != StackSeq::kD) return;
+  if (ld_acquire_u64(stk_cnt(a, l, 1)) < ep1) return;  // routing not published yet
+  const Route Rg = stk_route(a, l);
+  const int per = kind == StackSeq::kGU ? q.grp_g : q.grp_d;
+  const int ti = idx / per;
+  const int nt = __ldcg(Rg.n_tiles);
+  const Tile tl = ld_tile(Rg.tiles + ti);
+  const moe_expert_ptrs ep = ld_ptrs(reinterpret_cast<const moe_expert_ptrs*>(stk_layer(a, l) + a.sp.tptr) + ti);
+  if (ti >= nt || tl.flag) return;
+  if (kind == StackSeq::kGU) {
+    const int rg0 = (idx % per) * q.gpi, nrg = min(q.gpi, c.nRG - rg0);
+    const size_t off = (size_t)rg0 * c.gu_run;
+    prefetch_l2(static_cast<const uint8_t*>(ep.gate) + off, (uint32_t)(nrg * c.gu_run));
+    prefetch_l2(static_cast<const uint8_t*>(ep.up) + off, (uint32_t)(nrg * c.gu_run));
+  } else {
+    const int rg0 = (idx % per) * kDownRG * q.dpi, nrg = min(kDownRG * q.dpi, c.nRGH - rg0);
+    prefetch_l2(static_cast<const uint8_t*>(ep.down) + (size_t)rg0 * c.dn_rg_bytes,
+                (uint32_t)((size_t)nrg * c.dn_rg_bytes));
+  }
+}
+
+// R: router rows [8 idx, 8 idx + 8) of layer l, one warp per row
+template <int FMT>
+__device__ void stack_router_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx) {
+  const int T = c.T, H = c.H, E = c.E, lane = c.lane, H4 = H / 4;
+  float* logits = reinterpret_cast<float*>(stk_layer(c.a, l) + c.a.sp.logits);
+  const int e = idx * kRouterRows + c.warp;
+  if (e >= E) return;
+  const float4* wr = reinterpret_cast<const float4*>(lv.w_router + (size_t)e * H);
+  const float4* xr = reinterpret_cast<const float4*>(lv.x);
+  float acc[16];
+#pragma unroll
+  for (int t = 0; t < 16; ++t) acc[t] = 0.0f;
+  // 8 chunks of the row in flight at a time (chunks past the row end read as zero)
+  const float4 z4 = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int h0 = lane; h0 < H4; h0 += 32 * 8) {
+    float4 wv[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) wv[u] = h0 + 32 * u < H4 ? __ldg(wr + h0 + 32 * u) : z4;
+#pragma unroll
+    for (int t = 0; t < 16; ++t)
+      if (t < T) {
+        float4 xv[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)  // x may be a previous layer's output
+          xv[u] = h0 + 32 * u < H4 ? __ldcg(xr + (size_t)t * H4 + h0 + 32 * u) : z4;
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          acc[t] = fmaf(wv[u].x, xv[u].x, acc[t]);
+          acc[t] = fmaf(wv[u].y, xv[u].y, acc[t]);
+          acc[t] = fmaf(wv[u].z, xv[u].z, acc[t]);
+          acc[t] = fmaf(wv[u].w, xv[u].w, acc[t]);
+        }
+      }
+  }
+  const float be = lv.bias ? __ldg(lv.bias + e) : 0.0f;
+#pragma unroll
+  for (int t = 0; t < 16; ++t) {
+    if (t < T) {
+      float v = acc[t];
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+      if (lane == 0) logits[(size_t)t * E + e] = v + be;
+    }
+  }
+}
+
+// Q: q8_K of x_l, then top-k, bucketing and tile plan, published to route_l
+template <int FMT>
+__device__ void stack_routing_item(Ctx<FMT>& c, const LayerView& lv, int l, bool last) {
+  const DecodeArgs& a = c.a;
+  uint8_t* lb = stk_layer(a, l);
+  int8_t* xq = reinterpret_cast<int8_t*>(lb + a.sp.xq);
+  float* xd = reinterpret_cast<float*>(lb + a.sp.xd);
+  int16_t* xbs = reinterpret_cast<int16_t*>(lb + a.sp.xbs);
+  for (int qb = c.warp; qb < c.T * c.nbH; qb += kDecWarps) {
+    const float4* src = reinterpret_cast<const float4*>(lv.x + (size_t)qb * 256 + 8 * c.lane);
+    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    q8k_block_warp(v, c.lane, xq + (size_t)qb * 256, xd + qb, xbs + (size_t)qb * 16);
+  }
+  const Route R = c.route(0);
+  routing_phase(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R, false, last, true);
+  __syncthreads();
+  const int4* src = reinterpret_cast<const int4*>(c.sm.rbase);
+  int4* dst = reinterpret_cast<int4*>(lb + a.sp.route);
+  for (size_t i = c.tid; i < c.sm.rstride / 16; i += kDecThreads) dst[i] = src[i];
+  // each tile's weight pointers beside the tiles: a consumer reads tile and pointers in one round trip
+  moe_expert_ptrs* tp = reinterpret_cast<moe_expert_ptrs*>(lb + a.sp.tptr);
+  for (int t = c.tid; t < *R.n_tiles; t += kDecThreads) tp[t] = lv.table[R.tiles[t].expert];
+}
+
+
+// GU: (tile idx / grp_g, row groups gpi (idx % grp_g) ..) of gate and up;
+// h = silu(G) * U.  The 8 warps take the (row group, super-block) pairs in
+// turn.  staged_x: the layer whose q8_K(x) is in shared memory (-1: none).
+template <int FMT>
+__device__ void stack_gateup_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx, int gpi, int grp_g,
+                                  int& staged_x) {
+  using F = Fmt<FMT>;
+  const DecodeArgs& a = c.a;
+  const int T = c.T, H = c.H, I = c.I, nbH = c.nbH, lane = c.lane, warp = c.warp, tid = c.tid;
+  Smem& sm = c.sm;
+  uint8_t* lb = stk_layer(a, l);
+  const Route Rg = stk_route(a, l);
+  const int ti = idx / grp_g, rg0 = (idx % grp_g) * gpi;
+  const int nrg = min(gpi, c.nRG - rg0);
+  // tile count, tile and its weight pointers: independent loads, one round trip
+  const int nt = __ldcg(Rg.n_tiles);
+  const Tile tl = ld_tile(Rg.tiles + ti);
+  const moe_expert_ptrs ep = ld_ptrs(reinterpret_cast<const moe_expert_ptrs*>(lb + a.sp.tptr) + ti);
+  if (ti >= nt || tl.flag) return;
+  const uint8_t* gbase = static_cast<const uint8_t*>(ep.gate) + (size_t)rg0 * c.gu_run;
+  const uint8_t* ubase = static_cast<const uint8_t*>(ep.up) + (size_t)rg0 * c.gu_run;
+  const int npair = nrg * nbH;  // (row group, super-block) pairs; pair p = rgl * nbH + b
+  // this warp's first pair is in flight while x is staged
+  SbRegs<FMT> sg, su;
+  if (warp < npair) {
+    load_sb<FMT>(gbase + (size_t)warp * F::kSlabBytes, lane, sg);
+    load_sb<FMT>(ubase + (size_t)warp * F::kSlabBytes, lane, su);
+  }
+  if (staged_x != l) {
+    const int8_t* xq = reinterpret_cast<const int8_t*>(lb + a.sp.xq);
+    const int16_t* xbs = reinterpret_cast<const int16_t*>(lb + a.sp.xbs);
+    const float* xd = reinterpret_cast<const float*>(lb + a.sp.xd);
+    for (int i = tid; i < T * H / 16; i += kDecThreads)
+      reinterpret_cast<int4*>(sm.xq)[i] = __ldcg(reinterpret_cast<const int4*>(xq) + i);
+    for (int i = tid; i < T * H / 128; i += kDecThreads)
+      reinterpret_cast<int4*>(sm.xbs)[i] = __ldcg(reinterpret_cast<const int4*>(xbs) + i);
+    for (int i = tid; i < T * nbH; i += kDecThreads) sm.xd[i] = __ldcg(xd + i);
+    staged_x = l;
+  }
+  for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = __ldcg(Rg.tok + tl.start + t) * H;
+  // per-warp accumulators: [row group][gate, up][T][32]
+  float* accw = sm.red + (size_t)warp * gpi * 2 * T * 32;
+  for (int i = lane; i < gpi * 2 * T * 32; i += 32) accw[i] = 0.0f;
+  __syncthreads();
+  for (int p = warp; p < npair; p += kDecWarps) {
+    // slabs of consecutive row groups are consecutive: pair p's slab is p slabs from the base
+    if (p != warp) {
+      load_sb<FMT>(gbase + (size_t)p * F::kSlabBytes, lane, sg);
+      load_sb<FMT>(ubase + (size_t)p * F::kSlabBytes, lane, su);
+    }
+    const int rgl = p / nbH, b = p % nbH;
+    float* acc = accw + (size_t)rgl * 2 * T * 32;
+    sb_accum<FMT>(sg, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc, lane);
+    sb_accum<FMT>(su, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc + T * 32, lane);
+  }
+  __syncthreads();
+  float* h = reinterpret_cast<float*>(lb + a.sp.h);
+  for (int i = tid; i < nrg * tl.count * 32; i += kDecThreads) {
+    const int r = i & 31, t = (i >> 5) % tl.count, rgl = (i >> 5) / tl.count;
+    float Gv = 0.0f, Uv = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float* acc = sm.red + ((size_t)w * gpi + rgl) * 2 * T * 32;
+      Gv += acc[t * 32 + r];
+      Uv += acc[(T + t) * 32 + r];
+    }
+    h[(size_t)(tl.start + t) * I + (rg0 + rgl) * 32 + r] = Gv / (1.0f + expf(-Gv)) * Uv;
+  }
+}
+
+// D: (tile idx / grp_d, 8 dpi row groups) of down on q8_K(h); warp w owns row
+// groups w, w + 8, .. of the item; y by slot
+template <int FMT>
+__device__ void stack_down_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx, int dpi, int grp_d) {
+  using F = Fmt<FMT>;
+  const DecodeArgs& a = c.a;
+  const int T = c.T, H = c.H, I = c.I, nbI = c.nbI, lane = c.lane, warp = c.warp, tid = c.tid;
+  Smem& sm = c.sm;
+  uint8_t* lb = stk_layer(a, l);
+  const Route Rg = stk_route(a, l);
+  const int ti = idx / grp_d, rgi = (idx % grp_d) * kDownRG * dpi;
+  const int nt = __ldcg(Rg.n_tiles);
+  const Tile tl = ld_tile(Rg.tiles + ti);
+  const void* dn = reinterpret_cast<const void*>(
+      __ldcg(reinterpret_cast<const unsigned long long*>(lb + a.sp.tptr) + 3 * ti + 2));
+  if (ti >= nt || tl.flag) return;
+  const uint8_t* dbase = static_cast<const uint8_t*>(dn);
+  SbRegs<FMT> sd;
+  if (rgi + warp < c.nRGH) load_sb<FMT>(dbase + (size_t)(rgi + warp) * c.dn_rg_bytes, lane, sd);  // in flight
+  const float* h = reinterpret_cast<const float*>(lb + a.sp.h);
+  for (int task = warp; task < tl.count * nbI; task += kDecWarps) {
+    const int t = task / nbI, blk = task % nbI;
+    const float4* src = reinterpret_cast<const float4*>(h + (size_t)(tl.start + t) * I + blk * 256 + 8 * lane);
+    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    q8k_block_warp(v, lane, sm.hq + (size_t)t * I + blk * 256, sm.hd + t * nbI + blk,
+                   sm.hbs + (size_t)t * (I / 16) + blk * 16);
+  }
+  for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = t * I;
+  float* accw = sm.red + (size_t)warp * dpi * T * 32;  // [dpi][T][32]
+  for (int i = lane; i < dpi * T * 32; i += 32) accw[i] = 0.0f;
+  __syncthreads();
+  float* y = reinterpret_cast<float*>(lb + a.sp.y);
+  for (int j = 0; j < dpi; ++j) {
+    const int rg = rgi + j * kDownRG + warp;
+    if (rg >= c.nRGH) break;
+    const uint8_t* rbase = dbase + (size_t)rg * c.dn_rg_bytes;
+    float* acc = accw + (size_t)j * T * 32;
+    for (int b = 0; b < nbI; ++b) {
+      if (b > 0 || j > 0) load_sb<FMT>(rbase + (size_t)b * F::kSlabBytes, lane, sd);
+      sb_accum<FMT>(sd, sm.hq, sm.hbs, sm.hd, sm.aoff, b, tl.count, acc, lane);
+    }
+    __syncwarp();
+    for (int t = 0; t < tl.count; ++t)
+      y[(size_t)__ldcg(Rg.slot + tl.start + t) * H + rg * 32 + lane] = acc[t * 32 + lane];
+  }
+}
+
+// C: float4 elements [1024 idx, 1024 idx + 1024) of out_l
+template <int FMT>
+__device__ void stack_combine_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx) {
+  const DecodeArgs& a = c.a;
+  const int T = c.T, H4 = c.H / 4, k = c.k, S = c.S;
+  uint8_t* lb = stk_layer(a, l);
+  const Route Rg = stk_route(a, l);
+  float* s_g = c.sm.red;                                     // gates [T*k]
+  float* s_ok = c.sm.red + T * k;                            // presence [T*k + S]
+  for (int i = c.tid; i < T * k; i += kDecThreads) s_g[i] = __ldcg(Rg.gates + i);
+  for (int i = c.tid; i < T * k + S; i += kDecThreads) s_ok[i] = (float)__ldcg(Rg.ok + i);
+  __syncthreads();
+  const float4* y4 = reinterpret_cast<const float4*>(lb + a.sp.y);
+  const int end = min(T * H4, (idx + 1) * kCombineVec);
+  for (int e = idx * kCombineVec + c.tid; e < end; e += kDecThreads) {
+    const int t = e / H4, cc = e % H4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < k; ++s) {
+      if (s_ok[t * k + s] == 0.0f) continue;  // expert not present ("not mine"): contributes nothing
+      const float g = s_g[t * k + s];
+      const float4 v = __ldcg(y4 + (size_t)(t * k + s) * H4 + cc);
+      acc.x = fmaf(g, v.x, acc.x);
+      acc.y = fmaf(g, v.y, acc.y);
+      acc.z = fmaf(g, v.z, acc.z);
+      acc.w = fmaf(g, v.w, acc.w);
+    }
+    for (int sh = 0; sh < S; ++sh) {
+      if (s_ok[T * k + sh] == 0.0f) continue;
+      const float4 v = __ldcg(y4 + (size_t)(T * k + sh * T + t) * H4 + cc);
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    if (lv.residual) {
+      const float4 r = __ldcg(reinterpret_cast<const float4*>(lv.residual) + e);
+      acc.x += r.x;
+      acc.y += r.y;
+      acc.z += r.z;
+      acc.w += r.w;
+    }
+    reinterpret_cast<float4*>(lv.out)[e] = acc;
+  }
+}
+
+template <int FMT>
+__global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ DecodeArgs a) {
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  const long long t_launch = clock64();
+  Ctx<FMT> c(a, smem_raw);
+  StackSeq q;
+  q.L = a.n_layers;
+  q.overlap = stack_disjoint(a, q.L);
+  q.nR = (c.E + kRouterRows - 1) / kRouterRows;
+  // bigger items when a row group is little work (short K): fewer waits and
+  // signals per byte; bounded by the per-warp accumulators in shared memory
+  const int Tm = c.T > 16 ? c.T : 16;
+  q.gpi = max(1, min(2 * kDecWarps / c.nbH, Tm / c.T));
+  q.grp_g = (c.nRG + q.gpi - 1) / q.gpi;
+  q.nGU = c.P * q.grp_g;
+  q.dpi = (c.nbI <= 2 && 2 * c.T <= 2 * Tm) ? 2 : 1;
+  q.grp_d = (c.nRGH + kDownRG * q.dpi - 1) / (kDownRG * q.dpi);
+  q.nD = c.P * q.grp_d;
+  q.nC = (c.T * (c.H / 4) + kCombineVec - 1) / kCombineVec;
+  q.per_stage = q.nR + 1 + q.nGU + q.nD + q.nC;
+  q.n_stages = q.overlap ? q.L + 4 * StackSeq::kLag : q.L;
+  // this launch's counters start at zero (one grid barrier), so a launch
+  // depends on no state a previous launch left behind
+  {
+    unsigned long long* cnt = stk_cnt(a, 0, 0);
+    const size_t n = (size_t)q.L * a.sp.n_cnt;
+    for (size_t j = (size_t)blockIdx.x * kDecThreads + c.tid; j < n; j += (size_t)gridDim.x * kDecThreads) cnt[j] = 0;
+    if (blockIdx.x == 0 && c.tid < 15 && a.phase_ns) a.phase_ns[c.tid] = 0;
+  }
+  if (!grid_barrier(a.bar, a.status)) return;
+  // per item kind: cycles of work, cycles waiting, items (summed over CTAs at the end)
+  long long t_work[5] = {0, 0, 0, 0, 0}, t_wait[5] = {0, 0, 0, 0, 0};
+  const long long t_ready = clock64();
+  long long t_prev = t_ready, t_gaps = 0, t_head = -1, n_items_done = 0;
+  const unsigned long long ep1 = 1;  // counter targets are counts x ep1
+  if (blockIdx.x == 0 && c.tid == 0 && a.phase_ns) a.phase_ns[15] = q.overlap ? 2 : 1;  // which order ran
+  const long long n_items = q.count();
+  const int G = gridDim.x;
+  int staged_x = -1;
+  if (c.tid == 32) stack_prefetch(c, q, blockIdx.x, ep1);
+  for (long long i = blockIdx.x; i < n_items; i += G) {
+    int kind, l, idx;
+    q.item(i, kind, l, idx);
+    if (l < 0 || l >= q.L) continue;
+    const LayerView lv = layer_view(a, l);
+    bool ok = true;
+    auto next_pf = [&]() { stack_prefetch(c, q, i + G, ep1); };
+    const long long t0 = clock64();
+    if (t_head < 0) t_head = t0 - t_ready;
+    else t_gaps += t0 - t_prev;
+    long long t1 = t0;  // end of the wait
+    if (kind == StackSeq::kR) {
+      if (!q.overlap && l > 0) ok = wait_count(stk_cnt(a, l - 1, 3), ep1 * q.nC, a.status, next_pf);
+      else if (c.tid == 32) next_pf();
+      t1 = clock64();
+      if (ok) {
+        stack_router_item(c, lv, l, idx);
+        signal_count(stk_cnt(a, l, 0));
+      }
+    } else if (kind == StackSeq::kQ) {
+      ok = wait_count(stk_cnt(a, l, 0), ep1 * q.nR, a.status, next_pf);
+      t1 = clock64();
+      if (ok) {
+        stack_routing_item(c, lv, l, l == q.L - 1);
+        signal_count(stk_cnt(a, l, 1));
+      }
+    } else if (kind == StackSeq::kGU) {
+      ok = wait_count(stk_cnt(a, l, 1), ep1, a.status, next_pf);
+      t1 = clock64();
+      if (ok) {
+        stack_gateup_item(c, lv, l, idx, q.gpi, q.grp_g, staged_x);
+        signal_count(stk_cnt(a, l, kStackCnt + idx / q.grp_g));
+      }
+    } else if (kind == StackSeq::kD) {
+      ok = wait_count(stk_cnt(a, l, kStackCnt + idx / q.grp_d), ep1 * q.grp_g, a.status, next_pf);
+      t1 = clock64();
+      if (ok) {
+        stack_down_item(c, lv, l, idx, q.dpi, q.grp_d);
+        signal_count(stk_cnt(a, l, 2));
+      }
+    } else {
+      ok = wait_count(stk_cnt(a, l, 2), ep1 * q.nD, a.status, next_pf);
+      t1 = clock64();
+      if (ok) {
+        stack_combine_item(c, lv, l, idx);
+        signal_count(stk_cnt(a, l, 3));
+      }
+    }
+    if (!ok) return;  // the status word says why; CTAs waiting on this one run out too
+    t_wait[kind] += t1 - t0;
+    t_prev = clock64();
+    t_work[kind] += t_prev - t1;
+    ++n_items_done;
+  }
+  // totals over all CTAs (SM cycles): [0..4] work per item kind, [5..9] wait
+  // per item kind, [10] prologue (counter reset, order check, barrier),
+  // [11] before the first item, [12] between items, [13] items done
+  if (c.tid == 0 && a.phase_ns) {
+    for (int k = 0; k < 5; ++k) {
+      atomicAdd(a.phase_ns + k, (unsigned long long)t_work[k]);
+      atomicAdd(a.phase_ns + 5 + k, (unsigned long long)t_wait[k]);
+    }
+    atomicAdd(a.phase_ns + 10, (unsigned long long)(t_ready - t_launch));
+    atomicAdd(a.phase_ns + 11, (unsigned long long)(t_head < 0 ? 0 : t_head));
+    atomicAdd(a.phase_ns + 12, (unsigned long long)t_gaps);
+    atomicAdd(a.phase_ns + 13, (unsigned long long)n_items_done);
+  }
+}
+
+template <int FMT>
+cudaError_t launch_stack_t(const DecodeArgs& a, cudaStream_t s) {
+  const size_t smem = decode_smem(a.T, a.H, a.I, a.E, a.k, a.S, nullptr, nullptr);
+  auto kern = decode_stack_kernel<FMT>;
+  static size_t opted = 0;  // per instantiation; the opt-in only grows
+  if (smem > opted) {
+    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (err != cudaSuccess) return err;
+    opted = smem;
+  }
+  int per_sm = 0;
+  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
+  if (err != cudaSuccess) return err;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  const int grid = num_sms() * std::min(per_sm, 2);
+  DecodeArgs args = a;
+  void* params[] = {&args};
+  note_launch();
+  return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3(grid), dim3(kDecThreads), params,
+                                     smem, s);
+}
+
 template <int FMT>
 cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
   const size_t smem = decode_smem(a.T, a.H, a.I, a.E, a.k, a.S, nullptr, nullptr);
@@ -864,6 +1406,38 @@ size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S) {
 
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
   return a.fmt == kQ4K ? launch_decode_t<kQ4K>(a, s) : launch_decode_t<kQ2K>(a, s);
+}
+
+cudaError_t launch_decode_stack(const DecodeArgs& a, cudaStream_t s) {
+  return a.fmt == kQ4K ? launch_stack_t<kQ4K>(a, s) : launch_stack_t<kQ2K>(a, s);
+}
+
+StackPlan stack_plan(const moe_layer_desc& d, int n_layers) {
+  StackPlan p{};
+  const size_t T = (size_t)d.T_max, H = (size_t)d.H, I = (size_t)d.I, E = (size_t)d.E;
+  const size_t P = T * (size_t)(d.top_k + d.n_shared);
+  auto a256 = [](size_t v) { return (v + 255) / 256 * 256; };
+  p.n_layers = n_layers;
+  p.n_cnt = kStackCnt + (int)P;
+  p.cnt = 0;
+  p.layer0 = a256(p.cnt + (size_t)n_layers * p.n_cnt * 8);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = a256(off + bytes);
+    return at;
+  };
+  p.logits = take(T * E * 4);
+  p.xq = take(T * H);
+  p.xd = take(T * (H / 256) * 4);
+  p.xbs = take(T * (H / 16) * 2);
+  p.route = take(route_bytes((int)T, d.top_k, d.n_shared));
+  p.tptr = take(P * sizeof(moe_expert_ptrs));
+  p.h = take(P * I * 4);
+  p.y = take(P * H * 4);
+  p.layer_bytes = off;
+  p.total = p.layer0 + (size_t)n_layers * p.layer_bytes;
+  return p;
 }
 
 }  // namespace moe

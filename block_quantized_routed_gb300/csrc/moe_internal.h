@@ -96,6 +96,20 @@ void note_launch();
 // remembers a failed CUDA call of this host thread (moe_last_cuda_error); returns e
 cudaError_t record_error(cudaError_t e);
 
+// Workspace extension of a decode stack (moe_stack_forward): per-layer
+// buffers and dependency counters, placed after a layer workspace.  Offsets
+// are relative to the extension's base; a layer's block starts at
+// layer0 + l * layer_bytes.
+struct StackPlan {
+  size_t cnt;          // uint64 [L][kStackCnt + P] counters, zeroed by each launch
+  size_t layer0, layer_bytes;
+  size_t logits, xq, xd, xbs, route, tptr, h, y;  // inside a layer block (tptr: tile weight pointers)
+  int n_layers, n_cnt;                      // n_cnt = kStackCnt + P counters per layer
+  size_t total;
+};
+constexpr int kStackCnt = 4;  // router items, routing, down items, combine items (then one per tile)
+StackPlan stack_plan(const moe_layer_desc& d, int n_layers);
+
 // Single-launch decode layer (cooperative kernel); see moe_decode.cu.
 struct DecodeArgs {
   int fmt, H, I, E, k, S, route, T;
@@ -133,7 +147,11 @@ struct DecodeArgs {
   int pipeline_ok;                // the workspace holds the extra buffers of the pipelined schedule
   uint8_t* route_pub;             // 4 routing states published by the routing CTA (pipelined schedule)
   unsigned long long* route_flag; // monotonic count of published routing states
+  uint8_t* stk;                   // stack extension (decode_stack_kernel), or NULL
+  StackPlan sp;
 };
+cudaError_t launch_decode_stack(const DecodeArgs& a, cudaStream_t s);
+
 size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S);
 size_t decode_route_bytes(int T, int k, int S);  // one routing state of the decode kernel
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);

@@ -224,20 +224,31 @@ typedef struct {
   float* gates_out;             /* [T, k] or NULL                             */
 } moe_layer_ptrs;
 
-/* A stack of n_layers MoE layers of the same shape in ONE launch, with the
- * results of running them one after the other: a layer's x may point at the
- * previous layer's out (a decode step through the stack).  When no layer's x
- * overlaps the outputs of the three layers before it (independent inputs),
- * the kernel pipelines neighbouring layers (one grid barrier per layer
- * instead of four); otherwise every layer runs after the previous one has
- * finished.  Both schedules give the same results.  `layers` is a DEVICE array of n_layers records.  Only the
- * single-launch decode shapes are accepted: T <= 16, T*top_k <= 256, and
- * the layer's staging fits in shared memory; otherwise MOE_ERR_UNSUPPORTED
- * (run moe_layer_forward per layer instead).  ws: one workspace of
- * moe_layer_workspace_size(desc) bytes, shared by the layers (its
- * intermediates hold the last layer's).  While layer l computes its down
- * projection, the next layer's router rows and shared-expert gate/up weights
- * are prefetched into L2.  Source: Strata summary (the per-token layer loop
+/* Workspace bytes moe_stack_forward needs for n_layers layers of `desc`
+ * (0 if desc is invalid or n_layers < 1): a moe_layer_forward workspace
+ * followed by per-layer buffers (logits, q8_K(x), routing, h, y) and the
+ * stack's dependency counters.  Grows linearly with n_layers and T_max. */
+size_t moe_stack_workspace_size(const moe_layer_desc* desc, int32_t n_layers);
+
+/* A stack of n_layers MoE layers of the same shape in ONE cooperative
+ * launch, with the results of running them one after the other: a layer's x
+ * may point at the previous layer's out (a decode step through the stack).
+ * The stack runs as a sequence of small work items (router rows, routing,
+ * gate/up row groups, down row groups, combine chunks) handed out
+ * round-robin, ordered by per-layer dependency counters instead of grid
+ * barriers.  When no layer's out overlaps another layer's x, residual or
+ * out (independent inputs), neighbouring layers overlap; otherwise each
+ * layer starts after the previous one has finished.  Both orders give the
+ * same results.  `layers` is a DEVICE array of n_layers records.  Only the
+ * single-launch decode shapes are accepted: T <= 16, T*top_k <= 256, and the
+ * layer's staging fits in shared memory; otherwise MOE_ERR_UNSUPPORTED (run
+ * moe_layer_forward per layer instead).  ws: moe_stack_workspace_size(desc,
+ * n_layers) bytes, 256-byte aligned, its 16-byte status block zero before
+ * the first call (e.g. a zero-filled allocation); ids/gates/counts/offsets/
+ * perm in it hold the last layer's routing.  phase_ns[15] reports the order
+ * that ran: 2 overlapped, 1 one layer after the other.  Sources: Pulsar
+ * README, "How the streaming works" (the next layer's experts are fetched
+ * while the current one computes); Strata summary (the per-token layer loop
  * run as captured, replayed work with no allocation on the token path). */
 int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
                       void* ws, size_t ws_bytes, void* stream);

@@ -139,3 +139,15 @@ def test_prefill_parity_cases_take_the_tensor_path(lib):
                                          (0, 1, 4096, 1024, 512, 10, 1, 8192)]:
         d = desc(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
         assert moe.moe_layer_path(d, T) == moe.PATH_TENSOR_PREFILL
+
+
+def test_stack_workspace_size(lib):
+    d = desc(T_max=1)
+    one = moe.moe_stack_workspace_size(d, 1)
+    forty = moe.moe_stack_workspace_size(d, 40)
+    assert one > moe.moe_layer_workspace_size(d)
+    per_layer = (forty - one) / 39                           # per-layer buffers and counters
+    assert 80 * 1024 < per_layer < 1 << 20                   # logits, x codes, routing, h [9, 512], y [9, 2048]
+    assert moe.moe_stack_workspace_size(desc(T_max=4), 40) > forty
+    assert moe.moe_stack_workspace_size(d, 0) == 0
+    assert moe.moe_stack_workspace_size(desc(H=300), 4) == 0

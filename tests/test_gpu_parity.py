@@ -329,7 +329,7 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
     rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
             for l in range(L)]
     desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
-    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.moe_stack_workspace_size(desc, L), dtype=torch.uint8, device="cuda")
     moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
     assert moe.moe_get_status(ws) == 0
     marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
@@ -360,7 +360,7 @@ def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
     rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
             for l in range(L)]
     desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
-    ws = torch.zeros(moe.moe_layer_workspace_size(desc), dtype=torch.uint8, device="cuda")
+    ws = torch.zeros(moe.moe_stack_workspace_size(desc, L), dtype=torch.uint8, device="cuda")
     for rep in range(2):
         moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
         assert moe.moe_get_status(ws) == 0
