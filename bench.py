@@ -436,13 +436,13 @@ def run_ours(args, wl, T):
                   "gate_up": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[0:8])},
                   "down": {n: round(float(v) / mhz, 1) for n, v in zip(names, st[8:16])}}
         st = np.zeros(16, np.int64)
-    if stacked and path == moe.PATH_DECODE_FUSED:
+    if stacked and st[15] in (3, 4):
         # per item kind of the stack kernel, summed over CTAs: work and wait cycles, items
         mhz = clock_info.get("sm_mhz") or 2070.0
         kinds = ["router", "routing", "gate_up", "down", "combine"]
         G_ = int(torch.cuda.get_device_properties(dev).multi_processor_count) * 2
         us = lambda v: round(float(v) / mhz, 1)
-        phases = {"schedule": "stack_items_" + ("overlapped" if st[15] == 2 else "chained"),
+        phases = {"schedule": "stack_items_" + ("overlapped" if st[15] == 3 else "chained"),
                   "cta_us_summed_over_ctas": {**{f"work_{n}": us(st[k_]) for k_, n in enumerate(kinds)},
                                               **{f"wait_{n}": us(st[5 + k_]) for k_, n in enumerate(kinds)},
                                               "prologue": us(st[10]), "before_first_item": us(st[11]),

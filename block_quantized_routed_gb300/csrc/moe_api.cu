@@ -130,6 +130,18 @@ int last_error() { return g_last_error; }
 
 void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
+// Gate/up and down items of one layer of the dataflow stack per SM (the same
+// item sizes as decode_stack_kernel chooses).
+double stack_items_per_sm(const moe_layer_desc& d, int T) {
+  const int nbH = d.H / 256, nbI = d.I / 256, nRG = d.I / 32, nRGH = d.H / 32;
+  const int Tm = T > 16 ? T : 16;
+  const int gpi = std::max(1, std::min(16 / nbH, Tm / T));
+  const int dpi = nbI <= 2 ? 2 : 1;
+  const double P = (double)T * (d.top_k + d.n_shared);
+  const double items = P * ((nRG + gpi - 1) / gpi) + P * ((nRGH + 8 * dpi - 1) / (8 * dpi));
+  return items / num_sms();
+}
+
 void trace_record(cudaStream_t s) {
   if (!g_trace_events || g_trace_next >= g_trace_n) return;
   cudaEvent_t ev = static_cast<cudaEvent_t>(g_trace_events[g_trace_next++]);
@@ -473,6 +485,58 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   if (ws_bytes < ext + sp.total) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
+  // Layers with many expert items per CTA (wide experts, long verify
+  // windows) run faster on the barrier-pipelined kernel, whose CTAs
+  // prefetch all of their items of a layer at once; small layers run as the
+  // dataflow of items.
+  if (stack_items_per_sm(*desc, T) > 2.0) {
+    DecodeArgs d{};
+    d.fmt = desc->fmt;
+    d.H = H;
+    d.I = desc->I;
+    d.E = E;
+    d.k = k;
+    d.S = S;
+    d.route = desc->route;
+    d.T = T;
+    for (int i = 0; i < 3; ++i) {
+      d.xq[i] = static_cast<int8_t*>(at(p.xq_b[i]));
+      d.xd[i] = static_cast<float*>(at(p.xd_b[i]));
+      d.xbs[i] = static_cast<int16_t*>(at(p.xbs_b[i]));
+    }
+    for (int i = 0; i < 2; ++i) {
+      d.logits[i] = static_cast<float*>(at(p.logits_b[i]));
+      d.h[i] = static_cast<float*>(at(p.h_b[i]));
+      d.y[i] = static_cast<float*>(at(p.y_b[i]));
+    }
+    d.pipeline_ok = p.pipeline ? 1 : 0;
+    d.route_pub = p.pipeline ? static_cast<uint8_t*>(at(p.route_pub)) : nullptr;
+    d.route_flag = p.pipeline ? static_cast<unsigned long long*>(at(p.route_flag)) : nullptr;
+    d.gap = static_cast<float*>(at(p.pub.gap));
+    d.ids = static_cast<int32_t*>(at(p.pub.ids));
+    d.gates = static_cast<float*>(at(p.pub.gates));
+    d.counts = static_cast<int32_t*>(at(p.pub.counts));
+    d.offsets = static_cast<int32_t*>(at(p.pub.offsets));
+    d.perm = static_cast<int32_t*>(at(p.pub.perm));
+    d.inv = static_cast<int32_t*>(at(p.pub.inv));
+    d.hq = static_cast<int8_t*>(at(p.pub.hq));
+    d.hd = static_cast<float*>(at(p.pub.hd));
+    d.hbs = static_cast<int16_t*>(at(p.pub.hbs));
+    d.bar = static_cast<unsigned long long*>(at(p.bar));
+    d.phase_ns = static_cast<unsigned long long*>(at(p.phase_ns));
+    d.status = static_cast<int*>(at(p.pub.status));
+    d.n_layers = n_layers;
+    d.layers = layers;
+    cudaStream_t s = as_stream(stream);
+    trace_record(s);
+    const cudaError_t err = record_error(launch_decode_fused(d, s));
+    trace_record(s);
+    if (err == cudaErrorCooperativeLaunchTooLarge) {
+      cudaGetLastError();
+      return MOE_ERR_UNSUPPORTED;
+    }
+    return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
   DecodeArgs d{};
   d.fmt = desc->fmt;
   d.H = H;

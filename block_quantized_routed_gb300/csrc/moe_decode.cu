@@ -1278,7 +1278,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
   const long long t_ready = clock64();
   long long t_prev = t_ready, t_gaps = 0, t_head = -1, n_items_done = 0;
   const unsigned long long ep1 = 1;  // counter targets are counts x ep1
-  if (blockIdx.x == 0 && c.tid == 0 && a.phase_ns) a.phase_ns[15] = q.overlap ? 2 : 1;  // which order ran
+  if (blockIdx.x == 0 && c.tid == 0 && a.phase_ns) a.phase_ns[15] = q.overlap ? 3 : 4;  // which order ran
   const long long n_items = q.count();
   const int G = gridDim.x;
   int staged_x = -1;

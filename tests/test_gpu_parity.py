@@ -333,7 +333,7 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
     moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
     assert moe.moe_get_status(ws) == 0
     marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
-    assert int(marker[15]) == 1          # chained layers run one after the other
+    assert int(marker[15]) == 4          # chained layers run one after the other (dataflow stack)
     for l in range(L):
         xin = xs[l].cpu().numpy()
         gids = ids[l].cpu().numpy()
@@ -365,7 +365,7 @@ def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
         moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
         assert moe.moe_get_status(ws) == 0
         marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
-        assert int(marker[15]) == 2
+        assert int(marker[15]) == 3      # dataflow stack, layers overlapped
         for l in range(L):
             gids = ids[l].cpu().numpy()
             rl, rids, _, rgap = oracle.route(xs_h[l], wrs[l], None, k, route)
@@ -373,6 +373,39 @@ def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
             ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xs_h[l],
                                                 residual=xs_h[l], forced_ids=gids)
             assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
+
+
+@pytest.mark.parametrize("chained", [False, True])
+def test_stack_forward_heavy_layers_pipelined_kernel(moe, chained):
+    """Layers with many expert items per SM (8 tokens, 1024-wide experts) run
+    on the barrier-pipelined kernel; every layer must match the oracle."""
+    # chained: each layer scales the activations up by orders of magnitude at this
+    # shape, so two layers (a third would overflow fp32 in the oracle as well)
+    fmt, route, H, I, E, k, S, T = FMT_Q4K, 0, 2048, 1024, 64, 8, 1, 8
+    L = 2 if chained else 3
+    ex = [_experts_host(fmt, E + S, H, I, seed=90 + l, layer=l) for l in range(L)]
+    tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
+    wrs = [synth.router_weight(E, H, 90, l) for l in range(L)]
+    xs_h = [synth.activations(T, H, 90, layer=l) for l in range(L)]
+    outs = [torch.full((T, H), float("nan"), dtype=torch.float32, device="cuda") for _ in range(L)]
+    xs = [dev(xs_h[0])] + (outs[:-1] if chained else [dev(x) for x in xs_h[1:]])
+    ids = [torch.empty((T, k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
+            for l in range(L)]
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    ws = torch.zeros(moe.moe_stack_workspace_size(desc, L), dtype=torch.uint8, device="cuda")
+    moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
+    assert moe.moe_get_status(ws) == 0
+    marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
+    assert int(marker[15]) == (1 if chained else 2)
+    for l in range(L):
+        xin = xs[l].cpu().numpy()
+        gids = ids[l].cpu().numpy()
+        rl, rids, _, rgap = oracle.route(xin, wrs[l], None, k, route)
+        routing_ok(gids, rids, rgap, rl)
+        ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xin, residual=xin,
+                                            forced_ids=gids)
+        assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
 
 
 def test_stack_forward_rejects_prefill_shapes(moe):
