@@ -839,14 +839,18 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
 // moe_stack_forward: the stack as one sequence of small work items, handed
 // out round-robin (item i to CTA i % G, each CTA in increasing order), with
 // per-layer counters instead of grid barriers.  Item kinds of layer l:
-//   R   8 router rows (one warp each)                          -> logits_l
-//   Q   q8_K of x_l, top-k, bucketing, tile plan               -> route_l
+//   R   8 router rows (one warp each), part of q8_K(x_l)       -> logits_l
+//   Q   top-k, bucketing, tile plan                            -> route_l
 //   GU  (tile, 32-row group) of gate and up, SwiGLU            -> h_l
 //   D   (tile, 8 row groups) of down, on q8_K(h) of the tile   -> y_l by slot
 //   C   a chunk of out_l = residual + sum gate * y (fixed order)
 // An item waits (bounded) for the counters of what it reads: Q for all R of
 // its layer, GU for Q, D for the GU items of its tile, C for all D; in a
 // chained stack the R items of layer l also wait for all C of layer l-1.
+// In a chained stack the CTA that finishes the last R item of a layer runs
+// its Q at once, and the one that finishes the last D item runs all of its C
+// (the Q and C items of the sequence are then empty): two fewer hand-offs
+// on the critical path of a layer.
 // Every item increments its counter, also when it has nothing to do (a
 // tile slot beyond the layer's tiles), so the targets are fixed counts; the
 // counters are zeroed at the start of the launch (one grid barrier).  Waits
@@ -922,6 +926,22 @@ __device__ void signal_count(unsigned long long* p) {
     __threadfence();
     atomicAdd(p, 1ull);
   }
+}
+
+// The same, and tells every thread whether this item was the one that
+// brought the counter to `target` (then the items counted before it are all
+// visible to this CTA).
+__device__ bool signal_last(unsigned long long* p, unsigned long long target) {
+  __shared__ int s_last;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned long long old = atomicAdd(p, 1ull);
+    __threadfence();
+    s_last = old + 1 == target;
+  }
+  __syncthreads();
+  return s_last != 0;
 }
 
 // The item sequence of one launch.
@@ -1009,10 +1029,21 @@ __device__ void stack_prefetch(const Ctx<FMT>& c, const StackSeq& q, long long i
 }
 
 // R: router rows [8 idx, 8 idx + 8) of layer l, one warp per row
+// (The router items also make the q8_K of x: block qb by warp qb % 8 of item
+// (qb / 8) % nR, so it is done when all router items of the layer are.)
 template <int FMT>
-__device__ void stack_router_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx) {
+__device__ void stack_router_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx, int nR) {
   const int T = c.T, H = c.H, E = c.E, lane = c.lane, H4 = H / 4;
-  float* logits = reinterpret_cast<float*>(stk_layer(c.a, l) + c.a.sp.logits);
+  uint8_t* lb = stk_layer(c.a, l);
+  for (int qb = idx * kRouterRows + c.warp; qb < T * c.nbH; qb += nR * kRouterRows) {
+    const float4* src = reinterpret_cast<const float4*>(lv.x + (size_t)qb * 256 + 8 * lane);
+    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    q8k_block_warp(v, lane, reinterpret_cast<int8_t*>(lb + c.a.sp.xq) + (size_t)qb * 256,
+                   reinterpret_cast<float*>(lb + c.a.sp.xd) + qb,
+                   reinterpret_cast<int16_t*>(lb + c.a.sp.xbs) + (size_t)qb * 16);
+  }
+  float* logits = reinterpret_cast<float*>(lb + c.a.sp.logits);
   const int e = idx * kRouterRows + c.warp;
   if (e >= E) return;
   const float4* wr = reinterpret_cast<const float4*>(lv.w_router + (size_t)e * H);
@@ -1054,22 +1085,93 @@ __device__ void stack_router_item(Ctx<FMT>& c, const LayerView& lv, int l, int i
   }
 }
 
-// Q: q8_K of x_l, then top-k, bucketing and tile plan, published to route_l
+// Routing of a stack layer without the expert-wide count and scan: with at
+// most 256 (token, slot) pairs, a pair's bucket position is the number of
+// pairs of smaller experts plus the earlier pairs of its own expert, and an
+// expert's tile index is the number of distinct smaller experts.  Same
+// result as routing_phase (tiles by expert, shared experts last), without
+// writing the layer's counts and offsets to global memory.
+template <int FMT>
+__device__ void routing_small(Ctx<FMT>& c, const LayerView& lv, const float* logits, const Route& R) {
+  const DecodeArgs& a = c.a;
+  const int T = c.T, E = c.E, k = c.k, S = c.S, tid = c.tid, TK = T * k;
+  int* first = reinterpret_cast<int*>(c.sm.red);  // [TK]: pair is its expert's first
+  for (int t = c.warp; t < T; t += kDecWarps)
+    warp_topk(logits + (size_t)t * E, E, k, a.route, c.lane, R.ids + t * k, R.gates + t * k, nullptr);
+  __syncthreads();
+  for (int p = tid; p < TK + S; p += kDecThreads) {
+    const int e = p < TK ? R.ids[p] : E + (p - TK);
+    R.ok[p] = lv.table[e].gate != nullptr ? 1 : 0;  // present ("mine")?
+  }
+  for (int p = tid; p < TK; p += kDecThreads) {
+    const int e = R.ids[p];
+    int f = 1;
+    for (int q = 0; q < p; ++q) f &= R.ids[q] != e;
+    first[p] = f;
+  }
+  __syncthreads();
+  for (int p = tid; p < TK; p += kDecThreads) {
+    const int e = R.ids[p];
+    int before = 0, same_before = 0, cnt = 0, tix = 0;
+    for (int q = 0; q < TK; ++q) {
+      const int f = R.ids[q];
+      before += f < e;
+      same_before += (f == e) & (q < p);
+      cnt += f == e;
+      tix += (f < e) & first[q];
+    }
+    const int pos = before + same_before;
+    R.tok[pos] = p / k;
+    R.slot[pos] = p;
+    if (first[p]) {
+      Tile tl;
+      tl.expert = e;
+      tl.start = before;
+      tl.count = cnt;
+      tl.flag = R.ok[p] ? 0 : 1;
+      R.tiles[tix] = tl;
+    }
+  }
+  __shared__ int s_distinct;
+  if (tid == 0) {
+    int n = 0;
+    for (int q = 0; q < TK; ++q) n += first[q];
+    s_distinct = n;
+  }
+  __syncthreads();
+  const int nr = s_distinct;
+  for (int i = tid; i < S * T; i += kDecThreads) {
+    const int sh = i / T, t = i % T, pos = TK + sh * T + t;
+    R.tok[pos] = t;
+    R.slot[pos] = pos;
+    if (t == 0) {
+      Tile tl;
+      tl.expert = E + sh;
+      tl.start = TK + sh * T;
+      tl.count = T;
+      tl.flag = R.ok[TK + sh] ? 0 : 1;
+      R.tiles[nr + sh] = tl;
+    }
+  }
+  if (tid == 0) *R.n_tiles = nr + S;
+  for (int p = tid; p < TK; p += kDecThreads) {
+    if (lv.ids_out) lv.ids_out[p] = R.ids[p];
+    if (lv.gates_out) lv.gates_out[p] = R.gates[p];
+  }
+  __syncthreads();
+}
+
+// Q: top-k, bucketing and tile plan of layer l, published to route_l
 template <int FMT>
 __device__ void stack_routing_item(Ctx<FMT>& c, const LayerView& lv, int l, bool last) {
   const DecodeArgs& a = c.a;
   uint8_t* lb = stk_layer(a, l);
-  int8_t* xq = reinterpret_cast<int8_t*>(lb + a.sp.xq);
-  float* xd = reinterpret_cast<float*>(lb + a.sp.xd);
-  int16_t* xbs = reinterpret_cast<int16_t*>(lb + a.sp.xbs);
-  for (int qb = c.warp; qb < c.T * c.nbH; qb += kDecWarps) {
-    const float4* src = reinterpret_cast<const float4*>(lv.x + (size_t)qb * 256 + 8 * c.lane);
-    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
-    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-    q8k_block_warp(v, c.lane, xq + (size_t)qb * 256, xd + qb, xbs + (size_t)qb * 16);
-  }
   const Route R = c.route(0);
-  routing_phase(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R, false, last, true);
+  // the last layer also fills the workspace's counts/offsets/perm: the general routine
+  if (last || c.T * c.k > kDecThreads)
+    routing_phase(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R, false, last, true);
+  else
+    routing_small(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R);
   __syncthreads();
   const int4* src = reinterpret_cast<const int4*>(c.sm.rbase);
   int4* dst = reinterpret_cast<int4*>(lb + a.sp.route);
@@ -1299,15 +1401,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       else if (c.tid == 32) next_pf();
       t1 = clock64();
       if (ok) {
-        stack_router_item(c, lv, l, idx);
-        signal_count(stk_cnt(a, l, 0));
+        stack_router_item(c, lv, l, idx, q.nR);
+        // layer by layer: the CTA of the last router item routes the layer at once
+        if (q.overlap) {
+          signal_count(stk_cnt(a, l, 0));
+        } else if (signal_last(stk_cnt(a, l, 0), ep1 * q.nR)) {
+          stack_routing_item(c, lv, l, l == q.L - 1);
+          signal_count(stk_cnt(a, l, 1));
+        }
       }
     } else if (kind == StackSeq::kQ) {
-      ok = wait_count(stk_cnt(a, l, 0), ep1 * q.nR, a.status, next_pf);
-      t1 = clock64();
-      if (ok) {
-        stack_routing_item(c, lv, l, l == q.L - 1);
-        signal_count(stk_cnt(a, l, 1));
+      if (q.overlap) {
+        ok = wait_count(stk_cnt(a, l, 0), ep1 * q.nR, a.status, next_pf);
+        t1 = clock64();
+        if (ok) {
+          stack_routing_item(c, lv, l, l == q.L - 1);
+          signal_count(stk_cnt(a, l, 1));
+        }
       }
     } else if (kind == StackSeq::kGU) {
       ok = wait_count(stk_cnt(a, l, 1), ep1, a.status, next_pf);
@@ -1321,9 +1431,21 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       t1 = clock64();
       if (ok) {
         stack_down_item(c, lv, l, idx, q.dpi, q.grp_d);
-        signal_count(stk_cnt(a, l, 2));
+        // layer by layer: the CTA of the last down item combines the layer at once
+        if (q.overlap) {
+          signal_count(stk_cnt(a, l, 2));
+        } else if (signal_last(stk_cnt(a, l, 2), ep1 * q.nD)) {
+          for (int ci = 0; ci < q.nC; ++ci) {
+            stack_combine_item(c, lv, l, ci);
+            __syncthreads();  // the next chunk restages the gates
+          }
+          if (c.tid == 0) {
+            __threadfence();
+            atomicAdd(stk_cnt(a, l, 3), (unsigned long long)q.nC);
+          }
+        }
       }
-    } else {
+    } else if (q.overlap) {
       ok = wait_count(stk_cnt(a, l, 2), ep1 * q.nD, a.status, next_pf);
       t1 = clock64();
       if (ok) {
