@@ -102,6 +102,7 @@ def load():
         "moe_trace_used": (I32, []),
         "moe_kernel_launch_count": (ctypes.c_ulonglong, []),
         "moe_last_cuda_error": (ctypes.c_int, []),
+        "moe_debug_wait_timeout": (ctypes.c_int, [P, I32, P]),
         "moe_layer_path": (ctypes.c_int, [D, I32]),
     }
     for name, (res, args) in sig.items():
@@ -265,6 +266,11 @@ def moe_trace_events(events):
 
 def moe_trace_used() -> int:
     return int(load().moe_trace_used())
+
+
+def moe_debug_wait_timeout(ws, limit_us, stream=None):
+    """Test hook: a bounded device wait that runs out (see include/moe_q8k.h)."""
+    _check(load().moe_debug_wait_timeout(_ptr(ws), limit_us, _stream(stream)), "moe_debug_wait_timeout")
 
 
 def moe_kernel_launch_count() -> int:

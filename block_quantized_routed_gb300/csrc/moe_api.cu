@@ -620,6 +620,13 @@ int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
 
 int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }
 
+int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream) {
+  if (!ws || !aligned(ws, kAlign) || limit_us < 1 || limit_us > 1000000) return MOE_ERR_INVALID_ARG;
+  int* status = static_cast<int*>(ws);
+  const unsigned* flag = reinterpret_cast<const unsigned*>(static_cast<char*>(ws) + 4);  // never the magic
+  return check(launch_debug_wait(status, flag, (long long)limit_us * 1000, as_stream(stream)));
+}
+
 int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, int32_t T,
                             int32_t* isum, int32_t* bsum, void* stream) {
   if (fmt != MOE_FMT_Q4K && fmt != MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED;

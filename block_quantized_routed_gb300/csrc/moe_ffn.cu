@@ -316,6 +316,28 @@ cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int
   return cudaGetLastError();
 }
 
+// A bounded wait on a flag that nothing sets: runs out after limit_ns of
+// wall time (%globaltimer), records MOE_ERR_DEVICE_TIMEOUT and returns, like
+// every wait of the library's kernels.
+__global__ void debug_wait_kernel(int* status, const unsigned* flag, long long limit_ns) {
+  unsigned long long t0, t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  while (*reinterpret_cast<const volatile unsigned*>(flag) != 0x7FEEDBEEu) {
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if ((long long)(t - t0) > limit_ns) {
+      set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+      return;
+    }
+    __nanosleep(1000);
+  }
+}
+
+cudaError_t launch_debug_wait(int* status, const unsigned* flag, long long limit_ns, cudaStream_t s) {
+  note_launch();
+  debug_wait_kernel<<<1, 1, 0, s>>>(status, flag, limit_ns);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t* q, int T, int32_t* isum,
                               int32_t* bsum, cudaStream_t s) {
   const int blocks = (N / 32) * (K / 256);

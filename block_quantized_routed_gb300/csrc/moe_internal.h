@@ -213,6 +213,8 @@ cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int
 cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t* q, int T, int32_t* isum,
                               int32_t* bsum, cudaStream_t s);
 
+cudaError_t launch_debug_wait(int* status, const unsigned* flag, long long limit_ns, cudaStream_t s);
+
 int num_sms();
 
 }  // namespace moe

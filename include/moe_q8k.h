@@ -336,6 +336,15 @@ unsigned long long moe_kernel_launch_count(void);
 #define MOE_PATH_TENSOR_PREFILL 2
 int moe_layer_path(const moe_layer_desc* desc, int32_t T);
 
+/* Test hook for failure detection: one kernel waits on a word of the
+ * workspace's status block for a value nothing ever writes, with the same
+ * kind of bound as every wait in the library's kernels; after limit_us
+ * microseconds (1 .. 1,000,000) it records MOE_ERR_DEVICE_TIMEOUT in the
+ * status word and returns, leaving the context usable.  moe_get_status then
+ * reports it.  No counterpart on the pages.  Returns MOE_OK, or
+ * MOE_ERR_INVALID_ARG / MOE_ERR_CUDA. */
+int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream);
+
 /* Test hook: the integer sub-block sums of the device dot routine that the
  * expert kernels use, for matrix w [N, K] against q8_K codes q [T, K]:
  *   isum int32 [T, N, K/256, n_sub] = sum over sub-block j of q_w * q_a,

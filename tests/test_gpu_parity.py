@@ -415,3 +415,19 @@ def test_stack_forward_rejects_prefill_shapes(moe):
     with pytest.raises(moe.MoeError) as e:
         moe.moe_stack_forward(desc, rows, 64, ws)
     assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+
+
+def test_bounded_wait_runs_out_and_reports(moe):
+    """A device wait on a flag nothing sets ends by itself, records a timeout
+    in the status word, and the context stays usable for the next layer."""
+    desc = dict(H=512, I=256, E=8, top_k=2, n_shared=0, route=0, fmt=FMT_Q4K, T_max=2)
+    ex = _experts_host(FMT_Q4K, 8, 512, 256, 5)
+    wr = synth.router_weight(8, 512, 5)
+    layer = moe.MoeLayer(desc, moe.expert_table([tuple(dev(m) for m in e) for e in ex]), dev(wr))
+    moe.moe_debug_wait_timeout(layer.ws, 2000)
+    assert moe.moe_get_status(layer.ws) == moe.MOE_ERR_DEVICE_TIMEOUT
+    assert moe.moe_get_status(layer.ws) == 0            # read and cleared
+    x = synth.activations(2, 512, 5)
+    out = layer.forward(dev(x)).cpu().numpy()
+    ref, _, _, _ = oracle.layer_forward(FMT_Q4K, 512, 256, 8, 2, 0, 0, ex, wr, None, x)
+    assert_close_rows(out, ref)
