@@ -248,7 +248,7 @@ def cpu_baseline(wl, T, x_host, budget_s):
     tokens = token_sample(T)
     done, spent = 0, 0.0
     layers = []
-    while spent < budget_s and done < wl.layers * 4:
+    while spent < budget_s and done < wl.layers * 64:
         l = done % wl.layers
         _, s = oracle_layers(wl, T, x_host[0], [l], nthreads, tokens)
         spent += s
@@ -440,14 +440,14 @@ def run_ours(args, wl, T):
         # per item kind of the stack kernel, summed over CTAs: work and wait cycles, items
         mhz = clock_info.get("sm_mhz") or 2070.0
         kinds = ["router", "routing", "gate_up", "down", "combine"]
-        G_ = int(torch.cuda.get_device_properties(dev).multi_processor_count) * 2
+        G_ = int(st[14])  # CTAs of the launch
         us = lambda v: round(float(v) / mhz, 1)
         phases = {"schedule": "stack_items_" + ("overlapped" if st[15] == 3 else "chained"),
                   "cta_us_summed_over_ctas": {**{f"work_{n}": us(st[k_]) for k_, n in enumerate(kinds)},
                                               **{f"wait_{n}": us(st[5 + k_]) for k_, n in enumerate(kinds)},
                                               "prologue": us(st[10]), "before_first_item": us(st[11]),
                                               "between_items": us(st[12])},
-                  "items": int(st[13]), "ctas_assumed": G_}
+                  "items": int(st[13]), "ctas": G_}
         st = np.zeros(16, np.int64)
     if st[15] == 2:   # pipelined schedule: one stage
         order = [0, 3, 4, 6, 1, 8, 12]

@@ -1380,7 +1380,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
   const long long t_ready = clock64();
   long long t_prev = t_ready, t_gaps = 0, t_head = -1, n_items_done = 0;
   const unsigned long long ep1 = 1;  // counter targets are counts x ep1
-  if (blockIdx.x == 0 && c.tid == 0 && a.phase_ns) a.phase_ns[15] = q.overlap ? 3 : 4;  // which order ran
+  if (blockIdx.x == 0 && c.tid == 0 && a.phase_ns) {
+    a.phase_ns[15] = q.overlap ? 3 : 4;  // which order ran
+    a.phase_ns[14] = gridDim.x;
+  }
   const long long n_items = q.count();
   const int G = gridDim.x;
   int staged_x = -1;
@@ -1461,7 +1464,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
   }
   // totals over all CTAs (SM cycles): [0..4] work per item kind, [5..9] wait
   // per item kind, [10] prologue (counter reset, order check, barrier),
-  // [11] before the first item, [12] between items, [13] items done
+  // [11] before the first item, [12] between items, [13] items done;
+  // [14] is the grid size
   if (c.tid == 0 && a.phase_ns) {
     for (int k = 0; k < 5; ++k) {
       atomicAdd(a.phase_ns + k, (unsigned long long)t_work[k]);

@@ -344,6 +344,39 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
         assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
 
 
+@pytest.mark.parametrize("chained", [False, True])
+def test_stack_forward_sixteen_tokens(moe, chained):
+    """The largest decode batch (16 tokens) at H=2048 through the dataflow
+    stack (top-1, so that the items per SM stay within the dataflow kernel's
+    range), chained and independent; every layer matches the oracle."""
+    fmt, route, S, H, I, E, k, T, L = FMT_Q4K, 0, 0, 2048, 256, 16, 1, 16, 2
+    ex = [_experts_host(fmt, E + S, H, I, seed=90 + l, layer=l) for l in range(L)]
+    tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
+    wrs = [synth.router_weight(E, H, 90, l) for l in range(L)]
+    xs_h = [synth.activations(T, H, 90, layer=l) for l in range(L)]
+    xs = [dev(xs_h[0])] + ([torch.empty((T, H), dtype=torch.float32, device="cuda")] if chained
+                           else [dev(xs_h[1])])
+    outs = ([xs[1]] if chained else [torch.empty((T, H), dtype=torch.float32, device="cuda")]) + \
+        [torch.empty((T, H), dtype=torch.float32, device="cuda")]
+    ids = [torch.empty((T, k), dtype=torch.int32, device="cuda") for _ in range(L)]
+    rows = [dict(table=tables[l], w_router=dev(wrs[l]), x=xs[l], residual=xs[l], out=outs[l], ids_out=ids[l])
+            for l in range(L)]
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    ws = torch.zeros(moe.moe_stack_workspace_size(desc, L), dtype=torch.uint8, device="cuda")
+    moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
+    assert moe.moe_get_status(ws) == 0
+    marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
+    assert int(marker[15]) == (4 if chained else 3)
+    for l in range(L):
+        xin = xs[l].cpu().numpy()
+        gids = ids[l].cpu().numpy()
+        rl, rids, _, rgap = oracle.route(xin, wrs[l], None, k, route)
+        routing_ok(gids, rids, rgap, rl)
+        ref, _, _, _ = oracle.layer_forward(fmt, H, I, E, k, S, route, ex[l], wrs[l], None, xin, residual=xin,
+                                            forced_ids=gids)
+        assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
+
+
 @pytest.mark.parametrize("fmt,route,S,T,L", [(FMT_Q4K, 0, 1, 1, 6), (FMT_Q2K, 1, 1, 4, 5), (FMT_Q4K, 0, 0, 3, 2)])
 def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
     """Layers with their own inputs: the kernel pipelines neighbouring layers;
