@@ -919,13 +919,16 @@ __device__ bool wait_count(const unsigned long long* p, unsigned long long targe
   __syncthreads();
   return s_ok != 0;
 }
-// All of this CTA's writes of the item are done: count the item.
+// All of this CTA's writes of the item are done: count the item.  A release
+// pattern (acq_rel fence, then a relaxed add; the barrier orders the other
+// threads' writes before the fence), lighter than a sequentially consistent
+// fence before the add; waiters read the counter with ld.acquire.
+__device__ __forceinline__ void release_add(unsigned long long* p, unsigned long long v) {
+  asm volatile("fence.acq_rel.gpu;\n red.relaxed.gpu.global.add.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
 __device__ void signal_count(unsigned long long* p) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(p, 1ull);
-  }
+  if (threadIdx.x == 0) release_add(p, 1ull);
 }
 
 // The same, and tells every thread whether this item was the one that
@@ -935,9 +938,11 @@ __device__ bool signal_last(unsigned long long* p, unsigned long long target) {
   __shared__ int s_last;
   __syncthreads();
   if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned long long old = atomicAdd(p, 1ull);
-    __threadfence();
+    unsigned long long old;
+    asm volatile("fence.acq_rel.gpu;\n atom.relaxed.gpu.global.add.u64 %0, [%1], 1;\n fence.acq_rel.gpu;"
+                 : "=l"(old)
+                 : "l"(p)
+                 : "memory");
     s_last = old + 1 == target;
   }
   __syncthreads();
@@ -1300,6 +1305,231 @@ __device__ void stack_down_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx
   }
 }
 
+__host__ __device__ inline size_t ring_offset(size_t decode_bytes) { return (decode_bytes + 127) / 128 * 128; }
+
+// sb_accum on a staged slab: the same sums in the same order, with the code
+// lines read from shared memory per token instead of held in registers
+template <int FMT>
+__device__ __forceinline__ void sb_accum_staged(const uint8_t* slab, const int8_t* act, const int16_t* bs,
+                                                const float* d, const int* act_off, int b, int cnt, float* acc,
+                                                int lane) {
+  using F = Fmt<FMT>;
+  SbRegs<FMT> s;  // scale/min words and d|dmin only
+  s.dm = *reinterpret_cast<const uint32_t*>(slab + 4 * lane);
+  if constexpr (FMT == kQ4K) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) s.sm[i] = *reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * lane + 4 * i);
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(slab + F::kSmOff + 16 * lane);
+    s.sm[0] = v.x; s.sm[1] = v.y; s.sm[2] = v.z; s.sm[3] = v.w;
+  }
+  int sc[F::kNSub], mn[F::kNSub];
+#pragma unroll
+  for (int j = 0; j < F::kNSub; ++j) sb_scale_min<FMT>(s, j, sc[j], mn[j]);
+  const float dw = half_lo(s.dm), dmin = half_hi(s.dm);
+  const uint8_t* code = slab + F::kCodeOff + 16 * lane;
+#pragma unroll 1
+  for (int t = 0; t < cnt; ++t) {
+    const int o = act_off[t];
+    const int8_t* a = act + o + 256 * b;
+    const int16_t* bsp = bs + o / 16 + 16 * b;
+    int S = 0, M = 0;
+    if constexpr (FMT == kQ4K) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        uint32_t lo[4], hi[4];
+        mask_q4k(*reinterpret_cast<const uint4*>(code + 512 * j), lo, hi);
+        S += sc[j] * isum_q4k(lo, hi, *reinterpret_cast<const int4*>(a + 32 * j),
+                              *reinterpret_cast<const int4*>(a + 32 * j + 16));
+        M += mn[j] * ((int)bsp[2 * j] + (int)bsp[2 * j + 1]);
+      }
+    } else {
+#pragma unroll
+      for (int ln = 0; ln < 4; ++ln) {
+        const uint4 line = *reinterpret_cast<const uint4*>(code + 512 * ln);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * ln + jj;
+          uint32_t w[4];
+          mask_q2k(line, j, w);
+          S += sc[j] * isum_q2k(w, *reinterpret_cast<const int4*>(a + 16 * j));
+          M += mn[j] * (int)bsp[j];
+        }
+      }
+    }
+    acc[t * 32 + lane] += d[o / 256 + b] * fmaf(dw, (float)S, -dmin * (float)M);
+  }
+}
+
+// ---- staged gate/up and down items -------------------------------------------
+// Each warp streams its super-block rows of the item through its own ring of
+// two shared-memory stages with cp.async (16 bytes per lane per
+// instruction, one commit group per unit of up to two slabs), so a warp's
+// next unit is in flight while it computes the current one and no
+// registers hold weights.  cp.async streams at the load path's rate (a
+// bulk copy per unit would not).
+constexpr int kRingStages = 2;
+
+template <int FMT>
+__host__ __device__ inline uint32_t ring_unit_bytes() { return 2u * Fmt<FMT>::kSlabBytes; }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+template <int FMT>
+struct WarpRing {
+  uint8_t* base;        // kRingStages stages of ring_unit_bytes
+  uint32_t issued, taken;
+  int lane;
+  // n0 bytes at s0, then n1 at s1, into the next stage (sizes multiples of 16)
+  __device__ void issue(const uint8_t* s0, uint32_t n0, const uint8_t* s1, uint32_t n1) {
+    const uint32_t d = static_cast<uint32_t>(
+        __cvta_generic_to_shared(base + (size_t)(issued % kRingStages) * ring_unit_bytes<FMT>()));
+    for (uint32_t off = 16u * lane; off < n0; off += 512u) cp_async16(d + off, s0 + off);
+    for (uint32_t off = 16u * lane; off < n1; off += 512u) cp_async16(d + n0 + off, s1 + off);
+    asm volatile("cp.async.commit_group;" ::: "memory");
+    ++issued;
+  }
+  // the oldest unit not yet taken, once this warp's copies of it landed
+  __device__ const uint8_t* take() {
+    if (issued - taken > 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+    __syncwarp();
+    return base + (size_t)(taken % kRingStages) * ring_unit_bytes<FMT>();
+  }
+  __device__ void give() {
+    __syncwarp();
+    ++taken;
+  }
+};
+
+// GU with the ring: the same item as stack_gateup_item; unit j of warp w =
+// the gate and up slabs of pair w + 8 j
+template <int FMT>
+__device__ void stack_gateup_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx, int gpi, int grp_g,
+                                  int& staged_x, WarpRing<FMT>& rg) {
+  using F = Fmt<FMT>;
+  const DecodeArgs& a = c.a;
+  const int T = c.T, H = c.H, I = c.I, nbH = c.nbH, lane = c.lane, warp = c.warp, tid = c.tid;
+  Smem& sm = c.sm;
+  uint8_t* lb = stk_layer(a, l);
+  const Route Rg = stk_route(a, l);
+  const int ti = idx / grp_g, rg0 = (idx % grp_g) * gpi;
+  const int nrg = min(gpi, c.nRG - rg0);
+  const int nt = __ldcg(Rg.n_tiles);
+  const Tile tl = ld_tile(Rg.tiles + ti);
+  const moe_expert_ptrs ep = ld_ptrs(reinterpret_cast<const moe_expert_ptrs*>(lb + a.sp.tptr) + ti);
+  if (ti >= nt || tl.flag) return;
+  const uint8_t* gbase = static_cast<const uint8_t*>(ep.gate) + (size_t)rg0 * c.gu_run;
+  const uint8_t* ubase = static_cast<const uint8_t*>(ep.up) + (size_t)rg0 * c.gu_run;
+  const int npair = nrg * nbH;
+  const int nu = warp < npair ? (npair - warp + kDecWarps - 1) / kDecWarps : 0;
+  auto issue = [&](int j) {
+    const size_t off = (size_t)(warp + kDecWarps * j) * F::kSlabBytes;
+    rg.issue(gbase + off, F::kSlabBytes, ubase + off, F::kSlabBytes);
+  };
+  for (int j = 0; j < nu && j < kRingStages; ++j) issue(j);  // in flight while x is staged
+  if (staged_x != l) {
+    const int8_t* xq = reinterpret_cast<const int8_t*>(lb + a.sp.xq);
+    const int16_t* xbs = reinterpret_cast<const int16_t*>(lb + a.sp.xbs);
+    const float* xd = reinterpret_cast<const float*>(lb + a.sp.xd);
+    for (int i = tid; i < T * H / 16; i += kDecThreads)
+      reinterpret_cast<int4*>(sm.xq)[i] = __ldcg(reinterpret_cast<const int4*>(xq) + i);
+    for (int i = tid; i < T * H / 128; i += kDecThreads)
+      reinterpret_cast<int4*>(sm.xbs)[i] = __ldcg(reinterpret_cast<const int4*>(xbs) + i);
+    for (int i = tid; i < T * nbH; i += kDecThreads) sm.xd[i] = __ldcg(xd + i);
+    staged_x = l;
+  }
+  for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = __ldcg(Rg.tok + tl.start + t) * H;
+  float* accw = sm.red + (size_t)warp * gpi * 2 * T * 32;  // [row group][gate, up][T][32]
+  for (int i = lane; i < gpi * 2 * T * 32; i += 32) accw[i] = 0.0f;
+  __syncthreads();
+  for (int j = 0; j < nu; ++j) {
+    const uint8_t* st = rg.take();
+    const int p = warp + kDecWarps * j;
+    const int rgl = p / nbH, b = p % nbH;
+    float* acc = accw + (size_t)rgl * 2 * T * 32;
+    sb_accum_staged<FMT>(st, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc, lane);
+    sb_accum_staged<FMT>(st + F::kSlabBytes, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc + T * 32, lane);
+    rg.give();
+    if (j + kRingStages < nu) issue(j + kRingStages);
+  }
+  __syncthreads();
+  float* h = reinterpret_cast<float*>(lb + a.sp.h);
+  for (int i = tid; i < nrg * tl.count * 32; i += kDecThreads) {
+    const int r = i & 31, t = (i >> 5) % tl.count, rgl = (i >> 5) / tl.count;
+    float Gv = 0.0f, Uv = 0.0f;
+#pragma unroll
+    for (int w = 0; w < kDecWarps; ++w) {
+      const float* acc = sm.red + ((size_t)w * gpi + rgl) * 2 * T * 32;
+      Gv += acc[t * 32 + r];
+      Uv += acc[(T + t) * 32 + r];
+    }
+    h[(size_t)(tl.start + t) * I + (rg0 + rgl) * 32 + r] = Gv / (1.0f + expf(-Gv)) * Uv;
+  }
+}
+
+// D with the ring: the same item as stack_down_item; warp w's units are, for
+// each of its row groups rgi + 8 j + w, the slab pairs (2v, 2v + 1)
+template <int FMT>
+__device__ void stack_down_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx, int dpi, int grp_d,
+                                WarpRing<FMT>& rg) {
+  using F = Fmt<FMT>;
+  const DecodeArgs& a = c.a;
+  const int T = c.T, H = c.H, I = c.I, nbI = c.nbI, lane = c.lane, warp = c.warp, tid = c.tid;
+  Smem& sm = c.sm;
+  uint8_t* lb = stk_layer(a, l);
+  const Route Rg = stk_route(a, l);
+  const int ti = idx / grp_d, rgi = (idx % grp_d) * kDownRG * dpi;
+  const int nt = __ldcg(Rg.n_tiles);
+  const Tile tl = ld_tile(Rg.tiles + ti);
+  const void* dn = reinterpret_cast<const void*>(
+      __ldcg(reinterpret_cast<const unsigned long long*>(lb + a.sp.tptr) + 3 * ti + 2));
+  if (ti >= nt || tl.flag) return;
+  const uint8_t* dbase = static_cast<const uint8_t*>(dn);
+  const int upr = (nbI + 1) / 2;
+  int nj = 0;
+  for (int j = 0; j < dpi; ++j) nj += rgi + j * kDownRG + warp < c.nRGH;
+  const int nu = nj * upr;
+  auto issue = [&](int u) {
+    const int j = u / upr, v = u % upr;
+    rg.issue(dbase + (size_t)(rgi + j * kDownRG + warp) * c.dn_rg_bytes + (size_t)(2 * v) * F::kSlabBytes,
+             (uint32_t)min(2, nbI - 2 * v) * F::kSlabBytes, nullptr, 0);
+  };
+  for (int u = 0; u < nu && u < kRingStages; ++u) issue(u);  // in flight while h is quantized
+  const float* h = reinterpret_cast<const float*>(lb + a.sp.h);
+  for (int task = warp; task < tl.count * nbI; task += kDecWarps) {
+    const int t = task / nbI, blk = task % nbI;
+    const float4* src = reinterpret_cast<const float4*>(h + (size_t)(tl.start + t) * I + blk * 256 + 8 * lane);
+    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+    const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+    q8k_block_warp(v, lane, sm.hq + (size_t)t * I + blk * 256, sm.hd + t * nbI + blk,
+                   sm.hbs + (size_t)t * (I / 16) + blk * 16);
+  }
+  for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = t * I;
+  float* accw = sm.red + (size_t)warp * dpi * T * 32;  // [dpi][T][32]
+  for (int i = lane; i < dpi * T * 32; i += 32) accw[i] = 0.0f;
+  __syncthreads();
+  float* y = reinterpret_cast<float*>(lb + a.sp.y);
+  for (int j = 0; j < nj; ++j) {
+    const int rgrow = rgi + j * kDownRG + warp;
+    float* acc = accw + (size_t)j * T * 32;
+    for (int v = 0; v < upr; ++v) {
+      const int u = j * upr + v;
+      const uint8_t* st = rg.take();
+      for (int bb = 0; bb < 2 && 2 * v + bb < nbI; ++bb)
+        sb_accum_staged<FMT>(st + bb * F::kSlabBytes, sm.hq, sm.hbs, sm.hd, sm.aoff, 2 * v + bb, tl.count, acc,
+                             lane);
+      rg.give();
+      if (u + kRingStages < nu) issue(u + kRingStages);
+    }
+    __syncwarp();
+    for (int t = 0; t < tl.count; ++t)
+      y[(size_t)__ldcg(Rg.slot + tl.start + t) * H + rgrow * 32 + lane] = acc[t * 32 + lane];
+  }
+}
+
 // C: float4 elements [1024 idx, 1024 idx + 1024) of out_l
 template <int FMT>
 __device__ void stack_combine_item(Ctx<FMT>& c, const LayerView& lv, int l, int idx) {
@@ -1345,11 +1575,17 @@ __device__ void stack_combine_item(Ctx<FMT>& c, const LayerView& lv, int l, int 
   }
 }
 
-template <int FMT>
+template <int FMT, bool kRing>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const long long t_launch = clock64();
   Ctx<FMT> c(a, smem_raw);
+  // kRing: each warp's two weight stages after the decode buffers
+  WarpRing<FMT> ring;
+  ring.base = smem_raw + ring_offset(decode_smem(c.T, c.H, c.I, c.E, c.k, c.S, nullptr, nullptr)) +
+              (size_t)c.warp * kRingStages * ring_unit_bytes<FMT>();
+  ring.issued = ring.taken = 0;
+  ring.lane = c.lane;
   StackSeq q;
   q.L = a.n_layers;
   q.overlap = stack_disjoint(a, q.L);
@@ -1387,14 +1623,19 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
   const long long n_items = q.count();
   const int G = gridDim.x;
   int staged_x = -1;
-  if (c.tid == 32) stack_prefetch(c, q, blockIdx.x, ep1);
+  if (!kRing && c.tid == 32) stack_prefetch(c, q, blockIdx.x, ep1);
   for (long long i = blockIdx.x; i < n_items; i += G) {
     int kind, l, idx;
     q.item(i, kind, l, idx);
     if (l < 0 || l >= q.L) continue;
     const LayerView lv = layer_view(a, l);
     bool ok = true;
-    auto next_pf = [&]() { stack_prefetch(c, q, i + G, ep1); };
+    // while thread 0 waits, thread 32 prefetches the next item's weights
+    // towards L2; with the weight rings that lookup only delays the wait's
+    // closing barrier (measured), so they go without
+    auto next_pf = [&]() {
+      if constexpr (!kRing) stack_prefetch(c, q, i + G, ep1);
+    };
     const long long t0 = clock64();
     if (t_head < 0) t_head = t0 - t_ready;
     else t_gaps += t0 - t_prev;
@@ -1426,14 +1667,16 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       ok = wait_count(stk_cnt(a, l, 1), ep1, a.status, next_pf);
       t1 = clock64();
       if (ok) {
-        stack_gateup_item(c, lv, l, idx, q.gpi, q.grp_g, staged_x);
+        if constexpr (kRing) stack_gateup_ring(c, lv, l, idx, q.gpi, q.grp_g, staged_x, ring);
+        else stack_gateup_item(c, lv, l, idx, q.gpi, q.grp_g, staged_x);
         signal_count(stk_cnt(a, l, kStackCnt + idx / q.grp_g));
       }
     } else if (kind == StackSeq::kD) {
       ok = wait_count(stk_cnt(a, l, kStackCnt + idx / q.grp_d), ep1 * q.grp_g, a.status, next_pf);
       t1 = clock64();
       if (ok) {
-        stack_down_item(c, lv, l, idx, q.dpi, q.grp_d);
+        if constexpr (kRing) stack_down_ring(c, lv, l, idx, q.dpi, q.grp_d, ring);
+        else stack_down_item(c, lv, l, idx, q.dpi, q.grp_d);
         // layer by layer: the CTA of the last down item combines the layer at once
         if (q.overlap) {
           signal_count(stk_cnt(a, l, 2));
@@ -1442,10 +1685,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
             stack_combine_item(c, lv, l, ci);
             __syncthreads();  // the next chunk restages the gates
           }
-          if (c.tid == 0) {
-            __threadfence();
-            atomicAdd(stk_cnt(a, l, 3), (unsigned long long)q.nC);
-          }
+          if (c.tid == 0) release_add(stk_cnt(a, l, 3), (unsigned long long)q.nC);
         }
       }
     } else if (q.overlap) {
@@ -1480,16 +1720,25 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
 
 template <int FMT>
 cudaError_t launch_stack_t(const DecodeArgs& a, cudaStream_t s) {
-  const size_t smem = decode_smem(a.T, a.H, a.I, a.E, a.k, a.S, nullptr, nullptr);
-  auto kern = decode_stack_kernel<FMT>;
-  static size_t opted = 0;  // per instantiation; the opt-in only grows
-  if (smem > opted) {
-    cudaError_t err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  // with the warps' weight rings when they fit beside the decode buffers
+  const size_t base = decode_smem(a.T, a.H, a.I, a.E, a.k, a.S, nullptr, nullptr);
+  int dev = 0, optin = 0;
+  cudaError_t err = cudaGetDevice(&dev);
+  if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+  if (err != cudaSuccess) return err;
+  const size_t spare = 1024;  // the kernel's static shared variables
+  const size_t ring_smem = ring_offset(base) + (size_t)kDecWarps * kRingStages * ring_unit_bytes<FMT>();
+  const bool ring = ring_smem + spare <= (size_t)optin;
+  const size_t smem = ring ? ring_smem : base;
+  auto kern = ring ? decode_stack_kernel<FMT, true> : decode_stack_kernel<FMT, false>;
+  static size_t opted[2] = {0, 0};  // per instantiation; the opt-in only grows
+  if (smem > opted[ring]) {
+    err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (err != cudaSuccess) return err;
-    opted = smem;
+    opted[ring] = smem;
   }
   int per_sm = 0;
-  cudaError_t err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
+  err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecThreads, smem);
   if (err != cudaSuccess) return err;
   if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
   const int grid = num_sms() * std::min(per_sm, 2);

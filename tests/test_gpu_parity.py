@@ -345,11 +345,14 @@ def test_stack_forward_chained_layers(moe, fmt, route, S, T):
 
 
 @pytest.mark.parametrize("chained", [False, True])
-def test_stack_forward_sixteen_tokens(moe, chained):
-    """The largest decode batch (16 tokens) at H=2048 through the dataflow
-    stack (top-1, so that the items per SM stay within the dataflow kernel's
-    range), chained and independent; every layer matches the oracle."""
-    fmt, route, S, H, I, E, k, T, L = FMT_Q4K, 0, 0, 2048, 256, 16, 1, 16, 2
+@pytest.mark.parametrize("H", [2048, 4096])
+def test_stack_forward_sixteen_tokens(moe, chained, H):
+    """The largest decode batch (16 tokens) through the dataflow stack (top-1,
+    so that the items per SM stay within the dataflow kernel's range),
+    chained and independent; at H=4096 the 16 staged token rows leave no
+    room for the warps' weight rings, so that shape runs the register-load
+    items.  Every layer matches the oracle."""
+    fmt, route, S, I, E, k, T, L = FMT_Q4K, 0, 0, 256, 16, 1, 16, 2
     ex = [_experts_host(fmt, E + S, H, I, seed=90 + l, layer=l) for l in range(L)]
     tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
     wrs = [synth.router_weight(E, H, 90, l) for l in range(L)]
