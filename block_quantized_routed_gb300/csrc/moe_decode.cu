@@ -1429,21 +1429,34 @@ __device__ void stack_gateup_ring(Ctx<FMT>& c, const LayerView& lv, int l, int i
     const size_t off = (size_t)(warp + kDecWarps * j) * F::kSlabBytes;
     rg.issue(gbase + off, F::kSlabBytes, ubase + off, F::kSlabBytes);
   };
-  for (int j = 0; j < nu && j < kRingStages; ++j) issue(j);  // in flight while x is staged
-  if (staged_x != l) {
-    const int8_t* xq = reinterpret_cast<const int8_t*>(lb + a.sp.xq);
-    const int16_t* xbs = reinterpret_cast<const int16_t*>(lb + a.sp.xbs);
-    const float* xd = reinterpret_cast<const float*>(lb + a.sp.xd);
-    for (int i = tid; i < T * H / 16; i += kDecThreads)
-      reinterpret_cast<int4*>(sm.xq)[i] = __ldcg(reinterpret_cast<const int4*>(xq) + i);
-    for (int i = tid; i < T * H / 128; i += kDecThreads)
-      reinterpret_cast<int4*>(sm.xbs)[i] = __ldcg(reinterpret_cast<const int4*>(xbs) + i);
-    for (int i = tid; i < T * nbH; i += kDecThreads) sm.xd[i] = __ldcg(xd + i);
+  // the small reads first (they would otherwise queue behind the weight
+  // stream): q8_K(x) of the layer as one copy group, the tile's tokens
+  const bool stage = staged_x != l;
+  if (stage) {
+    const uint8_t* xq = lb + a.sp.xq;
+    const uint8_t* xbs = lb + a.sp.xbs;
+    const uint8_t* xd = lb + a.sp.xd;
+    const uint32_t dq = static_cast<uint32_t>(__cvta_generic_to_shared(sm.xq));
+    const uint32_t db = static_cast<uint32_t>(__cvta_generic_to_shared(sm.xbs));
+    const uint32_t dd = static_cast<uint32_t>(__cvta_generic_to_shared(sm.xd));
+    for (int i = tid; i < T * H / 16; i += kDecThreads) cp_async16(dq + 16 * i, xq + 16 * i);
+    for (int i = tid; i < T * H / 128; i += kDecThreads) cp_async16(db + 16 * i, xbs + 16 * i);
+    for (int i = tid; i < T * nbH; i += kDecThreads)
+      asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(dd + 4 * i), "l"(xd + 4 * i) : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
     staged_x = l;
   }
-  for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = __ldcg(Rg.tok + tl.start + t) * H;
+  const int tok = tid < tl.count ? __ldcg(Rg.tok + tl.start + tid) : 0;  // tl.count <= 16
+  for (int j = 0; j < nu && j < kRingStages; ++j) issue(j);
   float* accw = sm.red + (size_t)warp * gpi * 2 * T * 32;  // [row group][gate, up][T][32]
   for (int i = lane; i < gpi * 2 * T * 32; i += 32) accw[i] = 0.0f;
+  if (stage) {  // the x group is done; the weight groups after it may still be in flight
+    const int newer = min(nu, kRingStages);
+    if (newer >= 2) asm volatile("cp.async.wait_group 2;" ::: "memory");
+    else if (newer == 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
+    else asm volatile("cp.async.wait_group 0;" ::: "memory");
+  }
+  if (tid < tl.count) sm.aoff[tid] = tok * H;
   __syncthreads();
   for (int j = 0; j < nu; ++j) {
     const uint8_t* st = rg.take();
@@ -1497,12 +1510,25 @@ __device__ void stack_down_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx
     rg.issue(dbase + (size_t)(rgi + j * kDownRG + warp) * c.dn_rg_bytes + (size_t)(2 * v) * F::kSlabBytes,
              (uint32_t)min(2, nbI - 2 * v) * F::kSlabBytes, nullptr, 0);
   };
-  for (int u = 0; u < nu && u < kRingStages; ++u) issue(u);  // in flight while h is quantized
+  // the warp's first block of h is read before the weight stream is issued
+  // (small reads would otherwise queue behind it)
   const float* h = reinterpret_cast<const float*>(lb + a.sp.h);
+  auto h_src = [&](int task) {
+    const int t = task / nbI, blk = task % nbI;
+    return reinterpret_cast<const float4*>(h + (size_t)(tl.start + t) * I + blk * 256 + 8 * lane);
+  };
+  float4 v0 = make_float4(0.f, 0.f, 0.f, 0.f), v1 = v0;
+  if (warp < tl.count * nbI) {
+    v0 = __ldcg(h_src(warp));
+    v1 = __ldcg(h_src(warp) + 1);
+  }
+  for (int u = 0; u < nu && u < kRingStages; ++u) issue(u);
   for (int task = warp; task < tl.count * nbI; task += kDecWarps) {
     const int t = task / nbI, blk = task % nbI;
-    const float4* src = reinterpret_cast<const float4*>(h + (size_t)(tl.start + t) * I + blk * 256 + 8 * lane);
-    const float4 v0 = __ldcg(src), v1 = __ldcg(src + 1);
+    if (task != warp) {
+      v0 = __ldcg(h_src(task));
+      v1 = __ldcg(h_src(task) + 1);
+    }
     const float v[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
     q8k_block_warp(v, lane, sm.hq + (size_t)t * I + blk * 256, sm.hd + t * nbI + blk,
                    sm.hbs + (size_t)t * (I / 16) + blk * 16);
