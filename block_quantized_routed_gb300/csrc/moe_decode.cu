@@ -116,6 +116,7 @@ struct Smem {
   int16_t* hbs;    // [T][I/16]
   float* hd;       // [T][nbI]
   int* aoff;       // [T]  activation row offsets of the current item
+  int* srow;       // [T]  slot rows of the current down item's tokens
 };
 
 __host__ __device__ inline size_t al16(size_t v) { return (v + 15) / 16 * 16; }
@@ -162,6 +163,7 @@ __host__ __device__ inline size_t decode_smem(int T, int H, int I, int E, int k,
   p = take((size_t)T * (I / 16) * 2);      if (sm) sm->hbs = (int16_t*)p;
   p = take((size_t)T * (I / 256) * 4);     if (sm) sm->hd = (float*)p;
   p = take((size_t)T * 4);                 if (sm) sm->aoff = (int*)p;
+  p = take((size_t)T * 4);                 if (sm) sm->srow = (int*)p;
   return off;
 }
 
@@ -1522,6 +1524,7 @@ __device__ void stack_down_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx
     v0 = __ldcg(h_src(warp));
     v1 = __ldcg(h_src(warp) + 1);
   }
+  const int slot = tid < tl.count ? __ldcg(Rg.slot + tl.start + tid) : 0;  // tl.count <= 16
   for (int u = 0; u < nu && u < kRingStages; ++u) issue(u);
   for (int task = warp; task < tl.count * nbI; task += kDecWarps) {
     const int t = task / nbI, blk = task % nbI;
@@ -1534,6 +1537,8 @@ __device__ void stack_down_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx
                    sm.hbs + (size_t)t * (I / 16) + blk * 16);
   }
   for (int t = tid; t < tl.count; t += kDecThreads) sm.aoff[t] = t * I;
+  int* srow = sm.srow;
+  if (tid < tl.count) srow[tid] = slot;
   float* accw = sm.red + (size_t)warp * dpi * T * 32;  // [dpi][T][32]
   for (int i = lane; i < dpi * T * 32; i += 32) accw[i] = 0.0f;
   __syncthreads();
@@ -1551,8 +1556,7 @@ __device__ void stack_down_ring(Ctx<FMT>& c, const LayerView& lv, int l, int idx
       if (u + kRingStages < nu) issue(u + kRingStages);
     }
     __syncwarp();
-    for (int t = 0; t < tl.count; ++t)
-      y[(size_t)__ldcg(Rg.slot + tl.start + t) * H + rgrow * 32 + lane] = acc[t * 32 + lane];
+    for (int t = 0; t < tl.count; ++t) y[(size_t)srow[t] * H + rgrow * 32 + lane] = acc[t * 32 + lane];
   }
 }
 
@@ -1654,7 +1658,10 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
     int kind, l, idx;
     q.item(i, kind, l, idx);
     if (l < 0 || l >= q.L) continue;
-    const LayerView lv = layer_view(a, l);
+    // the layer's pointer record, read only by the items that use it (router,
+    // routing, combine): gate/up and down items do not wait for it
+    auto lv = [&]() { return layer_view(a, l); };
+    const LayerView none{};
     bool ok = true;
     // while thread 0 waits, thread 32 prefetches the next item's weights
     // towards L2; with the weight rings that lookup only delays the wait's
@@ -1671,12 +1678,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       else if (c.tid == 32) next_pf();
       t1 = clock64();
       if (ok) {
-        stack_router_item(c, lv, l, idx, q.nR);
+        stack_router_item(c, lv(), l, idx, q.nR);
         // layer by layer: the CTA of the last router item routes the layer at once
         if (q.overlap) {
           signal_count(stk_cnt(a, l, 0));
         } else if (signal_last(stk_cnt(a, l, 0), ep1 * q.nR)) {
-          stack_routing_item(c, lv, l, l == q.L - 1);
+          stack_routing_item(c, lv(), l, l == q.L - 1);
           signal_count(stk_cnt(a, l, 1));
         }
       }
@@ -1685,7 +1692,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
         ok = wait_count(stk_cnt(a, l, 0), ep1 * q.nR, a.status, next_pf);
         t1 = clock64();
         if (ok) {
-          stack_routing_item(c, lv, l, l == q.L - 1);
+          stack_routing_item(c, lv(), l, l == q.L - 1);
           signal_count(stk_cnt(a, l, 1));
         }
       }
@@ -1693,22 +1700,23 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       ok = wait_count(stk_cnt(a, l, 1), ep1, a.status, next_pf);
       t1 = clock64();
       if (ok) {
-        if constexpr (kRing) stack_gateup_ring(c, lv, l, idx, q.gpi, q.grp_g, staged_x, ring);
-        else stack_gateup_item(c, lv, l, idx, q.gpi, q.grp_g, staged_x);
+        if constexpr (kRing) stack_gateup_ring(c, none, l, idx, q.gpi, q.grp_g, staged_x, ring);
+        else stack_gateup_item(c, none, l, idx, q.gpi, q.grp_g, staged_x);
         signal_count(stk_cnt(a, l, kStackCnt + idx / q.grp_g));
       }
     } else if (kind == StackSeq::kD) {
       ok = wait_count(stk_cnt(a, l, kStackCnt + idx / q.grp_d), ep1 * q.grp_g, a.status, next_pf);
       t1 = clock64();
       if (ok) {
-        if constexpr (kRing) stack_down_ring(c, lv, l, idx, q.dpi, q.grp_d, ring);
-        else stack_down_item(c, lv, l, idx, q.dpi, q.grp_d);
+        if constexpr (kRing) stack_down_ring(c, none, l, idx, q.dpi, q.grp_d, ring);
+        else stack_down_item(c, none, l, idx, q.dpi, q.grp_d);
         // layer by layer: the CTA of the last down item combines the layer at once
         if (q.overlap) {
           signal_count(stk_cnt(a, l, 2));
         } else if (signal_last(stk_cnt(a, l, 2), ep1 * q.nD)) {
+          const LayerView lvc = lv();
           for (int ci = 0; ci < q.nC; ++ci) {
-            stack_combine_item(c, lv, l, ci);
+            stack_combine_item(c, lvc, l, ci);
             __syncthreads();  // the next chunk restages the gates
           }
           if (c.tid == 0) release_add(stk_cnt(a, l, 3), (unsigned long long)q.nC);
@@ -1718,7 +1726,7 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_stack_kernel(const __gr
       ok = wait_count(stk_cnt(a, l, 2), ep1 * q.nD, a.status, next_pf);
       t1 = clock64();
       if (ok) {
-        stack_combine_item(c, lv, l, idx);
+        stack_combine_item(c, lv(), l, idx);
         signal_count(stk_cnt(a, l, 3));
       }
     }
