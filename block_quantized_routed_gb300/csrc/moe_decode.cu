@@ -1099,16 +1099,21 @@ __device__ void stack_router_item(Ctx<FMT>& c, const LayerView& lv, int l, int i
 // result as routing_phase (tiles by expert, shared experts last), without
 // writing the layer's counts and offsets to global memory.
 template <int FMT>
-__device__ void routing_small(Ctx<FMT>& c, const LayerView& lv, const float* logits, const Route& R) {
+__device__ void routing_small(Ctx<FMT>& c, const LayerView& lv, const float* logits, const Route& R,
+                              moe_expert_ptrs* tptr) {
   const DecodeArgs& a = c.a;
   const int T = c.T, E = c.E, k = c.k, S = c.S, tid = c.tid, TK = T * k;
   int* first = reinterpret_cast<int*>(c.sm.red);  // [TK]: pair is its expert's first
+  // [TK + S]: each pair's expert pointer record (one read of the table
+  // serves the presence test here and the published tile pointers)
+  moe_expert_ptrs* rec = reinterpret_cast<moe_expert_ptrs*>(c.sm.red + 256);
   for (int t = c.warp; t < T; t += kDecWarps)
     warp_topk(logits + (size_t)t * E, E, k, a.route, c.lane, R.ids + t * k, R.gates + t * k, nullptr);
   __syncthreads();
   for (int p = tid; p < TK + S; p += kDecThreads) {
     const int e = p < TK ? R.ids[p] : E + (p - TK);
-    R.ok[p] = lv.table[e].gate != nullptr ? 1 : 0;  // present ("mine")?
+    rec[p] = lv.table[e];
+    R.ok[p] = rec[p].gate != nullptr ? 1 : 0;  // present ("mine")?
   }
   for (int p = tid; p < TK; p += kDecThreads) {
     const int e = R.ids[p];
@@ -1137,6 +1142,7 @@ __device__ void routing_small(Ctx<FMT>& c, const LayerView& lv, const float* log
       tl.count = cnt;
       tl.flag = R.ok[p] ? 0 : 1;
       R.tiles[tix] = tl;
+      if (tptr) tptr[tix] = rec[p];
     }
   }
   __shared__ int s_distinct;
@@ -1158,6 +1164,7 @@ __device__ void routing_small(Ctx<FMT>& c, const LayerView& lv, const float* log
       tl.count = T;
       tl.flag = R.ok[TK + sh] ? 0 : 1;
       R.tiles[nr + sh] = tl;
+      if (tptr) tptr[nr + sh] = rec[TK + sh];
     }
   }
   if (tid == 0) *R.n_tiles = nr + S;
@@ -1174,18 +1181,21 @@ __device__ void stack_routing_item(Ctx<FMT>& c, const LayerView& lv, int l, bool
   const DecodeArgs& a = c.a;
   uint8_t* lb = stk_layer(a, l);
   const Route R = c.route(0);
+  // each tile's weight pointers beside the tiles: a consumer reads tile and
+  // pointers in one round trip (routing_small writes them as it plans)
+  moe_expert_ptrs* tp = reinterpret_cast<moe_expert_ptrs*>(lb + a.sp.tptr);
   // the last layer also fills the workspace's counts/offsets/perm: the general routine
-  if (last || c.T * c.k > kDecThreads)
+  const bool general = last || c.T * c.k > kDecThreads;
+  if (general)
     routing_phase(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R, false, last, true);
   else
-    routing_small(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R);
+    routing_small(c, lv, reinterpret_cast<const float*>(lb + a.sp.logits), R, tp);
   __syncthreads();
   const int4* src = reinterpret_cast<const int4*>(c.sm.rbase);
   int4* dst = reinterpret_cast<int4*>(lb + a.sp.route);
   for (size_t i = c.tid; i < c.sm.rstride / 16; i += kDecThreads) dst[i] = src[i];
-  // each tile's weight pointers beside the tiles: a consumer reads tile and pointers in one round trip
-  moe_expert_ptrs* tp = reinterpret_cast<moe_expert_ptrs*>(lb + a.sp.tptr);
-  for (int t = c.tid; t < *R.n_tiles; t += kDecThreads) tp[t] = lv.table[R.tiles[t].expert];
+  if (general)
+    for (int t = c.tid; t < *R.n_tiles; t += kDecThreads) tp[t] = lv.table[R.tiles[t].expert];
 }
 
 
