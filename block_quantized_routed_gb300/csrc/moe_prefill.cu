@@ -172,13 +172,16 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+constexpr int kEpilogueSleepNs = 256;  // the 16 epilogue warps wait a whole tile's MMAs at a time
+
 // Bounded wait for phase `parity`.  Gives up when another role has aborted,
 // or after about a second, recording a timeout; false = abort.
 // `spent` accumulates the cycles waited (per-role wait statistics).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                         long long& spent) {
+                                         long long& spent, int sleep_ns = 0) {
   const long long t0 = clock64();  // before the first try: try_wait itself may suspend the thread
   while (!mbar_try(bar, parity)) {
+    if (sleep_ns) __nanosleep(sleep_ns);  // a waiter off the critical path leaves issue slots to the others
     if (*abort_flag) return false;
     if (clock64() - t0 > kWaitCycles) {
       *abort_flag = 1;
@@ -193,9 +196,9 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 // The same, taken by lane 0 for its whole (converged) warp: every lane gets
 // the same answer, so the warp stays converged for .sync.aligned operations.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
-                                          long long& spent) {
+                                          long long& spent, int sleep_ns = 0) {
   bool ok = true;
-  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status, spent);
+  if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort_flag, status, spent, sleep_ns);
   ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
   __syncwarp();  // orders the other lanes after lane 0's acquire
   return ok;
@@ -706,7 +709,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr + (size_t)(b + 1) * slab_bytes));
           da_n = vt ? __ldg(dgp + (int64_t)(b + 1) * a.P) : 0.0f;
         }
-        if (!(ok = warp_wait(tfull(ab), (tb >> 1) & 1, abort_flag, a.status, w0))) break;
+        if (!(ok = warp_wait(tfull(ab), (tb >> 1) & 1, abort_flag, a.status, w0, kEpilogueSleepNs))) break;
         tc_fence_after();
         s_da[lane] = da;
         __syncwarp();
