@@ -427,6 +427,7 @@ def run_ours(args, wl, T):
     phases = None
     phase_ws = ws if stacked else layers[-1].ws
     st = moe.MoeLayer.ws_view_of(phase_ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,)).cpu().numpy()
+    ran = int(st[15])  # which single-launch kernel ran a stack: 3/4 dataflow, 1/2 pipelined
     if path == moe.PATH_TENSOR_PREFILL:
         # wait statistics of the GEMMs' CTA 0 (SM cycles): per role, then the CTA's total
         mhz = clock_info.get("sm_mhz") or 2070.0
@@ -477,9 +478,10 @@ def run_ours(args, wl, T):
         launch_ms = events[0].elapsed_time(events[1])
         alg = float(union[last_r].sum() * exp_bytes + L * router_bytes)
         gbs = alg / (launch_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "kernel": "decode_stack_kernel (all layers of a step, one cooperative launch)",
+        kname = "decode_stack_kernel" if ran in (3, 4) else "decode_fused_kernel"
+        roofline = {"bound": "hbm", "kernel": f"{kname} (all layers of a step, one cooperative launch)",
                     "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "peak_source": peak_src,
-                    "traffic": profiled_traffic(wl.name, "decode_stack_kernel"),
+                    "traffic": profiled_traffic(wl.name, kname),
                     "algorithmic_bytes_per_launch": alg, "avg_launch_us": 1e3 * launch_ms}
     elif path == moe.PATH_TENSOR_PREFILL:
         # the tcgen05 gate/up GEMM (+ SwiGLU) is the dominant kernel; a contraction: tensor-bound

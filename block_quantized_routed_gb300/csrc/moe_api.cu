@@ -132,6 +132,8 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 // Gate/up and down items of one layer of the dataflow stack per SM (the same
 // item sizes as decode_stack_kernel chooses).
+constexpr int kFlowMinLayers = 4;  // heavy layers take the dataflow kernel from this many layers on
+
 double stack_items_per_sm(const moe_layer_desc& d, int T) {
   const int nbH = d.H / 256, nbI = d.I / 256, nRG = d.I / 32, nRGH = d.H / 32;
   const int Tm = T > 16 ? T : 16;
@@ -485,11 +487,12 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   if (ws_bytes < ext + sp.total) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
-  // Layers with many expert items per CTA (wide experts, long verify
-  // windows) run faster on the barrier-pipelined kernel, whose CTAs
-  // prefetch all of their items of a layer at once; small layers run as the
-  // dataflow of items.
-  if (stack_items_per_sm(*desc, T) > 2.0) {
+  // Short stacks of layers with many expert items per CTA (a wide layer on
+  // its own) run faster on the barrier-pipelined kernel, whose CTAs
+  // prefetch all of their items of a layer at once; small layers, and heavy
+  // layers with enough neighbours to overlap (measured: a 48-layer verify
+  // stack), run as the dataflow of items.
+  if (stack_items_per_sm(*desc, T) > 2.0 && n_layers < kFlowMinLayers) {
     DecodeArgs d{};
     d.fmt = desc->fmt;
     d.H = H;

@@ -245,10 +245,10 @@ size_t moe_stack_workspace_size(const moe_layer_desc* desc, int32_t n_layers);
  * moe_layer_forward per layer instead).  ws: moe_stack_workspace_size(desc,
  * n_layers) bytes, 256-byte aligned, its 16-byte status block zero before
  * the first call (e.g. a zero-filled allocation); ids/gates/counts/offsets/
- * perm in it hold the last layer's routing.  Layers with many expert
- * items per SM (wide experts, long verify windows) run instead on the
- * barrier-pipelined single-launch kernel, which prefetches all of a CTA's
- * items of a layer at once.  phase_ns[15] reports what ran: 3 dataflow,
+ * perm in it hold the last layer's routing.  Stacks of fewer than 4
+ * layers with many expert items per SM (a wide layer on its own) run
+ * instead on the barrier-pipelined single-launch kernel, which prefetches
+ * all of a CTA's items of a layer at once.  phase_ns[15] reports what ran: 3 dataflow,
  * layers overlapped; 4 dataflow, one layer after the other; 2 pipelined
  * kernel, neighbouring layers overlapped; 1 pipelined kernel, sequential.  Sources: Pulsar
  * README, "How the streaming works" (the next layer's experts are fetched

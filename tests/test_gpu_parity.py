@@ -411,14 +411,14 @@ def test_stack_forward_independent_layers_pipelined(moe, fmt, route, S, T, L):
             assert_close_rows(outs[l].cpu().numpy(), ref, f"layer {l}")
 
 
-@pytest.mark.parametrize("chained", [False, True])
-def test_stack_forward_heavy_layers_pipelined_kernel(moe, chained):
-    """Layers with many expert items per SM (8 tokens, 1024-wide experts) run
-    on the barrier-pipelined kernel; every layer must match the oracle."""
+@pytest.mark.parametrize("chained,L", [(False, 3), (True, 2), (False, 5)])
+def test_stack_forward_heavy_layers(moe, chained, L):
+    """Layers with many expert items per SM (8 tokens, 1024-wide experts):
+    short stacks run on the barrier-pipelined kernel, stacks of 4 or more
+    layers on the dataflow kernel; every layer must match the oracle."""
     # chained: each layer scales the activations up by orders of magnitude at this
     # shape, so two layers (a third would overflow fp32 in the oracle as well)
     fmt, route, H, I, E, k, S, T = FMT_Q4K, 0, 2048, 1024, 64, 8, 1, 8
-    L = 2 if chained else 3
     ex = [_experts_host(fmt, E + S, H, I, seed=90 + l, layer=l) for l in range(L)]
     tables = [moe.expert_table([tuple(dev(m) for m in e) for e in ex[l]]) for l in range(L)]
     wrs = [synth.router_weight(E, H, 90, l) for l in range(L)]
@@ -433,7 +433,7 @@ def test_stack_forward_heavy_layers_pipelined_kernel(moe, chained):
     moe.moe_stack_forward(desc, moe.stack_pointer_table(rows), T, ws)
     assert moe.moe_get_status(ws) == 0
     marker = moe.MoeLayer.ws_view_of(ws, moe.moe_workspace_layout(desc), "phase_ns", torch.int64, (16,))
-    assert int(marker[15]) == (1 if chained else 2)
+    assert int(marker[15]) == (3 if L >= 4 else 1 if chained else 2)
     for l in range(L):
         xin = xs[l].cpu().numpy()
         gids = ids[l].cpu().numpy()
