@@ -1373,6 +1373,84 @@ __device__ __forceinline__ void sb_accum_staged(const uint8_t* slab, const int8_
   }
 }
 
+// sb_accum_staged of the gate and the up slab of one pair at once: the same
+// sums in the same order per matrix, with each token's activation words and
+// 16-sums read once for both
+template <int FMT>
+__device__ __forceinline__ void sb_accum_pair_staged(const uint8_t* sg, const uint8_t* su, const int8_t* act,
+                                                     const int16_t* bs, const float* d, const int* act_off, int b,
+                                                     int cnt, float* accg, float* accu, int lane) {
+  using F = Fmt<FMT>;
+  SbRegs<FMT> g, u;  // scale/min words and d|dmin only
+  g.dm = *reinterpret_cast<const uint32_t*>(sg + 4 * lane);
+  u.dm = *reinterpret_cast<const uint32_t*>(su + 4 * lane);
+  if constexpr (FMT == kQ4K) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) {
+      g.sm[i] = *reinterpret_cast<const uint32_t*>(sg + F::kSmOff + 12 * lane + 4 * i);
+      u.sm[i] = *reinterpret_cast<const uint32_t*>(su + F::kSmOff + 12 * lane + 4 * i);
+    }
+  } else {
+    const uint4 vg = *reinterpret_cast<const uint4*>(sg + F::kSmOff + 16 * lane);
+    const uint4 vu = *reinterpret_cast<const uint4*>(su + F::kSmOff + 16 * lane);
+    g.sm[0] = vg.x; g.sm[1] = vg.y; g.sm[2] = vg.z; g.sm[3] = vg.w;
+    u.sm[0] = vu.x; u.sm[1] = vu.y; u.sm[2] = vu.z; u.sm[3] = vu.w;
+  }
+  int scg[F::kNSub], mng[F::kNSub], scu[F::kNSub], mnu[F::kNSub];
+#pragma unroll
+  for (int j = 0; j < F::kNSub; ++j) {
+    sb_scale_min<FMT>(g, j, scg[j], mng[j]);
+    sb_scale_min<FMT>(u, j, scu[j], mnu[j]);
+  }
+  const float dwg = half_lo(g.dm), dming = half_hi(g.dm), dwu = half_lo(u.dm), dminu = half_hi(u.dm);
+  const uint8_t* cg = sg + F::kCodeOff + 16 * lane;
+  const uint8_t* cu = su + F::kCodeOff + 16 * lane;
+#pragma unroll 1
+  for (int t = 0; t < cnt; ++t) {
+    const int o = act_off[t];
+    const int8_t* a = act + o + 256 * b;
+    const int16_t* bsp = bs + o / 16 + 16 * b;
+    int Sg = 0, Mg = 0, Su = 0, Mu = 0;
+    if constexpr (FMT == kQ4K) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int4 alo = *reinterpret_cast<const int4*>(a + 32 * j);
+        const int4 ahi = *reinterpret_cast<const int4*>(a + 32 * j + 16);
+        const int bsum = (int)bsp[2 * j] + (int)bsp[2 * j + 1];
+        uint32_t lo[4], hi[4];
+        mask_q4k(*reinterpret_cast<const uint4*>(cg + 512 * j), lo, hi);
+        Sg += scg[j] * isum_q4k(lo, hi, alo, ahi);
+        Mg += mng[j] * bsum;
+        mask_q4k(*reinterpret_cast<const uint4*>(cu + 512 * j), lo, hi);
+        Su += scu[j] * isum_q4k(lo, hi, alo, ahi);
+        Mu += mnu[j] * bsum;
+      }
+    } else {
+#pragma unroll
+      for (int ln = 0; ln < 4; ++ln) {
+        const uint4 lg = *reinterpret_cast<const uint4*>(cg + 512 * ln);
+        const uint4 lu = *reinterpret_cast<const uint4*>(cu + 512 * ln);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) {
+          const int j = 4 * ln + jj;
+          const int4 av = *reinterpret_cast<const int4*>(a + 16 * j);
+          const int bsum = (int)bsp[j];
+          uint32_t w[4];
+          mask_q2k(lg, j, w);
+          Sg += scg[j] * isum_q2k(w, av);
+          Mg += mng[j] * bsum;
+          mask_q2k(lu, j, w);
+          Su += scu[j] * isum_q2k(w, av);
+          Mu += mnu[j] * bsum;
+        }
+      }
+    }
+    const float da = d[o / 256 + b];
+    accg[t * 32 + lane] += da * fmaf(dwg, (float)Sg, -dming * (float)Mg);
+    accu[t * 32 + lane] += da * fmaf(dwu, (float)Su, -dminu * (float)Mu);
+  }
+}
+
 // ---- staged gate/up and down items -------------------------------------------
 // Each warp streams its super-block rows of the item through its own ring of
 // two shared-memory stages with cp.async (16 bytes per lane per
@@ -1475,8 +1553,8 @@ __device__ void stack_gateup_ring(Ctx<FMT>& c, const LayerView& lv, int l, int i
     const int p = warp + kDecWarps * j;
     const int rgl = p / nbH, b = p % nbH;
     float* acc = accw + (size_t)rgl * 2 * T * 32;
-    sb_accum_staged<FMT>(st, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc, lane);
-    sb_accum_staged<FMT>(st + F::kSlabBytes, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc + T * 32, lane);
+    sb_accum_pair_staged<FMT>(st, st + F::kSlabBytes, sm.xq, sm.xbs, sm.xd, sm.aoff, b, tl.count, acc,
+                              acc + T * 32, lane);
     rg.give();
     if (j + kRingStages < nu) issue(j + kRingStages);
   }
