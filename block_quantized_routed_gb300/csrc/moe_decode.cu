@@ -843,8 +843,8 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
 // per-layer counters instead of grid barriers.  Item kinds of layer l:
 //   R   8 router rows (one warp each), part of q8_K(x_l)       -> logits_l
 //   Q   top-k, bucketing, tile plan                            -> route_l
-//   GU  (tile, 32-row group) of gate and up, SwiGLU            -> h_l
-//   D   (tile, 8 row groups) of down, on q8_K(h) of the tile   -> y_l by slot
+//   GU  (tile, gpi 32-row groups) of gate and up, SwiGLU       -> h_l
+//   D   (tile, 8 dpi row groups) of down, on q8_K(h) of the tile -> y_l by slot
 //   C   a chunk of out_l = residual + sum gate * y (fixed order)
 // An item waits (bounded) for the counters of what it reads: Q for all R of
 // its layer, GU for Q, D for the GU items of its tile, C for all D; in a
@@ -864,6 +864,12 @@ __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __gr
 // it waits for), so several layers overlap with no grid barrier; otherwise
 // layer by layer.  Each layer owns its buffers, so no
 // layer's data is overwritten while another still reads it.
+// Counters are incremented with a release pattern (barrier, acq_rel fence,
+// relaxed add) and read with ld.acquire.  Where shared memory allows
+// (kRing), each warp streams its gate/up and down super-block rows through
+// a two-stage cp.async ring and the item's small reads are issued ahead of
+// that stream; otherwise the rows are loaded into registers and thread 32
+// prefetches the CTA's next item towards L2 while thread 0 waits.
 constexpr int kRouterRows = kDecWarps;  // router rows per R item
 constexpr int kCombineVec = 1024;       // float4 elements per C item
 constexpr int kDownRG = kDecWarps;      // row groups per D item (one per warp)
