@@ -24,6 +24,7 @@ __all__ = [
     "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "moe_stack_workspace_size", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
     "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
+    "moe_stack_kernel", "STACK_PIPELINED", "STACK_DATAFLOW",
 ]
 
 FMT_Q4K = 0
@@ -36,6 +37,9 @@ N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16}
 PATH_DECODE_FUSED = 0
 PATH_GEMV = 1
 PATH_TENSOR_PREFILL = 2
+
+STACK_PIPELINED = 1
+STACK_DATAFLOW = 2
 
 MOE_OK = 0
 MOE_ERR_INVALID_ARG = -1
@@ -104,6 +108,7 @@ def load():
         "moe_last_cuda_error": (ctypes.c_int, []),
         "moe_debug_wait_timeout": (ctypes.c_int, [P, I32, P]),
         "moe_layer_path": (ctypes.c_int, [D, I32]),
+        "moe_stack_kernel": (ctypes.c_int, [D, I32, I32, I32]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -281,6 +286,14 @@ def moe_layer_path(desc, T) -> int:
     rc = int(load().moe_layer_path(ctypes.byref(_desc(desc)), T))
     if rc < 0:
         raise MoeError(rc, "moe_layer_path")
+    return rc
+
+
+def moe_stack_kernel(desc, n_layers, T, n_sms=0) -> int:
+    """Which single-launch kernel moe_stack_forward takes (STACK_DATAFLOW or STACK_PIPELINED)."""
+    rc = int(load().moe_stack_kernel(ctypes.byref(_desc(desc)), n_layers, T, n_sms))
+    if rc < 0:
+        raise MoeError(rc, "moe_stack_kernel")
     return rc
 
 

@@ -134,14 +134,23 @@ void note_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 // item sizes as decode_stack_kernel chooses).
 constexpr int kFlowMinLayers = 4;  // heavy layers take the dataflow kernel from this many layers on
 
-double stack_items_per_sm(const moe_layer_desc& d, int T) {
+double stack_items_per_sm(const moe_layer_desc& d, int T, int sms) {
   const int nbH = d.H / 256, nbI = d.I / 256, nRG = d.I / 32, nRGH = d.H / 32;
   const int Tm = T > 16 ? T : 16;
   const int gpi = std::max(1, std::min(16 / nbH, Tm / T));
   const int dpi = nbI <= 2 ? 2 : 1;
   const double P = (double)T * (d.top_k + d.n_shared);
   const double items = P * ((nRG + gpi - 1) / gpi) + P * ((nRGH + 8 * dpi - 1) / (8 * dpi));
-  return items / num_sms();
+  return items / (sms > 0 ? sms : num_sms());
+}
+
+// Short stacks of layers with many expert items per CTA (a wide layer on
+// its own) run faster on the barrier-pipelined kernel, whose CTAs prefetch
+// all of their items of a layer at once; small layers, and heavy layers
+// with enough neighbours to overlap (measured: a 48-layer verify stack),
+// run as the dataflow of items.
+bool stack_takes_pipelined(const moe_layer_desc& d, int n_layers, int T, int sms) {
+  return stack_items_per_sm(d, T, sms) > 2.0 && n_layers < kFlowMinLayers;
 }
 
 void trace_record(cudaStream_t s) {
@@ -487,12 +496,7 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
   if (ws_bytes < ext + sp.total) return MOE_ERR_WORKSPACE;
   char* base = static_cast<char*>(ws);
   auto at = [&](size_t off) { return static_cast<void*>(base + off); };
-  // Short stacks of layers with many expert items per CTA (a wide layer on
-  // its own) run faster on the barrier-pipelined kernel, whose CTAs
-  // prefetch all of their items of a layer at once; small layers, and heavy
-  // layers with enough neighbours to overlap (measured: a 48-layer verify
-  // stack), run as the dataflow of items.
-  if (stack_items_per_sm(*desc, T) > 2.0 && n_layers < kFlowMinLayers) {
+  if (stack_takes_pipelined(*desc, n_layers, T, 0)) {
     DecodeArgs d{};
     d.fmt = desc->fmt;
     d.H = H;
@@ -619,6 +623,17 @@ int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
       decode_smem_bytes(T, desc->H, desc->I, desc->E, k, desc->n_shared) <= kDecodeSmemMax)
     return MOE_PATH_DECODE_FUSED;
   return prefill_path(T, k, desc->E) && prefill_fits(desc->T_max, *desc) ? MOE_PATH_TENSOR_PREFILL : MOE_PATH_GEMV;
+}
+
+int moe_stack_kernel(const moe_layer_desc* desc, int32_t n_layers, int32_t T, int32_t n_sms) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (n_layers < 1 || T < 1 || T > desc->T_max) return MOE_ERR_INVALID_ARG;
+  const int k = desc->top_k;
+  if (T > kDecodeMaxT || (int64_t)T * k > kSmallPairs ||
+      decode_smem_bytes(T, desc->H, desc->I, desc->E, k, desc->n_shared) > kDecodeSmemMax)
+    return MOE_ERR_UNSUPPORTED;
+  return stack_takes_pipelined(*desc, n_layers, T, n_sms) ? MOE_STACK_PIPELINED : MOE_STACK_DATAFLOW;
 }
 
 int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }

@@ -110,7 +110,8 @@ struct StackPlan {
 constexpr int kStackCnt = 4;  // router items, routing, down items, combine items (then one per tile)
 StackPlan stack_plan(const moe_layer_desc& d, int n_layers);
 // gate/up + down items of one stack layer per SM (decides which stack kernel runs)
-double stack_items_per_sm(const moe_layer_desc& d, int T);
+double stack_items_per_sm(const moe_layer_desc& d, int T, int sms);  // sms <= 0: the current device's
+bool stack_takes_pipelined(const moe_layer_desc& d, int n_layers, int T, int sms);
 
 // Single-launch decode layer (cooperative kernel); see moe_decode.cu.
 struct DecodeArgs {

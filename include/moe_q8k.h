@@ -336,6 +336,20 @@ unsigned long long moe_kernel_launch_count(void);
 #define MOE_PATH_TENSOR_PREFILL 2
 int moe_layer_path(const moe_layer_desc* desc, int32_t T);
 
+/* Which single-launch kernel moe_stack_forward runs for a stack of n_layers
+ * layers of `desc` at T tokens on a device with n_sms SMs (n_sms <= 0: the
+ * current device's).  Host-side only; launches nothing:
+ *   MOE_STACK_DATAFLOW   the layers as a dataflow of small items ordered by
+ *                        per-layer counters (phase_ns[15] = 3 or 4)
+ *   MOE_STACK_PIPELINED  the barrier-pipelined kernel (phase_ns[15] = 1 or 2):
+ *                        layers with more than 2 gate/up + down items per SM
+ *                        in stacks of fewer than 4 layers
+ * Returns one of them, MOE_ERR_UNSUPPORTED for shapes moe_stack_forward
+ * rejects, or MOE_ERR_INVALID_ARG.  No counterpart on the pages. */
+#define MOE_STACK_PIPELINED 1
+#define MOE_STACK_DATAFLOW 2
+int moe_stack_kernel(const moe_layer_desc* desc, int32_t n_layers, int32_t T, int32_t n_sms);
+
 /* Test hook for failure detection: one kernel waits on a word of the
  * workspace's status block for a value nothing ever writes, with the same
  * kind of bound as every wait in the library's kernels; after limit_us

@@ -105,6 +105,33 @@ def test_host_validation_rejects_before_launch(lib):
     assert moe.moe_expert_ffn_workspace_size(d, 5) == 0
 
 
+def test_stack_kernel_selection(lib):
+    """moe_stack_forward's choice of single-launch kernel (host logic), on a
+    152-SM device: layers with at most 2 gate/up + down items per SM, and
+    heavier layers in stacks of 4 or more, take the dataflow kernel; heavy
+    layers in shorter stacks the barrier-pipelined one."""
+    dec = desc(H=2048, I=512, E=256, top_k=8, n_shared=1, T_max=1)          # 0.7 items per SM
+    assert moe.moe_stack_kernel(dec, 40, 1, 152) == moe.STACK_DATAFLOW
+    assert moe.moe_stack_kernel(dec, 1, 1, 152) == moe.STACK_DATAFLOW
+    ver = desc(H=4096, I=1024, E=512, top_k=10, n_shared=1, route=1, fmt=1, T_max=4)  # 13.9 per SM
+    assert moe.moe_stack_kernel(ver, 48, 4, 152) == moe.STACK_DATAFLOW
+    assert moe.moe_stack_kernel(ver, 3, 4, 152) == moe.STACK_PIPELINED
+    wide = desc(H=6144, I=2048, E=192, top_k=8, n_shared=0, T_max=16)     # 4.6 per SM at T = 1
+    assert moe.moe_stack_kernel(wide, 1, 1, 152) == moe.STACK_PIPELINED
+    assert moe.moe_stack_kernel(wide, 4, 1, 152) == moe.STACK_DATAFLOW
+    heavy = desc(H=2048, I=1024, E=64, top_k=8, n_shared=1, T_max=8)      # the GPU test's heavy stack
+    assert moe.moe_stack_kernel(heavy, 3, 8, 152) == moe.STACK_PIPELINED
+    assert moe.moe_stack_kernel(heavy, 5, 8, 152) == moe.STACK_DATAFLOW
+    # the same 0.7-items layer on a 32-SM part: 3.4 per SM
+    assert moe.moe_stack_kernel(dec, 2, 1, 32) == moe.STACK_PIPELINED
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_stack_kernel(desc(H=512, I=256, E=16, top_k=2, T_max=32), 2, 17, 152)   # beyond 16 tokens
+    assert e.value.status == moe.MOE_ERR_UNSUPPORTED
+    with pytest.raises(moe.MoeError) as e:
+        moe.moe_stack_kernel(dec, 0, 1, 152)
+    assert e.value.status == moe.MOE_ERR_INVALID_ARG
+
+
 def test_layer_path_selection(lib):
     assert moe.moe_layer_path(desc(), 1) == moe.PATH_DECODE_FUSED
     # 40 tokens x 10 of 40 experts: 400 pairs, 10 per expert -> GEMV kernels
