@@ -1488,6 +1488,8 @@ struct WarpRing {
     ++issued;
   }
   // the oldest unit not yet taken, once this warp's copies of it landed
+  // (at most kRingStages = 2 units are issued and not taken)
+  static_assert(kRingStages == 2, "take() waits with wait_group 1 / 0");
   __device__ const uint8_t* take() {
     if (issued - taken > 1) asm volatile("cp.async.wait_group 1;" ::: "memory");
     else asm volatile("cp.async.wait_group 0;" ::: "memory");
