@@ -65,25 +65,35 @@ __device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
   asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
-// Grid-wide barrier on a monotonic 64-bit counter: arrivals are grouped in
-// generations of gridDim.x.  Returns false if the wait ran out.
+// Grid-wide barrier on one 64-bit word: the arrival count in the low 32
+// bits, a generation number in the high 32 bits.  The CTA that arrives last
+// sets the count back to zero and advances the generation in one atomic
+// store; the others wait (bounded) for the generation to change.  Every
+// completed barrier leaves the count at zero, so a launch does not depend
+// on the grid size of the launch before it on the same workspace.  Returns
+// false if the wait ran out (the count is then left partial; the status
+// read that reports the timeout clears the word).
 __device__ bool grid_barrier(unsigned long long* bar, int* status) {
   __shared__ int s_ok;
   __syncthreads();
   if (threadIdx.x == 0) {
     __threadfence();
-    const unsigned long long n = gridDim.x;
     const unsigned long long old = atomicAdd(bar, 1ull);
-    const unsigned long long target = (old / n + 1ull) * n;
+    const unsigned gen = (unsigned)(old >> 32);
     int ok = 1;
-    long long spins = 0;
-    while (ld_acquire_u64(bar) < target) {
-      if (++spins > kSpinLimit) {
-        set_status(status, MOE_ERR_DEVICE_TIMEOUT);
-        ok = 0;
-        break;
+    if ((unsigned)(old & 0xFFFFFFFFull) == gridDim.x - 1u) {
+      __threadfence();  // every other CTA's arrival (and its writes) is seen before the release
+      atomicExch(bar, (unsigned long long)(gen + 1u) << 32);
+    } else {
+      long long spins = 0;
+      while ((unsigned)(ld_acquire_u64(bar) >> 32) == gen) {
+        if (++spins > kSpinLimit) {
+          set_status(status, MOE_ERR_DEVICE_TIMEOUT);
+          ok = 0;
+          break;
+        }
+        __nanosleep(64);
       }
-      __nanosleep(64);
     }
     __threadfence();
     s_ok = ok;
@@ -127,17 +137,31 @@ __host__ __device__ inline size_t route_bytes(int T, int k, int S) {
   return al16((size_t)T * k * 4) * 2 + al16(P * 4) * 2 + al16(P * sizeof(Tile)) + al16((size_t)T * k + S) + 16;
 }
 
-__device__ __forceinline__ Route route_at(uint8_t* base, int T, int k, int S) {
+// byte offsets of the fields of one routing state (host and device agree on it)
+__host__ __device__ inline RouteFields route_fields_of(int T, int k, int S) {
   const size_t P = (size_t)T * (k + S);
+  RouteFields f;
+  size_t o = 0;
+  f.ids = o;     o += al16((size_t)T * k * 4);
+  f.gates = o;   o += al16((size_t)T * k * 4);
+  f.tok = o;     o += al16(P * 4);
+  f.slot = o;    o += al16(P * 4);
+  f.tiles = o;   o += al16(P * sizeof(Tile));
+  f.ok = o;      o += al16((size_t)T * k + S);
+  f.n_tiles = o;
+  return f;
+}
+
+__device__ __forceinline__ Route route_at(uint8_t* base, int T, int k, int S) {
+  const RouteFields f = route_fields_of(T, k, S);
   Route r;
-  uint8_t* p = base;
-  r.ids = reinterpret_cast<int*>(p);      p += al16((size_t)T * k * 4);
-  r.gates = reinterpret_cast<float*>(p);  p += al16((size_t)T * k * 4);
-  r.tok = reinterpret_cast<int*>(p);      p += al16(P * 4);
-  r.slot = reinterpret_cast<int*>(p);     p += al16(P * 4);
-  r.tiles = reinterpret_cast<Tile*>(p);   p += al16(P * sizeof(Tile));
-  r.ok = p;                               p += al16((size_t)T * k + S);
-  r.n_tiles = reinterpret_cast<int*>(p);
+  r.ids = reinterpret_cast<int*>(base + f.ids);
+  r.gates = reinterpret_cast<float*>(base + f.gates);
+  r.tok = reinterpret_cast<int*>(base + f.tok);
+  r.slot = reinterpret_cast<int*>(base + f.slot);
+  r.tiles = reinterpret_cast<Tile*>(base + f.tiles);
+  r.ok = base + f.ok;
+  r.n_tiles = reinterpret_cast<int*>(base + f.n_tiles);
   return r;
 }
 
@@ -1904,6 +1928,8 @@ cudaError_t launch_decode_t(const DecodeArgs& a, cudaStream_t s) {
 }  // namespace
 
 size_t decode_route_bytes(int T, int k, int S) { return route_bytes(T, k, S); }
+
+RouteFields route_fields(int T, int k, int S) { return route_fields_of(T, k, S); }
 
 size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S) {
   return decode_smem(T, H, I, E, k, S, nullptr, nullptr);
