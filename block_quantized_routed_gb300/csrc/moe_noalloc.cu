@@ -13,10 +13,12 @@
 // The scratch is a file-scope __device__ array of kNoAllocScratchBytes.  The
 // CUDA runtime creates it on every device that loads this library and keeps
 // it until the process exits.  Host code cannot use the array's name as a
-// device address, so the first call on each device looks the address up
-// with cudaGetSymbolAddress (with that device current) and caches it.
+// device address, so every call looks the address up with
+// cudaGetSymbolAddress in the context current on the calling thread: a
+// host-side lookup that allocates nothing, and that stays right for callers
+// that run the layer in a context of their own or reset the device between
+// calls (a cached address would belong to the context it was taken in).
 #include <cstdint>
-#include <mutex>
 
 #include "moe_internal.h"
 
@@ -25,27 +27,15 @@ namespace {
 
 // Largest workspace (moe_layer_workspace_size) this entry point can serve.
 constexpr size_t kNoAllocScratchBytes = MOE_NOALLOC_MAX_WORKSPACE;  // 16 MiB
-constexpr int kMaxDevices = 64;
 
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-std::mutex g_scratch_mu;
-void* g_scratch_ptr[kMaxDevices] = {};
-
-// Device address of the scratch array on the current device (looked up once per device).
+// Device address of the scratch array in the calling thread's current context.
 cudaError_t scratch_address(void** out) {
-  int dev = 0;
-  cudaError_t err = cudaGetDevice(&dev);
+  void* p = nullptr;
+  const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
   if (err != cudaSuccess) return err;
-  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  std::lock_guard<std::mutex> lock(g_scratch_mu);
-  if (!g_scratch_ptr[dev]) {
-    void* p = nullptr;
-    err = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (err != cudaSuccess) return err;
-    g_scratch_ptr[dev] = p;
-  }
-  *out = g_scratch_ptr[dev];
+  *out = p;
   return cudaSuccess;
 }
 

@@ -18,8 +18,12 @@ torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
 
 
+# the first two shapes take the single-launch decode kernel; the third
+# (T*k = 320 > 256 pairs) the multi-kernel route/bucket/GEMV path, whose tile
+# count and arrival counters also live in the shared array
 @pytest.mark.parametrize("fmt,route,H,I,E,k,S,T", [(FMT_Q4K, 0, 2048, 512, 64, 8, 1, 1),
-                                                   (FMT_Q2K, 1, 1024, 512, 32, 4, 1, 4)])
+                                                   (FMT_Q2K, 1, 1024, 512, 32, 4, 1, 4),
+                                                   (FMT_Q4K, 0, 1024, 256, 32, 8, 1, 40)])
 def test_noalloc_matches_workspace_entry_point_twice(fmt, route, H, I, E, k, S, T):
     import block_quantized_routed_gb300 as moe
     moe.load()
@@ -31,6 +35,8 @@ def test_noalloc_matches_workspace_entry_point_twice(fmt, route, H, I, E, k, S, 
     wr = dev(synth.router_weight(E, H, seed))
     desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
     assert moe.moe_layer_workspace_size(desc) <= 16 << 20
+    if T * k > 256:
+        assert moe.moe_layer_path(desc, T) == moe.PATH_GEMV
     layer = moe.MoeLayer(desc, table, wr)
     for rep in range(2):                      # two calls in a row: the shared scratch is reused
         x = dev(synth.activations(T, H, seed, rep=rep))
