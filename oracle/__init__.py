@@ -66,6 +66,8 @@ def _load():
             lib.orc_subblock_dots.restype = None
             lib.orc_qmatvec.argtypes = [P, I, I64, I64, P, P, I64, P, I]
             lib.orc_qmatvec.restype = None
+            lib.orc_qmatvec_absterms.argtypes = [P, I, I64, I64, P, P, I64, P, I]
+            lib.orc_qmatvec_absterms.restype = None
             lib.orc_route.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, P, P, P]
             lib.orc_route.restype = None
             lib.orc_bucket.argtypes = [P, I64, I64, I64, I64, P, P, P]
@@ -149,6 +151,19 @@ def qmatvec(w: np.ndarray, fmt: int, N: int, K: int, qa: np.ndarray, da: np.ndar
     y = np.zeros((T, N), np.float64)
     _load().orc_qmatvec(_p(w), fmt, N, K, _p(qa), _p(da), T, _p(y), nthreads or default_threads())
     return y
+
+
+def qmatvec_absterms(w: np.ndarray, fmt: int, N: int, K: int, qa: np.ndarray, da: np.ndarray,
+                     nthreads: int | None = None) -> np.ndarray:
+    """a [T, N]: the sum of the magnitudes of the super-block terms that
+    qmatvec adds into each output (|qmatvec| <= a), for error bounds."""
+    w = _c(w, np.uint8)
+    qa = _c(qa, np.int8)
+    da = _c(da, np.float32)
+    T = qa.shape[0]
+    a = np.zeros((T, N), np.float64)
+    _load().orc_qmatvec_absterms(_p(w), fmt, N, K, _p(qa), _p(da), T, _p(a), nthreads or default_threads())
+    return a
 
 
 def route(x, wr, bias, k: int, route_kind: int, forced_ids=None):

@@ -293,6 +293,41 @@ void orc_qmatvec(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* 
   });
 }
 
+// Magnitude of the terms that orc_qmatvec sums into y[t][n], for
+// floating-point error bounds of an implementation that sums them in fp32:
+//   a[t][n] = sum_b |da[b]| * (|d_w| * |S_b| + |dmin| * |M_b|),
+// S_b = sum_j sc_j * isum_j and M_b = sum_j mn_j * bsum_j of super-block b
+// (the integer sums of row_dot).  |y[t][n]| <= a[t][n], with equality when
+// no term cancels another.
+void orc_qmatvec_absterms(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, const float* da,
+                          int64_t T, double* a, int nthreads) {
+  int64_t nb = K / 256;
+  int ns = n_sub(fmt), sl = sub_len(fmt);
+  parallel_for(N, nthreads, [&](int64_t n) {
+    SuperBlock sb;
+    for (int64_t t = 0; t < T; ++t) {
+      const int8_t* q = qa + t * K;
+      double acc = 0.0;
+      for (int64_t b = 0; b < nb; ++b) {
+        unpack_sb(w, fmt, nb, n, b, &sb);
+        int64_t S = 0, M = 0;
+        for (int j = 0; j < ns; ++j) {
+          int64_t isum = 0, bsum = 0;
+          for (int i = 0; i < sl; ++i) {
+            isum += (int64_t)sb.q[j * sl + i] * q[256 * b + j * sl + i];
+            bsum += q[256 * b + j * sl + i];
+          }
+          S += (int64_t)sb.sc[j] * isum;
+          M += (int64_t)sb.mn[j] * bsum;
+        }
+        acc += std::fabs((double)da[t * nb + b]) *
+               (std::fabs(sb.d) * std::fabs((double)S) + std::fabs(sb.dmin) * std::fabs((double)M));
+      }
+      a[t * N + n] = acc;
+    }
+  });
+}
+
 // Router: logits[t][e] = sum_h W_r[e][h] * x[t][h] (+ bias[e]) in fp64 from
 // the fp32 inputs.  Top-k by a full stable sort on descending logit (equal
 // logits: lower expert index first).  Gates renormalised over the k:

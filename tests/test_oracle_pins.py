@@ -168,6 +168,47 @@ def test_extreme_codes_stay_exact():
     assert (y == 1.0 * (1.0 * S - 0.5 * M)).all()
 
 
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+def test_absterms_from_fields_brute_force(fmt):
+    """qmatvec_absterms = sum over super-blocks of |d_a| (|d| |S_b| + |dmin| |M_b|), with S_b and M_b
+    recomputed here from the encoded fields by plain loops; and it bounds |qmatvec| (triangle inequality)."""
+    rng = np.random.default_rng(51 + fmt)
+    N, K, T = 256, 768, 2
+    q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    xq, xd, _ = oracle.q8k_quantize(x)
+    a = oracle.qmatvec_absterms(w, fmt, N, K, xq, xd)
+    sl = 32 if fmt == FMT_Q4K else 16
+    ns = 256 // sl
+    want = np.zeros((T, N))
+    for t in range(T):
+        for n in range(N):
+            for b in range(K // 256):
+                qa = xq[t, 256 * b:256 * b + 256].astype(np.int64).reshape(ns, sl)
+                qw = np.asarray(q[n, b], np.int64).reshape(ns, sl)
+                S = int((sc[n, b] * (qw * qa).sum(axis=1)).sum())
+                M = int((mn[n, b] * qa.sum(axis=1)).sum())
+                want[t, n] += abs(float(xd[t, b])) * (abs(float(d[n, b])) * abs(S) + abs(float(dmin[n, b])) * abs(M))
+    np.testing.assert_allclose(a, want, rtol=1e-13)
+    y = oracle.qmatvec(w, fmt, N, K, xq, xd)
+    assert (np.abs(y) <= a * (1 + 1e-12)).all()
+    assert (a > np.abs(y)).any()                          # random signs do cancel somewhere
+
+
+def test_absterms_equal_output_when_nothing_cancels():
+    """dmin = 0 and non-negative activations: every term is >= 0, so the magnitude sum is the output."""
+    fmt = FMT_Q4K
+    rng = np.random.default_rng(61)
+    N, K = 256, 512
+    q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
+    dmin[:] = 0
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
+    x = np.abs(rng.standard_normal((3, K))).astype(np.float32)
+    xq, xd, _ = oracle.q8k_quantize(x)
+    np.testing.assert_array_equal(oracle.qmatvec_absterms(w, fmt, N, K, xq, xd), oracle.qmatvec(w, fmt, N, K, xq, xd))
+
+
 # ---------------------------------------------------------------- routing
 
 @pytest.mark.parametrize("case", _load("route_cases.json")["cases"], ids=lambda c: c["name"][:40])
