@@ -54,9 +54,12 @@ def parse_args():
     ap.add_argument("--rotations", type=int, default=16, help="distinct input sets cycled through the steps")
     ap.add_argument("--no-graph", action="store_true", help="launch eagerly instead of replaying a CUDA graph")
     ap.add_argument("--chained", action="store_true",
-                    help="layer l reads layer l-1's output (a decode step through the stack) instead of its own input")
+                    help="the chained order of a decode step: layers 1, L/2 and L-1 read the previous layer's "
+                         "output, which makes the kernel run every layer after the one before it")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget-s", type=float, default=12.0)
+    ap.add_argument("--ref-budget-s", type=float, default=100.0,
+                    help="oracle seconds the reference arm spends in its timed steps")
     return ap.parse_args()
 
 
@@ -201,6 +204,18 @@ def host_inputs(wl, T, R):
                      for r in range(R)])
 
 
+def chain_links(L):
+    """Layers that read the previous layer's output in the chained order.
+
+    Any one such link makes the stack kernel run every layer after the one
+    before it (the order of a decode step through the stack), so the timing
+    is that of a full chain.  The links are few because these synthetic
+    weights have a non-zero mean: with residual = x, a deeper chain of real
+    data grows past fp32 within about four layers, after which the routing
+    of NaN logits degenerates to experts 0..k-1 (an unrealistic workload)."""
+    return sorted({1, L // 2, L - 1}) if L > 1 else []
+
+
 # ----------------------------------------------------------------------------- CPU oracle
 
 # Tokens are independent through a layer (routing, expert FFNs and combine
@@ -242,22 +257,25 @@ def oracle_layers(wl, T, x_rl, layers, nthreads, tokens=None):
     return outs, spent
 
 
-def cpu_baseline(wl, T, x_host, budget_s):
-    import oracle
-    nthreads = oracle.default_threads()
-    tokens = token_sample(T)
-    done, spent = 0, 0.0
-    layers = []
-    while spent < budget_s and done < wl.layers * 64:
-        l = done % wl.layers
-        _, s = oracle_layers(wl, T, x_host[0], [l], nthreads, tokens)
-        spent += s
-        layers.append(l)
-        done += 1
-    tok_s = (done / wl.layers) * len(tokens) / spent
-    return {"value": tok_s, "unit": "tokens/s", "cores": nthreads, "kind": "oracle",
-            "sample": f"{done} of {wl.layers} layers x {len(tokens)} of {T} token(s) of rotation 0 "
-                      f"({spent:.1f} s of oracle time); tokens/s = layers done / layers per step * tokens / seconds"}
+def cpu_baseline(args, wl, T, budget_s):
+    """The oracle timed the way the reference arm times it, in a fresh process
+    (no CUDA context, no GPU-side threads), so both report one measurement."""
+    cmd = [sys.executable, os.path.abspath(__file__), "--impl", "reference", "--workload", args.workload,
+           "--steps", "3", "--warmup", "1", "--ref-budget-s", str(budget_s)]
+    if args.T:
+        cmd += ["--T", str(args.T)]
+    if args.layers:
+        cmd += ["--layers", str(args.layers)]
+    env = {k_: v for k_, v in os.environ.items() if k_ not in ("RANK", "WORLD_SIZE", "LOCAL_RANK")}
+    r = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=max(120.0, 6 * budget_s))
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    if r.returncode != 0 or not lines:
+        return {"value": None, "unit": "tokens/s", "kind": "oracle", "error": (r.stderr or "")[-300:]}
+    ref = json.loads(lines[-1])
+    cb = dict(ref["cpu_baseline"])
+    cb["value"] = ref["value"]
+    cb["how"] = "bench.py --impl reference in a child process (" + " ".join(cmd[2:]) + ")"
+    return cb
 
 
 # ----------------------------------------------------------------------------- reference arm
@@ -273,9 +291,9 @@ def run_reference(args, wl, T):
     x_host = host_inputs(wl, T, 1)
     nthreads = oracle.default_threads()
     tokens = token_sample(T)
-    # size each step's sample so that the whole run stays within ~2 minutes
+    # size each step's sample so that the timed steps take about --ref-budget-s
     _, t_layer = oracle_layers(wl, T, x_host[0], [0], nthreads, tokens)
-    per_step = max(1, min(wl.layers, int(120.0 / max(K + W, 1) / max(t_layer, 1e-3))))
+    per_step = max(1, min(wl.layers * 16, int(args.ref_budget_s / max(K, 1) / max(t_layer, 1e-3))))
     for i in range(W):
         oracle_layers(wl, T, x_host[0], [(i * per_step + j) % wl.layers for j in range(per_step)], nthreads, tokens)
     spent = 0.0
@@ -290,11 +308,98 @@ def run_reference(args, wl, T):
         "vs_baseline": None, "dtype": "f64 (int64 sub-block sums)", "data": "synthetic",
         "config": {"workload": wl.name, "layers": wl.layers, "T": T, "sample_layers_per_step": per_step},
         "cpu_baseline": {"kind": "oracle", "cores": nthreads, "value": tok_s, "unit": "tokens/s",
-                         "sample": f"{per_step} of {wl.layers} layers per step, {len(tokens)} of {T} token(s) "
-                                   f"per layer"},
+                         "threads": f"{nthreads} std::thread workers per parallel loop (rows or tokens), "
+                                    f"not pinned; host cores {os.cpu_count()}",
+                         "sample": f"{per_step} layer evaluations per step (layers cycled over the {wl.layers} of "
+                                   f"the workload), {len(tokens)} of {T} token(s) per layer, rotation 0; "
+                                   f"tokens/s = evaluations / layers per step * tokens / oracle seconds"},
         "e2e": {"value": tok_s, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
+
+
+# ----------------------------------------------------------------------------- parity spot check
+
+def snapshot_layers(moe, wl, T, desc, L, stacked, ws, layers, check_layers, xin, out, ids_buf):
+    """Host copies of what the oracle comparison reads, for the checked layers
+    of the run just made: the layer's input, its q8_K codes, routing, bucket
+    order, and the h / y rows of the sampled tokens' slots."""
+    import torch
+    tokens = token_sample(T)
+    P = T * (wl.k + wl.S)
+    snap = {"tokens": tokens, "layers": {}}
+    # the dataflow stack kernel keeps every layer's buffers; the pipelined one
+    # (short stacks of heavy layers) keeps a single layer's in the layer
+    # workspace at the start of the stack workspace
+    per_layer = stacked and moe.moe_stack_kernel(desc, L, T) == moe.STACK_DATAFLOW
+    if stacked and not per_layer:
+        if L > 1:
+            return None
+        layout = moe.moe_workspace_layout(desc)
+
+        class _One:
+            def ws_view(self, name, dt, shape):
+                return moe.MoeLayer.ws_view_of(ws, layout, name, dt, shape)
+        layers = [_One()]
+    for l in check_layers:
+        if per_layer:
+            lay = moe.moe_stack_layer_layout(desc, L, T, l)
+            v = lambda off, dt, shape: moe.ws_view(ws, off, dt, shape)
+            xq, ids, gates = v(lay.xq, torch.int8, (T, wl.H)), v(lay.ids, torch.int32, (T, wl.k)), \
+                v(lay.gates, torch.float32, (T, wl.k))
+            perm, h, y = v(lay.slot, torch.int32, (P,)), v(lay.h, torch.float32, (P, wl.I)), \
+                v(lay.y, torch.float32, (P, wl.H))
+        else:
+            ly = layers[l]
+            xq, gates = ly.ws_view("xq", torch.int8, (T, wl.H)), ly.ws_view("gates", torch.float32, (T, wl.k))
+            ids = ids_buf[l]
+            perm, h, y = ly.ws_view("perm", torch.int32, (P,)), ly.ws_view("h", torch.float32, (P, wl.I)), \
+                ly.ws_view("y", torch.float32, (P, wl.H))
+        perm_h = perm.cpu().numpy()
+        inv = np.empty(P, np.int64)
+        inv[perm_h] = np.arange(P)
+        slots = sorted({int(t) * wl.k + s_ for t in tokens for s_ in range(wl.k)} |
+                       {T * wl.k + sh * T + int(t) for t in tokens for sh in range(wl.S)})
+        sl = torch.as_tensor(slots, device=h.device, dtype=torch.int64)
+        hrows = h.index_select(0, torch.as_tensor(inv[slots], device=h.device)).cpu().numpy()
+        yrows = y.index_select(0, sl).cpu().numpy()
+        snap["layers"][l] = dict(x=xin(l).cpu().numpy(), xq=xq.cpu().numpy(), ids=ids.cpu().numpy(),
+                                 gates=gates.cpu().numpy(), perm=perm_h, out=out[l].cpu().numpy(),
+                                 h={int(inv[p]): hrows[i] for i, p in enumerate(slots)},
+                                 y={p: yrows[i] for i, p in enumerate(slots)})
+    return snap
+
+
+def spot_check(wl, T, snap):
+    """The oracle comparison rule of the parity tests (oracle.parity) on the
+    snapshot: codes, ids, bucketing exact; near-ties and h-code flips counted;
+    y and out within the fp32 forward-error bound; out within 1e-3 of the
+    row's L2 norm of the oracle's own layer."""
+    from oracle import parity
+    if snap is None:
+        return {"skipped": "the pipelined kernel of a multi-layer stack keeps no per-layer buffers"}
+    t0 = time.perf_counter()
+    metrics, fails = [], []
+    for l, d in snap["layers"].items():
+        wr = synth.router_weight(wl.E, wl.H, wl.seed, l)
+        bias = synth.router_bias(wl.E, wl.bias_std, wl.seed, l) if wl.bias_std > 0 else None
+        tokens = snap["tokens"]
+        need = sorted(set(d["ids"][tokens].reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
+        experts = [None] * (wl.E + wl.S)
+        for e in need:
+            experts[e] = (synth.gen_matrix(wl.fmt, wl.I, wl.H, wl.seed, l, e, 0),
+                          synth.gen_matrix(wl.fmt, wl.I, wl.H, wl.seed, l, e, 1),
+                          synth.gen_matrix(wl.fmt, wl.H, wl.I, wl.seed, l, e, 2))
+        m, f = parity.check_layer(wl.fmt, wl.H, wl.I, wl.E, wl.k, wl.S, wl.route, experts, wr, bias, d["x"],
+                                  d["x"], d, tokens)
+        metrics.append(m)
+        fails += [f"layer {l}: {x}" for x in f]
+    out = parity.merge(metrics)
+    out.update({"layers": sorted(snap["layers"]), "failures": len(fails), "first_failures": fails[:3],
+                "seconds": round(time.perf_counter() - t0, 1),
+                "rule": "oracle/parity.py: exact codes/ids/bucketing; y, out within the fp32 forward-error bound; "
+                        "out within 1e-3 of the row L2 norm"})
+    return out
 
 
 # ----------------------------------------------------------------------------- our arm
@@ -326,8 +431,10 @@ def run_ours(args, wl, T):
     desc = wl.desc(T)
     ws = torch.zeros(max(moe.moe_layer_workspace_size(desc), moe.moe_stack_workspace_size(desc, L)),
                      dtype=torch.uint8, device=dev)
+    links = chain_links(L) if args.chained else []
+
     def xin(l):  # layer l's input (and residual)
-        return out[l - 1] if args.chained and l > 0 else x_static[l]
+        return out[l - 1] if l in links else x_static[l]
 
     rows = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=xin(l), residual=xin(l),
                  out=out[l], ids_out=ids_buf[l]) for l in range(L)]
@@ -367,7 +474,10 @@ def run_ours(args, wl, T):
     x_static.copy_(xs[0])
     body()
     torch.cuda.synchronize()
-    out_r0 = out.cpu().numpy()
+    # device results of rotation 0 on the layers the parity spot check compares
+    check_layers = sorted({0, L // 2, L - 1} | ({1} if links else set()))
+    snap = snapshot_layers(moe, wl, T, desc, L, stacked, ws if stacked else None,
+                           None if stacked else layers, check_layers, xin, out, ids_buf)
 
     # CUDA graph of one step, with trace events around the expert launches
     events = [torch.cuda.Event(enable_timing=True) for _ in range(4 * L)]
@@ -524,8 +634,10 @@ def run_ours(args, wl, T):
                         "avg_launch_us": 1e3 * float(np.mean(gu_ms)),
                         "down_kernel_gbs": dn_gbs, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms))}
 
-    # end to end through the public call with host buffers: pinned H2D of the
-    # step's inputs, the layers, D2H of the outputs, every step
+    # end to end through the public call with host buffers, every step: a
+    # pinned H2D copy of the step's inputs, the C-ABI call(s) themselves
+    # (argument checks and launches on the host, no graph replay), and a D2H
+    # copy of the outputs
     x_pinned = torch.from_numpy(x_host).pin_memory()
     out_pinned = torch.empty((L, T, H), dtype=torch.float32).pin_memory()
     Ke = max(10, min(K, 2000))
@@ -534,10 +646,7 @@ def run_ours(args, wl, T):
     e0.record(stream)
     for i in range(Ke):
         x_static.copy_(x_pinned[i % R], non_blocking=True)
-        if use_graph:
-            graph.replay()
-        else:
-            body()
+        body()
         out_pinned.copy_(out, non_blocking=True)
     e1.record(stream)
     torch.cuda.synchronize()
@@ -560,7 +669,8 @@ def run_ours(args, wl, T):
                          "plus %.0f MB of router weights (L2 129 MB)" % (
                              np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
                    "graph": use_graph, "rotations": R, "single_launch_stack": stacked,
-                   "layer_inputs": "chained" if args.chained else "independent",
+                   "layer_inputs": (f"chained order (layers {links} read the previous layer's output)"
+                                    if links else "independent"),
                    "path": ["decode_fused", "gemv", "tensor_prefill"][path]},
         "clocks": clock_info,
         "us_per_layer": 1e3 * ms_step / L,
@@ -571,22 +681,14 @@ def run_ours(args, wl, T):
         "roofline": roofline,
         "decode_phases_us": phases,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms},
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                "how": "per step: pinned H2D of x, the C-ABI call through the binding (no graph), D2H of out"},
         "gpu_launches": launches_per_step * K,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(wl, T, x_host, args.cpu_budget_s)
-        # parity spot check of the bench's own launch configuration on the first layers
-        import oracle
-        tokens = token_sample(T)
-        # a chained stack's later layers read GPU outputs: check the layer whose input is known
-        check = [0] if args.chained else sorted({0, L - 1})
-        outs, _ = oracle_layers(wl, T, x_host[0], check, oracle.default_threads(), tokens)
-        worst = 0.0
-        for l, ref in outs.items():
-            err = np.abs(out_r0[l][tokens] - ref) / (1e-4 + 1e-3 * np.linalg.norm(ref, axis=1, keepdims=True))
-            worst = max(worst, float(err.max()))
-        line["parity_spot_check"] = {"layers": sorted(outs), "tokens": int(len(tokens)), "worst_err_over_tol": worst}
+        line["cpu_baseline"] = cpu_baseline(args, wl, T, args.cpu_budget_s)
+        # parity spot check of the bench's own launch (rotation 0) on layers 0, L/2, L-1
+        line["parity"] = spot_check(wl, T, snap)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

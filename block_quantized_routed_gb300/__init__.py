@@ -24,7 +24,8 @@ __all__ = [
     "moe_layer_workspace_size", "moe_workspace_layout", "moe_stack_forward", "moe_stack_workspace_size", "stack_pointer_table", "moe_layer_forward_noalloc", "moe_get_status", "moe_status_string",
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
     "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
-    "moe_stack_kernel", "STACK_PIPELINED", "STACK_DATAFLOW",
+    "moe_stack_kernel", "STACK_PIPELINED", "STACK_DATAFLOW", "StackLayerLayout", "moe_stack_layer_layout",
+    "ws_view",
 ]
 
 FMT_Q4K = 0
@@ -71,6 +72,10 @@ class WsLayout(ctypes.Structure):
                  "h", "hq", "hd", "hbs", "y", "phase_ns", "total")]
 
 
+class StackLayerLayout(ctypes.Structure):
+    _fields_ = [(n, ctypes.c_size_t) for n in ("logits", "xq", "xd", "xbs", "ids", "gates", "tok", "slot", "h", "y")]
+
+
 _lib = None
 
 
@@ -109,6 +114,7 @@ def load():
         "moe_debug_wait_timeout": (ctypes.c_int, [P, I32, P]),
         "moe_layer_path": (ctypes.c_int, [D, I32]),
         "moe_stack_kernel": (ctypes.c_int, [D, I32, I32, I32]),
+        "moe_stack_layer_layout": (ctypes.c_int, [D, I32, I32, I32, ctypes.POINTER(StackLayerLayout)]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -220,6 +226,24 @@ def moe_layer_forward_noalloc(desc, table, w_router, router_bias, x, residual, o
 
 def moe_stack_workspace_size(desc, n_layers) -> int:
     return int(load().moe_stack_workspace_size(ctypes.byref(_desc(desc)), n_layers))
+
+
+def moe_stack_layer_layout(desc, n_layers, T, layer) -> StackLayerLayout:
+    """Byte offsets of one stack layer's buffers in a moe_stack_forward workspace."""
+    out = StackLayerLayout()
+    _check(load().moe_stack_layer_layout(ctypes.byref(_desc(desc)), n_layers, T, layer, ctypes.byref(out)),
+           "moe_stack_layer_layout")
+    return out
+
+
+def ws_view(ws, offset, dtype, shape):
+    """A typed view of `shape` elements at byte `offset` of a uint8 workspace tensor."""
+    import torch
+    n = 1
+    for s_ in shape:
+        n *= s_
+    itemsize = torch.empty((), dtype=dtype).element_size()
+    return ws[offset:offset + n * itemsize].view(dtype).view(*shape)
 
 
 def moe_stack_forward(desc, layers, T, ws, stream=None):

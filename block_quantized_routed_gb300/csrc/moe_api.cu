@@ -477,6 +477,36 @@ size_t moe_stack_workspace_size(const moe_layer_desc* desc, int32_t n_layers) {
   return (plan_workspace(*desc).total + 255) / 256 * 256 + stack_plan(*desc, n_layers).total;
 }
 
+int moe_stack_layer_layout(const moe_layer_desc* desc, int32_t n_layers, int32_t T, int32_t layer,
+                           moe_stack_ws_layout* out) {
+  int why;
+  if (!desc_valid(desc, &why)) return why;
+  if (!out || n_layers < 1 || T < 1 || T > desc->T_max || layer < 0 || layer >= n_layers) return MOE_ERR_INVALID_ARG;
+  const int k = desc->top_k, S = desc->n_shared;
+  if (T > kDecodeMaxT || (int64_t)T * k > kSmallPairs ||
+      decode_smem_bytes(T, desc->H, desc->I, desc->E, k, S) > kDecodeSmemMax)
+    return MOE_ERR_UNSUPPORTED;
+  // the same placement as moe_stack_forward: the layer workspace of desc,
+  // then the stack extension planned for the call's T
+  moe_layer_desc dT = *desc;
+  dT.T_max = T;
+  const size_t ext = (plan_workspace(*desc).total + 255) / 256 * 256;
+  const StackPlan sp = stack_plan(dT, n_layers);
+  const size_t lb = ext + sp.layer0 + (size_t)layer * sp.layer_bytes;
+  const RouteFields rf = route_fields(T, k, S);
+  out->logits = lb + sp.logits;
+  out->xq = lb + sp.xq;
+  out->xd = lb + sp.xd;
+  out->xbs = lb + sp.xbs;
+  out->ids = lb + sp.route + rf.ids;
+  out->gates = lb + sp.route + rf.gates;
+  out->tok = lb + sp.route + rf.tok;
+  out->slot = lb + sp.route + rf.slot;
+  out->h = lb + sp.h;
+  out->y = lb + sp.y;
+  return MOE_OK;
+}
+
 int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
                       void* ws, size_t ws_bytes, void* stream) {
   int why;

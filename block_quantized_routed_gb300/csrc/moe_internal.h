@@ -157,6 +157,13 @@ cudaError_t launch_decode_stack(const DecodeArgs& a, cudaStream_t s);
 
 size_t decode_smem_bytes(int T, int H, int I, int E, int k, int S);
 size_t decode_route_bytes(int T, int k, int S);  // one routing state of the decode kernel
+// byte offsets of the fields of one routing state of T tokens (ids, gates
+// [T*k]; tok, slot [P]: token and slot index of each bucket position; tiles
+// [P]; ok [T*k + S]; n_tiles)
+struct RouteFields {
+  size_t ids, gates, tok, slot, tiles, ok, n_tiles;
+};
+RouteFields route_fields(int T, int k, int S);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
 // largest token count of the single-launch decode path
 constexpr int kDecodeMaxT = 16;

@@ -205,7 +205,12 @@ int moe_combine(const float* y_slots, const float* gates, int32_t T, int32_t H, 
  * records.  ids_out int32 [T, k] and gates_out float [T, k] are optional
  * copies of the routing (NULL to skip).  ws: at least
  * moe_layer_workspace_size(desc) bytes, 256-byte aligned; the intermediates
- * stay in it after the call at the offsets moe_workspace_layout gives. */
+ * stay in it after the call at the offsets moe_workspace_layout gives.
+ * Sources: Pulsar README, "How the streaming works" (per token the router
+ * picks the experts first; the expert kernels receive explicit per-(token,
+ * slot) gate/up/down pointers, NULL = not mine; one expert union per batch)
+ * and "Fidelity notes" (every matmul on q8_K activations with integer dp4a
+ * dots; the layer output is the per-slot sum of the expert outputs). */
 int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table,
                       const float* w_router, const float* router_bias, const float* x,
                       const float* residual, float* out, int32_t T, int32_t* ids_out,
@@ -257,6 +262,32 @@ size_t moe_stack_workspace_size(const moe_layer_desc* desc, int32_t n_layers);
 int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_layer_ptrs* layers, int32_t T,
                       void* ws, size_t ws_bytes, void* stream);
 
+/* Byte offsets, from the start of a moe_stack_forward workspace, of the
+ * buffers that layer `layer` of the dataflow stack kernel (MOE_STACK_DATAFLOW)
+ * fills, for inspection after a call with the same desc, n_layers and T.
+ * P = T * (top_k + n_shared) bucket positions; bucket positions are ordered
+ * by expert (routed experts ascending, then the shared experts), and within
+ * an expert by token. */
+typedef struct {
+  size_t logits; /* float [T, E]      router logits                             */
+  size_t xq;     /* int8  [T, H]      q8_K codes of x                           */
+  size_t xd;     /* float [T, H/256]                                            */
+  size_t xbs;    /* int16 [T, H/16]                                             */
+  size_t ids;    /* int32 [T, top_k]  selected experts                          */
+  size_t gates;  /* float [T, top_k]  renormalised gates                        */
+  size_t tok;    /* int32 [P]         token of each bucket position             */
+  size_t slot;   /* int32 [P]         slot index of each bucket position (the
+                                      perm of moe_bucket)                       */
+  size_t h;      /* float [P, I]      silu(G) * U, rows in bucket order         */
+  size_t y;      /* float [P, H]      expert outputs, by slot index             */
+} moe_stack_ws_layout;
+
+/* Fills `out` for layer 0 <= layer < n_layers.  Host-side only.  Returns
+ * MOE_OK, MOE_ERR_INVALID_ARG, or MOE_ERR_UNSUPPORTED for shapes that
+ * moe_stack_forward rejects.  No counterpart on the pages. */
+int moe_stack_layer_layout(const moe_layer_desc* desc, int32_t n_layers, int32_t T, int32_t layer,
+                           moe_stack_ws_layout* out);
+
 /* Largest workspace, in bytes, that moe_layer_forward_noalloc can serve. */
 #define MOE_NOALLOC_MAX_WORKSPACE ((size_t)16 << 20)
 
@@ -274,9 +305,11 @@ int moe_stack_forward(const moe_layer_desc* desc, int32_t n_layers, const moe_la
  *     MOE_NOALLOC_MAX_WORKSPACE are rejected with MOE_ERR_WORKSPACE (decode
  *     shapes fit: e.g. H=6144, I=2048, 192 experts, top-8, 16 tokens needs
  *     about 5 MB).
- *   - The first call on a device looks up the array's device address for
- *     that device (with it current); make that first call before any stream
- *     capture.
+ *   - Each call looks up the array's device address in the context current
+ *     on the calling thread (a host-side lookup; the runtime's primary
+ *     context or a context the caller made current both work).  The first
+ *     call on a device may also load the library's device code there: make
+ *     that first call before any stream capture.
  *   - All calls share the one array and it keeps the last call's contents;
  *     each call clears the parts that must start at zero.  Calls that
  *     overlap on the GPU (other streams, other host threads) race on it:

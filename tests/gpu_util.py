@@ -1,22 +1,22 @@
 """Helpers of the GPU parity tests: device copies of synthetic inputs and the
-tolerance rule.
+relative tolerance rule.
 
-Tolerance (floating-point outputs of the layer): per token row t and element
-i, |gpu - oracle| <= 1e-4 + 1e-3 * ||oracle_row_t||_2.  A row's L2 norm is
-the "output's L2 norm" of the relative bound; 1e-4 is the absolute bound.
+Relative bound (floating-point outputs): per token row t and element i,
+|gpu - oracle| <= 1e-3 * ||oracle_row_t||_2, the row's L2 norm being the
+"output's L2 norm" of the stated bound.  The absolute side of the rule (the
+fp32 forward-error bound, and the count of elements within 1e-4) needs the
+oracle's per-slot terms and is applied by oracle.parity.check_layer.
 Integer results (q8_K codes, expert ids, bucket order, sub-block sums) are
 compared bit for bit."""
 from __future__ import annotations
 
 import numpy as np
 
-ABS_TOL = 1e-4
-REL_TOL = 1e-3
-NEAR_TIE = 1e-5
+from oracle.parity import NEAR_TIE, REL_TOL  # noqa: F401  (one definition of the rule)
 
 
 def tol_rows(ref: np.ndarray) -> np.ndarray:
-    return ABS_TOL + REL_TOL * np.linalg.norm(ref, axis=-1, keepdims=True)
+    return REL_TOL * np.linalg.norm(ref, axis=-1, keepdims=True)
 
 
 def assert_close_rows(got, ref, what="output"):

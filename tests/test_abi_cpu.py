@@ -178,3 +178,30 @@ def test_stack_workspace_size(lib):
     assert moe.moe_stack_workspace_size(desc(T_max=4), 40) > forty
     assert moe.moe_stack_workspace_size(d, 0) == 0
     assert moe.moe_stack_workspace_size(desc(H=300), 4) == 0
+
+
+@pytest.mark.parametrize("L,T,kw", [(40, 1, {}), (48, 4, dict(H=4096, I=1024, E=512, top_k=10, fmt=1, route=1))])
+def test_stack_layer_layout_regions(lib, L, T, kw):
+    """Per-layer buffers of the stack workspace: inside it, 256-byte aligned, one fixed stride per layer,
+    and no two regions of one layer overlapping."""
+    d = desc(T_max=T, **kw)
+    total = moe.moe_stack_workspace_size(d, L)
+    k, S = d.top_k, d.n_shared
+    P = T * (k + S)
+    size = dict(logits=T * d.E * 4, xq=T * d.H, xd=T * d.H // 256 * 4, xbs=T * d.H // 16 * 2, ids=T * k * 4,
+                gates=T * k * 4, tok=P * 4, slot=P * 4, h=P * d.I * 4, y=P * d.H * 4)
+    lays = [moe.moe_stack_layer_layout(d, L, T, l) for l in range(L)]
+    stride = lays[1].logits - lays[0].logits
+    assert stride > 0
+    for l, lay in enumerate(lays):
+        spans = sorted((getattr(lay, n), getattr(lay, n) + b) for n, b in size.items())
+        assert all(a[1] <= b[0] for a, b in zip(spans, spans[1:]))      # disjoint
+        assert spans[-1][1] <= total
+        assert lay.logits % 256 == 0 and lay.h % 256 == 0 and lay.y % 256 == 0
+        assert lay.logits == lays[0].logits + l * stride
+    # the layer workspace (status block first) comes before every layer's buffers
+    assert lays[0].logits >= moe.moe_layer_workspace_size(d)
+    with pytest.raises(moe.MoeError):
+        moe.moe_stack_layer_layout(d, L, T, L)
+    with pytest.raises(moe.MoeError):
+        moe.moe_stack_layer_layout(desc(T_max=32), L, 32, 0)              # beyond the decode shapes

@@ -3,7 +3,8 @@
 Integer results are compared bit for bit: q8_K codes/scales/16-sums, the
 integer sub-block dot sums of the device dot routine, expert ids (away from
 near-ties), bucket counts/offsets/permutation.  Floating-point results use
-the per-row tolerance of tests/gpu_util.py.  Sizes span several 32-row
+the relative rule of tests/gpu_util.py, and the layer cases also the fp32
+forward-error bound of oracle/parity.py.  Sizes span several 32-row
 groups, several 256-column blocks and ragged token counts."""
 import numpy as np
 import pytest
@@ -12,6 +13,7 @@ import oracle
 import synth
 from synth.layout import FMT_Q4K, FMT_Q2K
 from tests import fieldpack
+from oracle import parity
 from tests.gpu_util import assert_close_rows, routing_ok, to_dev
 
 torch = pytest.importorskip("torch")
@@ -266,6 +268,13 @@ def test_layer_forward(moe, case):
     rq, rd, _ = oracle.q8k_quantize(h)
     np.testing.assert_array_equal(hq, rq)
     np.testing.assert_array_equal(hd, rd)
+    # per-slot y and the output within the fp32 forward-error bound, h-code flips counted
+    devd = dict(xq=layer.ws_view("xq", torch.int8, (T, H)).cpu().numpy(), ids=gids, gates=gates.cpu().numpy(),
+                perm=layer.ws_view("perm", torch.int32, (P,)).cpu().numpy(), h=h,
+                y=layer.ws_view("y", torch.float32, (P, H)).cpu().numpy(), out=out.cpu().numpy())
+    tokens = np.arange(T) if T <= 64 else np.unique(np.linspace(0, T - 1, 64).round().astype(np.int64))
+    _, fails = parity.check_layer(fmt, H, I, E, k, S, route, ex, wr, bias, x, res, devd, tokens)
+    assert not fails, "; ".join(fails[:5])
 
 
 def test_layer_forward_is_deterministic(moe):

@@ -1,8 +1,12 @@
-"""Parity at the full sizes of the five workloads, in the launch configuration
-bench.py times (one MoeLayer per layer, all experts resident on the device,
-weights made by the device generator).  The oracle recomputes sampled layers
-and sampled tokens one by one from host-generated copies of the routed
-experts; bucketing is checked bit for bit on every token."""
+"""Parity at the full sizes of the five workloads through moe_layer_forward
+(one layer per call, all experts resident on the device, weights made by
+the device generator): the single-launch decode kernel for the decode,
+verify and wide workloads, the tcgen05 grouped GEMMs for the prefill chunk.
+(bench.py times the decode and verify workloads as one moe_stack_forward per
+step; tests/test_gpu_stack_workloads.py checks that launch.)  The oracle
+recomputes sampled layers and tokens one by one from host-generated copies
+of the routed experts, with the rule of oracle.parity.check_layer; bucketing
+is checked bit for bit on every token."""
 import gc
 
 import numpy as np
@@ -10,8 +14,8 @@ import pytest
 
 import oracle
 import synth
+from oracle import parity
 from synth.workloads import WORKLOADS
-from tests.gpu_util import assert_close_rows, routing_ok
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -39,9 +43,20 @@ def _host_experts(wl, layer, need):
     return experts
 
 
-def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0):
-    """Run one layer on the device, compare ids/gates/bucketing (all tokens) and
-    outputs of `tokens` (all if None) with the oracle."""
+class Rows:
+    """Row access to a device tensor (one row copied to the host per access)."""
+
+    def __init__(self, t):
+        self.t = t
+
+    def __getitem__(self, i):
+        return self.t[int(i)].cpu().numpy()
+
+
+def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0, tile_rows=False):
+    """Run one layer on the device and compare it with the oracle on `tokens`
+    (all if None); with tile_rows, also on the first and last rows of the
+    128-row token tiles of some experts (the tensor-core path's tile edges)."""
     import synth.gpu  # noqa: F401
     dev = bank.buf.device
     wr = synth.router_weight(wl.E, wl.H, wl.seed, layer)
@@ -54,27 +69,30 @@ def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0):
     gates = torch.empty((T, wl.k), dtype=torch.float32, device=dev)
     out = lay.forward(xd, residual=xd, ids_out=ids, gates_out=gates)
     assert moe.moe_get_status(lay.ws) == 0
-    gids = ids.cpu().numpy()
-    # bucketing of every token, bit for bit, from the device's own ids
     P = T * (wl.k + wl.S)
-    rc, ro, rp = oracle.bucket(gids, wl.E, wl.S)
+    gids = ids.cpu().numpy()
+    rc, ro, _ = oracle.bucket(gids, wl.E, wl.S)
     np.testing.assert_array_equal(lay.ws_view("counts", torch.int32, (wl.E + wl.S,)).cpu().numpy(), rc)
     np.testing.assert_array_equal(lay.ws_view("offsets", torch.int32, (wl.E + wl.S + 1,)).cpu().numpy(), ro)
-    np.testing.assert_array_equal(lay.ws_view("perm", torch.int32, (P,)).cpu().numpy(), rp)
-    # q8_K codes of every token, bit for bit
-    xq = lay.ws_view("xq", torch.int8, (T, wl.H)).cpu().numpy()
-    rq, rd, _ = oracle.q8k_quantize(x)
-    np.testing.assert_array_equal(xq, rq)
+    perm = lay.ws_view("perm", torch.int32, (P,)).cpu().numpy()
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
-    rl, rids, _, rgap = oracle.route(x[sel], wr, bias, wl.k, wl.route)
-    near = routing_ok(gids[sel], rids, rgap, rl)
+    if tile_rows:
+        # first and last rows of the 128-row tiles of the experts with the most tokens
+        edge = []
+        for e in np.argsort(-rc[:wl.E], kind="stable")[:6]:
+            for pos in (ro[e], ro[e] + 127, ro[e] + 128, ro[e + 1] - 1):
+                if ro[e] <= pos < ro[e + 1]:
+                    edge.append(int(perm[pos]) // wl.k)
+        sel = np.unique(np.concatenate([sel, np.asarray(edge, np.int64)]))
     need = sorted(set(gids[sel].reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
     experts = _host_experts(wl, layer, need)
-    ref, _, rg, _ = oracle.layer_forward(wl.fmt, wl.H, wl.I, wl.E, wl.k, wl.S, wl.route, experts, wr, bias, x[sel],
-                                         residual=x[sel], forced_ids=gids[sel])
-    np.testing.assert_allclose(gates.cpu().numpy()[sel], rg, rtol=1e-5, atol=1e-6)
-    assert_close_rows(out.cpu().numpy()[sel], ref, f"layer {layer}")
-    return near
+    devd = dict(xq=lay.ws_view("xq", torch.int8, (T, wl.H)).cpu().numpy(), ids=gids, gates=gates.cpu().numpy(),
+                perm=perm, h=Rows(lay.ws_view("h", torch.float32, (P, wl.I))),
+                y=Rows(lay.ws_view("y", torch.float32, (P, wl.H))), out=out.cpu().numpy())
+    metrics, fails = parity.check_layer(wl.fmt, wl.H, wl.I, wl.E, wl.k, wl.S, wl.route, experts, wr, bias, x, x,
+                                        devd, sel)
+    assert not fails, f"layer {layer}: " + "; ".join(fails[:5])
+    return metrics
 
 
 def test_device_generator_matches_host_generator(moe):
@@ -133,6 +151,9 @@ def test_prefill_chunk_8192(moe):
     import synth.gpu
     wl = WORKLOADS["prefill_h4096_e512k10s1_i1024_q4k_t8192"]
     bank = synth.gpu.ExpertBank(wl.fmt, wl.H, wl.I, wl.E + wl.S, wl.layers, wl.seed)
-    _check_layer(moe, wl, bank, 0, wl.T, tokens=[0, 1, 4095, 8191])
+    tokens = np.unique(np.linspace(0, wl.T - 1, 64).round().astype(np.int64))
+    m = _check_layer(moe, wl, bank, 0, wl.T, tokens=tokens, tile_rows=True)
+    assert m["tokens"] >= 64
+    print(f"\nprefill: {m}")
     del bank
     _free()
