@@ -347,11 +347,13 @@ def snapshot_layers(moe, wl, T, desc, L, stacked, ws, layers, check_layers, xin,
             v = lambda off, dt, shape: moe.ws_view(ws, off, dt, shape)
             xq, ids, gates = v(lay.xq, torch.int8, (T, wl.H)), v(lay.ids, torch.int32, (T, wl.k)), \
                 v(lay.gates, torch.float32, (T, wl.k))
+            logits = v(lay.logits, torch.float32, (T, wl.E))
             perm, h, y = v(lay.slot, torch.int32, (P,)), v(lay.h, torch.float32, (P, wl.I)), \
                 v(lay.y, torch.float32, (P, wl.H))
         else:
             ly = layers[l]
             xq, gates = ly.ws_view("xq", torch.int8, (T, wl.H)), ly.ws_view("gates", torch.float32, (T, wl.k))
+            logits = ly.ws_view("logits", torch.float32, (T, wl.E))
             ids = ids_buf[l]
             perm, h, y = ly.ws_view("perm", torch.int32, (P,)), ly.ws_view("h", torch.float32, (P, wl.I)), \
                 ly.ws_view("y", torch.float32, (P, wl.H))
@@ -364,7 +366,8 @@ def snapshot_layers(moe, wl, T, desc, L, stacked, ws, layers, check_layers, xin,
         hrows = h.index_select(0, torch.as_tensor(inv[slots], device=h.device)).cpu().numpy()
         yrows = y.index_select(0, sl).cpu().numpy()
         snap["layers"][l] = dict(x=xin(l).cpu().numpy(), xq=xq.cpu().numpy(), ids=ids.cpu().numpy(),
-                                 gates=gates.cpu().numpy(), perm=perm_h, out=out[l].cpu().numpy(),
+                                 gates=gates.cpu().numpy(), logits=logits.cpu().numpy(), perm=perm_h,
+                                 out=out[l].cpu().numpy(),
                                  h={int(inv[p]): hrows[i] for i, p in enumerate(slots)},
                                  y={p: yrows[i] for i, p in enumerate(slots)})
     return snap

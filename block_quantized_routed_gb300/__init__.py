@@ -25,7 +25,7 @@ __all__ = [
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
     "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
     "moe_stack_kernel", "STACK_PIPELINED", "STACK_DATAFLOW", "StackLayerLayout", "moe_stack_layer_layout",
-    "ws_view",
+    "ws_view", "moe_debug_prefill_sums", "moe_debug_prefill_sums_workspace_size",
 ]
 
 FMT_Q4K = 0
@@ -115,6 +115,8 @@ def load():
         "moe_layer_path": (ctypes.c_int, [D, I32]),
         "moe_stack_kernel": (ctypes.c_int, [D, I32, I32, I32]),
         "moe_stack_layer_layout": (ctypes.c_int, [D, I32, I32, I32, ctypes.POINTER(StackLayerLayout)]),
+        "moe_debug_prefill_sums_workspace_size": (SZ, [I32, I32, I32]),
+        "moe_debug_prefill_sums": (ctypes.c_int, [I32, P, I32, I32, P, P, P, I32, P, P, P, SZ, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -325,6 +327,18 @@ def moe_debug_subblock_dots(fmt, w, N, K, q, isum, bsum, stream=None):
     T = q.shape[0]
     _check(load().moe_debug_subblock_dots(fmt, _ptr(w), N, K, _ptr(q), T, _ptr(isum), _ptr(bsum), _stream(stream)),
            "moe_debug_subblock_dots")
+
+
+def moe_debug_prefill_sums_workspace_size(N, K, T) -> int:
+    return int(load().moe_debug_prefill_sums_workspace_size(N, K, T))
+
+
+def moe_debug_prefill_sums(fmt, w, N, K, q, d, bsum16, S, M, ws, stream=None):
+    """Test hook: integer super-block sums S, M (int32 [T, N, K/256]) of the tensor-core path."""
+    T = q.shape[0]
+    _check(load().moe_debug_prefill_sums(fmt, _ptr(w), N, K, _ptr(q), _ptr(d), _ptr(bsum16), T, _ptr(S), _ptr(M),
+                                         _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "moe_debug_prefill_sums")
 
 
 # ----------------------------------------------------------------- convenience

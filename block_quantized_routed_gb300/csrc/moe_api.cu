@@ -684,4 +684,35 @@ int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, co
   return check(launch_debug_dots(fmt, w, N, K, q, T, isum, bsum, as_stream(stream)));
 }
 
+size_t moe_debug_prefill_sums_workspace_size(int32_t N, int32_t K, int32_t T) {
+  if (N <= 0 || K <= 0 || T < 1 || N % 128 || K % 256 || N > MOE_MAX_DIM || K > MOE_MAX_DIM) return 0;
+  return sums_plan(N, K, T).total;
+}
+
+int moe_debug_prefill_sums(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, const float* d,
+                           const int16_t* bsum16, int32_t T, int32_t* S, int32_t* M, void* ws, size_t ws_bytes,
+                           void* stream) {
+  if (fmt != MOE_FMT_Q4K && fmt != MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED;
+  if (N <= 0 || K <= 0 || T < 1) return MOE_ERR_INVALID_ARG;
+  if (N % 128 || K % 256 || N > MOE_MAX_DIM || K > MOE_MAX_DIM || (int64_t)T * (K / 256) * 2 >= ((int64_t)1 << 31))
+    return MOE_ERR_UNSUPPORTED;
+  if (!w || !q || !d || !bsum16 || !S || !M || !ws) return MOE_ERR_INVALID_ARG;
+  if (!aligned(w, 16) || !aligned(q, 16) || !aligned(d, 4) || !aligned(bsum16, 4) || !aligned(ws, kAlign))
+    return MOE_ERR_INVALID_ARG;
+  if (ws_bytes < sums_plan(N, K, T).total) return MOE_ERR_WORKSPACE;
+  SumsArgs a{};
+  a.fmt = fmt;
+  a.N = N;
+  a.K = K;
+  a.T = T;
+  a.w = w;
+  a.q = q;
+  a.d = d;
+  a.bs16 = bsum16;
+  a.S = S;
+  a.M = M;
+  a.ws = ws;
+  return check(launch_prefill_sums(a, as_stream(stream)));
+}
+
 }  // extern "C"

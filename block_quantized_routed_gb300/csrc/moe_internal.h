@@ -215,6 +215,25 @@ struct PrefillArgs {
 };
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s);
 
+// Test hook of the tensor-core path: the integer super-block sums S and M of
+// a matrix w [N, K] (N a multiple of 128) against q8_K rows, from the same
+// GEMM kernel with an epilogue that writes them instead of rescaling.
+struct SumsArgs {
+  int fmt, N, K, T;
+  const void* w;
+  const int8_t* q;
+  const float* d;
+  const int16_t* bs16;
+  int32_t* S;  // [T][N][K/256]
+  int32_t* M;
+  void* ws;
+};
+struct SumsPlan {
+  size_t status, xg, sg, dg, items, n_items, total;
+};
+SumsPlan sums_plan(int N, int K, int T);
+cudaError_t launch_prefill_sums(const SumsArgs& a, cudaStream_t s);
+
 cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S,
                            const float* residual, float* out, cudaStream_t s);
 

@@ -9,17 +9,26 @@
 //   B (activations) the q8_K codes of the tokens               (|q| <= 127: exact)
 //   S[m, n, b] = sum over the 256 columns of super-block b of A * B
 //
-// tcgen05.mma kind::f16 accumulates in fp32 in tensor memory (TMEM); the
-// integer partial sums stay below 2^24 (Q4_K: |S| <= 63*15*127*256 fits
-// except in contrived all-extreme blocks, where fp32 rounding is the only
-// deviation; Q2_K always fits), so S is the integer sub-block sum.  The
-// min term M[m, n, b] = sum_j mn_j * bsum_j(n) is one extra K=16 MMA per
-// super-block on the tokens' code sums (Q4_K: bsum = 64*hi + lo against
-// mn and 64*mn, both halves exact; Q2_K: |bsum16| <= 2032 as is).  The
-// epilogue rescales per super-block in fp32 registers:
+// tcgen05.mma kind::f16 accumulates in fp32 in tensor memory (TMEM).  Each
+// half super-block (128 columns) accumulates into its own TMEM region, S0
+// and S1: every partial sum of a half is an integer of magnitude at most
+// 63*15*127*128 < 2^24 (Q4_K; Q2_K: 15*3*127*128), so S0 and S1 are the
+// exact integer sums of their halves.  (A whole Q4_K super-block can reach
+// 63*15*127*256 > 2^24, which one fp32 accumulator could not hold.)  The
+// epilogue adds them in fp32, which rounds the exact S = S0 + S1 once, as
+// the int -> fp32 conversion of the dp4a kernels does.  The min term
+// M[m, n, b] = sum_j mn_j * bsum_j(n) is one extra K=16 MMA per super-block
+// on the tokens' code sums into a third region (Q4_K: bsum = 64*hi + lo
+// against mn and 64*mn, both halves exact; Q2_K: |bsum16| <= 2032 as is;
+// |M| <= 63*127*256).  The epilogue rescales per super-block in fp32
+// registers:
 //
-//   D[m, n] = sum_b d_a[n, b] * (d_w[m, b] * S[m, n, b] - dmin[m, b] * M[m, n, b])
+//   D[m, n] = sum_b d_a[n, b] * (d_w[m, b] * (S0 + S1)[m, n, b] - dmin[m, b] * M[m, n, b])
 //
+// TMEM holds four regions of 128 columns used as a ring: super-block
+// number tb of a CTA writes S0, S1, M to regions 3tb, 3tb+1, 3tb+2 (mod 4),
+// so the MMAs of the next super-block start while the epilogue still reads
+// this one.
 // This is the same contraction the GEMV kernels compute with dp4a; the
 // pages' prefill design reaches it with int8 MMA (Pulsar README, "What it
 // does today"; Strata, 0.1.13 prefill notes: grouped int8 tensor-core expert
@@ -31,10 +40,10 @@
 //                tiles of the activation codes / code sums into rings
 //   warps 16-23  expanders: raw slab -> fp16 sc*q tile (two threads per
 //                weight row, one swizzle atom each), mins tile for the min MMA
-//   warp 25      MMA issuer (one thread): 8 MMAs per half super-block into a
-//                double-buffered TMEM accumulator, the min MMA with the last
-//                half; commits are grouped (a commit costs the issuing
-//                thread several hundred cycles, so each group carries 8+ MMAs)
+//   warp 25      MMA issuer (one thread): 8 MMAs per half super-block into
+//                that half's TMEM region, the min MMA with the last half;
+//                commits are grouped (a commit costs the issuing thread
+//                several hundred cycles, so each group carries 8+ MMAs)
 //   warps 0-15   epilogue: TMEM -> registers, per-block rescale, output
 // (26 warps at 72 registers: the register file is split between the SM's
 // four sub-partitions, so the warp count bounds the registers per thread.)
@@ -47,6 +56,8 @@
 //            holds G and U of one (row, token): SwiGLU is a shuffle, and h is
 //            written in bucket order.
 //   down:    128 rows of H; y goes to the (token, slot) rows of the slot buffer.
+//   sums:    (test hook) as down, but the epilogue writes the integer S and
+//            M of every super-block instead of the rescaled sum.
 // Activations are first gathered into bucket order as fp16 codes (and the
 // code sums and block scales into TMA-friendly planes) by a small kernel, so
 // a token tile is a plain 2-D box for TMA.
@@ -256,7 +267,18 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
+__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
+  uint32_t r[4];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+               : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
+}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
+
+// TMEM column of region i (0..3, 128 columns each) of the ring
+__device__ __forceinline__ uint32_t tmem_region(uint32_t i) { return 128u * (i & 3u); }
 
 // byte offset of element (row, k) in a K-major canonical tile without
 // swizzle, kc core matrices along K (16-bit elements)
@@ -416,9 +438,15 @@ struct GemmArgs {
   float* y;
   int* status;
   unsigned long long* stats;  // [16] wait statistics of CTA 0 (nullable)
+  // MODE 2 (test hook): the one matrix [N_out, K], and the integer sums out [T][N_out][K/256]
+  const void* dbg_w;
+  int32_t* dbg_s;
+  int32_t* dbg_m;
+  int dbg_n;
 };
 
-template <int FMT, int MODE>  // MODE 0: gate/up + SwiGLU -> h; MODE 1: down -> y
+// MODE 0: gate/up + SwiGLU -> h; MODE 1: down -> y; MODE 2: integer S and M of a matrix (test hook)
+template <int FMT, int MODE>
 __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid_constant__ GemmArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ uint8_t sm_raw[];
@@ -426,7 +454,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int K = MODE == 0 ? a.H : a.I;
   const int nb = K / 256;
-  const int N_out = MODE == 0 ? a.I : a.H;
+  const int N_out = MODE == 0 ? a.I : MODE == 1 ? a.H : a.dbg_n;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar0 = sbase + kSmBar;
   // barrier slots: full_a, empty_a, full_b, empty_b, full_raw, empty_raw, tfull, tempty
@@ -483,7 +511,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       bool ok = true;
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const PItem it = a.items[item];
-        const moe_expert_ptrs ep = a.table[it.expert];
+        moe_expert_ptrs ep;
+        if (MODE == 2) ep.gate = ep.up = ep.down = a.dbg_w;
+        else ep = a.table[it.expert];
         const int nbox = (it.count + kBoxRows - 1) / kBoxRows;
         // the four row groups of the tile: gate/up -> gate 2w, 2w+1, up 2w, 2w+1; down -> 4w .. 4w+3
         const uint8_t* src[4];
@@ -633,24 +663,28 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       int as = 0, bs = 0;
       uint32_t pa = 0, pb = 0;
       bool ok = true;
+      static_assert(256 / kStageK == 2, "one TMEM region per half super-block");
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const PItem it = a.items[item];
         const int N = (it.count + 15) / 16 * 16;
         const uint32_t idesc = idesc_f16(kTileM, N);
         for (int b = 0; b < nb && ok; ++b) {
           const int ab = tb & 1;
-          if (!(ok = wait_bar(tempty(ab), ((tb >> 1) & 1) ^ 1, abort_flag, a.status, w0))) break;
-          tc_fence_after();
-          const uint32_t dS = tmem + ab * 256, dM = dS + 128;
           const int rs = ri % kRaw;
-          for (int c = 0; c < 256 / kStageK && ok; ++c) {
+          for (int c = 0; c < 2 && ok; ++c) {
+            // S0 of super-block tb reuses the region of super-block tb-2's M;
+            // S1 and M reuse tb-1's S0 and S1: wait until the epilogue has
+            // read that super-block (tempty[j & 1] completes phase j >> 1)
+            const int done = (int)tb - 2 + c;
+            if (done >= 0 && !(ok = wait_bar(tempty(done & 1), (done >> 1) & 1, abort_flag, a.status, w0))) break;
             if (!(ok = wait_bar(full_a(as), pa, abort_flag, a.status, w1))) break;
             if (!(ok = wait_bar(full_b(bs), pb, abort_flag, a.status, w1))) break;
-            const bool last = c == 256 / kStageK - 1;
+            const bool last = c == 1;
             if (last && !(ok = wait_bar(full_raw(rs), (ri / kRaw) & 1, abort_flag, a.status, w1))) break;
             tc_fence_after();
+            const uint32_t dS = tmem + tmem_region(3 * tb + c), dM = tmem + tmem_region(3 * tb + 2);
             const uint64_t da = dA0 + (uint64_t)((as * kAStage) >> 4), db = dB0 + (uint64_t)((bs * kBStage) >> 4);
-            mma_stage4(dS, da, db, idesc, c > 0);
+            mma_stage4(dS, da, db, idesc, false);
             mma_stage4(dS, da + (kAtomBytes >> 4), db + (kAtomBytes >> 4), idesc, true);
             if (last) mma_f16(dM, dA2 + (uint64_t)((rs * 4096) >> 4), dB2 + (uint64_t)((rs * 4096) >> 4), idesc, false);
             mma_commit(empty_a(as));
@@ -679,7 +713,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       const PItem it = a.items[item];
-      const moe_expert_ptrs ep = a.table[it.expert];
+      moe_expert_ptrs ep;
+      if (MODE == 2) ep.gate = ep.up = ep.down = a.dbg_w;
+      else ep = a.table[it.expert];
       const int ntok = it.count;
       const int N = (ntok + 15) / 16 * 16;
       const uint8_t* hdr;  // d/dmin word of this row's super-block 0
@@ -715,23 +751,42 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         __syncwarp();
         const float dw = half_lo(dm), dmin = half_hi(dm);
         const unsigned long long dw2 = f2_pack(dw, dw), ndm2 = f2_pack(-dmin, -dmin);
-        const uint32_t tS = tmem + ((uint32_t)(32 * qd) << 16) + ab * 256;
+        const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+        const uint32_t tS0 = tl + tmem_region(3 * tb), tS1 = tl + tmem_region(3 * tb + 1),
+                       tM = tl + tmem_region(3 * tb + 2);
 #pragma unroll
         for (int kl = 0; kl < 2; ++kl) {
           const int c = 4 * kl + cg;  // chunk of 16 tokens
           if (16 * c < N) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              float Sv[8], Mv[8];
-              tmem_ld8(tS + 16 * c + 8 * hh, Sv);
-              tmem_ld8(tS + 128 + 16 * c + 8 * hh, Mv);
+            for (int q4 = 0; q4 < 4; ++q4) {
+              float S0v[4], S1v[4], Mv[4];
+              const uint32_t col = 16 * c + 4 * q4;
+              tmem_ld4(tS0 + col, S0v);
+              tmem_ld4(tS1 + col, S1v);
+              tmem_ld4(tM + col, Mv);
               tmem_wait_ld();
+              if constexpr (MODE == 2) {
+                // the integer sums of the super-block: S = S0 + S1 exactly (each half below 2^24)
+                const int row = it.wtile * kTileM + m;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) {
-                const float2 d2 = *reinterpret_cast<const float2*>(s_da + 16 * kl + 8 * hh + 2 * j);
-                const unsigned long long t =
-                    f2_fma(dw2, f2_pack(Sv[2 * j], Sv[2 * j + 1]), f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
-                acc[8 * kl + 4 * hh + j] = f2_fma(f2_pack(d2.x, d2.y), t, acc[8 * kl + 4 * hh + j]);
+                for (int i = 0; i < 4; ++i) {
+                  const int tok = col + i;
+                  if (tok < ntok) {
+                    const int64_t o = ((int64_t)(it.start + tok) * N_out + row) * nb + b;
+                    a.dbg_s[o] = (int32_t)S0v[i] + (int32_t)S1v[i];
+                    a.dbg_m[o] = (int32_t)Mv[i];
+                  }
+                }
+              } else {
+#pragma unroll
+                for (int j = 0; j < 2; ++j) {
+                  // S0 + S1: both exact integers, so the fp32 sum rounds the exact S once
+                  const float2 d2 = *reinterpret_cast<const float2*>(s_da + 16 * kl + 4 * q4 + 2 * j);
+                  const unsigned long long S2 = f2_pack(S0v[2 * j] + S1v[2 * j], S0v[2 * j + 1] + S1v[2 * j + 1]);
+                  const unsigned long long t = f2_fma(dw2, S2, f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
+                  acc[8 * kl + 2 * q4 + j] = f2_fma(f2_pack(d2.x, d2.y), t, acc[8 * kl + 2 * q4 + j]);
+                }
               }
             }
           }
@@ -742,6 +797,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         ++tb;
       }
       if (!ok) break;
+      if constexpr (MODE == 2) continue;
 #pragma unroll
       for (int p = 0; p < 16; ++p) {
         const int kl = p >> 3, j = 2 * (p & 7);
@@ -893,7 +949,80 @@ cudaError_t launch_prefill_fmt(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
+// Items of the sums hook: token tiles of up to 128 rows x the 128-row weight tiles.
+__global__ void sums_items_kernel(int T, int n_wtiles, PItem* items, int32_t* n_items) {
+  const int nt = (T + kTileN - 1) / kTileN;
+  for (int i = threadIdx.x; i < nt * n_wtiles; i += blockDim.x) {
+    PItem it;
+    it.expert = 0;
+    it.start = (i / n_wtiles) * kTileN;
+    it.count = min(kTileN, T - it.start);
+    it.wtile = i % n_wtiles;
+    items[i] = it;
+  }
+  if (threadIdx.x == 0) *n_items = nt * n_wtiles;
+}
+
+template <int FMT>
+cudaError_t launch_sums_t(const SumsArgs& a, cudaStream_t s) {
+  const SumsPlan p = sums_plan(a.N, a.K, a.T);
+  char* base = static_cast<char*>(a.ws);
+  __half* xg = reinterpret_cast<__half*>(base + p.xg);
+  __half* sg = reinterpret_cast<__half*>(base + p.sg);
+  float* dg = reinterpret_cast<float*>(base + p.dg);
+  PItem* items = reinterpret_cast<PItem*>(base + p.items);
+  int32_t* n_items = reinterpret_cast<int32_t*>(base + p.n_items);
+  cudaError_t err = launch_gather<FMT>(a.q, a.bs16, a.d, nullptr, a.T, 1, a.T, a.K, xg, sg, dg, s);
+  if (err != cudaSuccess) return err;
+  GemmArgs g{};
+  g.fmt = FMT;
+  g.H = a.N;
+  g.I = a.K;
+  g.T = a.T;
+  g.k = 1;
+  g.P = a.T;
+  g.dg = dg;
+  g.items = items;
+  g.n_items = n_items;
+  g.status = reinterpret_cast<int*>(base + p.status);
+  g.dbg_w = a.w;
+  g.dbg_s = a.S;
+  g.dbg_m = a.M;
+  g.dbg_n = a.N;
+  if (!make_map(&g.map_x, xg, (uint64_t)a.K, (uint64_t)a.T, 64, kBoxRows, true) ||
+      !make_map(&g.map_s, sg, 8, (uint64_t)(a.K / 256) * 2 * a.T, 8, 128, false))
+    return cudaErrorInvalidValue;
+  const int n_wtiles = a.N / kTileM;
+  note_launch();
+  sums_items_kernel<<<1, 256, 0, s>>>(a.T, n_wtiles, items, n_items);
+  if ((err = cudaGetLastError()) != cudaSuccess) return err;
+  return launch_gemm_t<FMT, 2>(g, ((a.T + kTileN - 1) / kTileN) * n_wtiles, s);
+}
+
 }  // namespace
+
+SumsPlan sums_plan(int N, int K, int T) {
+  SumsPlan p{};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = off;
+    off = (off + bytes + 255) / 256 * 256;
+    return at;
+  };
+  const size_t nb = (size_t)K / 256;
+  p.status = take(16);
+  p.xg = take((size_t)T * K * 2);
+  p.sg = take(nb * 2 * (size_t)T * 16);
+  p.dg = take(nb * (size_t)T * 4);
+  p.items = take((size_t)((T + kTileN - 1) / kTileN) * (N / kTileM) * sizeof(PItem));
+  p.n_items = take(16);
+  p.total = off;
+  return p;
+}
+
+cudaError_t launch_prefill_sums(const SumsArgs& a, cudaStream_t s) {
+  return a.fmt == kQ4K ? launch_sums_t<kQ4K>(a, s) : launch_sums_t<kQ2K>(a, s);
+}
 
 size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I) {
   const int64_t EpS = E + S;

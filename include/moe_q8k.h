@@ -400,6 +400,27 @@ int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream);
 int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q,
                             int32_t T, int32_t* isum, int32_t* bsum, void* stream);
 
+/* Workspace bytes moe_debug_prefill_sums needs (0 for invalid sizes). */
+size_t moe_debug_prefill_sums_workspace_size(int32_t N, int32_t K, int32_t T);
+
+/* Test hook: the integer super-block sums that the tensor-core (prefill)
+ * path forms, for matrix w [N, K] (N a multiple of 128, K of 256) against
+ * the q8_K rows q [T, K], d [T, K/256], bsum16 [T, K/16] (as
+ * moe_q8k_quantize writes them):
+ *   S int32 [T, N, K/256] = sum_j scale_j * (sum over sub-block j of q_w * q_a)
+ *   M int32 [T, N, K/256] = sum_j min_j * (sum over sub-block j of q_a)
+ * computed by the same tcgen05 GEMM kernel and TMEM accumulators as the
+ * prefill expert FFNs (token tiles of up to 128 rows), with an epilogue that
+ * writes S and M instead of the rescaled sum.  ws: at least
+ * moe_debug_prefill_sums_workspace_size(N, K, T) bytes, 256-byte aligned.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG / UNSUPPORTED / WORKSPACE or
+ * MOE_ERR_CUDA.  Source: Pulsar README, "What it does today" (int8
+ * tensor-core expert GEMMs that keep the weights block-quantized and
+ * rescale per quant block). */
+int moe_debug_prefill_sums(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, const float* d,
+                           const int16_t* bsum16, int32_t T, int32_t* S, int32_t* M, void* ws, size_t ws_bytes,
+                           void* stream);
+
 #ifdef __cplusplus
 }
 #endif

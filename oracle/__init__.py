@@ -66,6 +66,8 @@ def _load():
             lib.orc_subblock_dots.restype = None
             lib.orc_qmatvec.argtypes = [P, I, I64, I64, P, P, I64, P, I]
             lib.orc_qmatvec.restype = None
+            lib.orc_superblock_sums.argtypes = [P, I, I64, I64, P, I64, P, P]
+            lib.orc_superblock_sums.restype = None
             lib.orc_qmatvec_absterms.argtypes = [P, I, I64, I64, P, P, I64, P, I]
             lib.orc_qmatvec_absterms.restype = None
             lib.orc_route.argtypes = [P, P, P, I64, I64, I64, I64, I, P, P, P, P, P]
@@ -140,6 +142,18 @@ def subblock_dots(w: np.ndarray, fmt: int, N: int, K: int, qa: np.ndarray):
     bsum = np.zeros((T, nb, ns), np.int32)
     _load().orc_subblock_dots(_p(w), fmt, N, K, _p(qa), T, _p(isum), _p(bsum))
     return isum, bsum
+
+
+def superblock_sums(w: np.ndarray, fmt: int, N: int, K: int, qa: np.ndarray):
+    """(S int64 [T, N, K/256], M int64 [T, N, K/256]): per super-block
+    S = sum_j sc_j * isum_j and M = sum_j mn_j * bsum_j."""
+    w = _c(w, np.uint8)
+    qa = _c(qa, np.int8)
+    T = qa.shape[0]
+    S = np.zeros((T, N, K // 256), np.int64)
+    M = np.zeros((T, N, K // 256), np.int64)
+    _load().orc_superblock_sums(_p(w), fmt, N, K, _p(qa), T, _p(S), _p(M))
+    return S, M
 
 
 def qmatvec(w: np.ndarray, fmt: int, N: int, K: int, qa: np.ndarray, da: np.ndarray,

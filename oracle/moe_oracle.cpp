@@ -284,6 +284,35 @@ void orc_subblock_dots(const uint8_t* w, int fmt, int64_t N, int64_t K, const in
     }
 }
 
+// Integer super-block sums of activation rows qa[T, K] against W[N, K], the
+// integer part of row_dot before the scales are applied:
+//   S[t][n][b] = sum_j sc_j * isum_j,  M[t][n][b] = sum_j mn_j * bsum_j  (int64)
+void orc_superblock_sums(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, int64_t T,
+                         int64_t* S, int64_t* M) {
+  int64_t nb = K / 256;
+  int ns = n_sub(fmt), sl = sub_len(fmt);
+  SuperBlock sb;
+  for (int64_t n = 0; n < N; ++n)
+    for (int64_t b = 0; b < nb; ++b) {
+      unpack_sb(w, fmt, nb, n, b, &sb);
+      for (int64_t t = 0; t < T; ++t) {
+        const int8_t* q = qa + t * K + 256 * b;
+        int64_t s = 0, m = 0;
+        for (int j = 0; j < ns; ++j) {
+          int64_t isum = 0, bsum = 0;
+          for (int i = 0; i < sl; ++i) {
+            isum += (int64_t)sb.q[j * sl + i] * q[j * sl + i];
+            bsum += q[j * sl + i];
+          }
+          s += (int64_t)sb.sc[j] * isum;
+          m += (int64_t)sb.mn[j] * bsum;
+        }
+        S[(t * N + n) * nb + b] = s;
+        M[(t * N + n) * nb + b] = m;
+      }
+    }
+}
+
 // y[T, N] = block-quantized W[N, K] applied to q8_K rows (qa[T, K], da[T, K/256]).
 void orc_qmatvec(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, const float* da,
                  int64_t T, double* y, int nthreads) {

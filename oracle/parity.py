@@ -8,10 +8,20 @@ What is compared, for sampled tokens of a layer (device arrays in, numpy):
 
   exact      q8_K codes and scales of x; expert ids (a token whose oracle gap
              l_(k) - l_(k+1), or a gap between two of its selected logits,
-             is below NEAR_TIE may differ: counted as a near-tie, not failed);
-             the bucket order (perm) of the device's own ids.
+             is below NEAR_TIE, or below twice the device's own logit error
+             of that token (checked against the bound below), may differ:
+             counted as a near-tie, not failed); the bucket order (perm) of
+             the device's own ids.
+  logits     (when the device's logits are given) against the oracle's fp64
+             logits: |dl| <= (H + 8) * u * sum_h |w_eh x_h| + u * |bias_e|,
+             the forward error bound of an fp32 dot product of length H in
+             any summation order.
   gates      the device's fp32 gates against the oracle's fp64 gates of the
-             same ids: |dg| <= GATE_RTOL * g + GATE_ATOL.
+             same ids: |dg| <= g * (2 * max_s |dl_s| + 16 u) + GATE_ATOL, the
+             first-order change of a renormalised softmax or sigmoid gate
+             under the device's own logit errors dl plus the rounding of its
+             exp and division (without the device's logits: GATE_RTOL * g +
+             GATE_ATOL).
   h codes    the q8_K codes and block scales of the device's h against the
              oracle's q8_K of its own h (fp64 rounded to fp32).  A code whose
              h sits within rounding of a .5 boundary may flip: flips are
@@ -55,14 +65,15 @@ U32 = 2.0 ** -24
 MAX_FLIP_FRAC = 1e-2
 
 
-def _routing(gpu_ids, oracle_ids, gap, logits):
-    """(near-tie tokens whose ids differ, hard mismatches [token indices])."""
+def _routing(gpu_ids, oracle_ids, gap, logits, tie):
+    """(near-tie tokens whose ids differ, hard mismatches [token indices]).
+    tie [T]: per token, the logit gap below which an order may differ."""
     mism = (gpu_ids != oracle_ids).any(axis=1)
-    allowed = gap < NEAR_TIE
+    allowed = gap < tie
     sel = np.take_along_axis(logits, oracle_ids, axis=1)
     same_set = (np.sort(gpu_ids, axis=1) == np.sort(oracle_ids, axis=1)).all(axis=1)
     if sel.shape[1] > 1:
-        inner = np.abs(np.diff(sel, axis=1)).min(axis=1) < NEAR_TIE
+        inner = np.abs(np.diff(sel, axis=1)).min(axis=1) < tie
     else:
         inner = np.zeros(len(sel), bool)
     allowed = allowed | (same_set & inner)
@@ -78,7 +89,7 @@ def check_layer(fmt, H, I, E, k, S, route_kind, experts, wr, bias, x, residual, 
     dev: device results as numpy arrays over all T tokens:
       ids [T, k], gates [T, k], perm [P] (bucket position -> slot index),
       h [P, I] (bucket order), y [P, H] (by slot index), out [T, H];
-      optional xq [T, H].
+      optional xq [T, H], logits [T, E].
     Returns (metrics dict, list of failure strings)."""
     tokens = np.asarray(tokens, np.int64)
     T = x.shape[0]
@@ -93,16 +104,36 @@ def check_layer(fmt, H, I, E, k, S, route_kind, experts, wr, bias, x, residual, 
     if "xq" in dev and not np.array_equal(dev["xq"][tokens], xq):
         fails.append(f"q8_K codes of x differ at {int((dev['xq'][tokens] != xq).sum())} positions")
     logits, rids, _, gap = route(xs, wr, bias, k, route_kind)
+    # fp32 error bound of each logit: (H + 8) u sum_h |w x| + u |bias|
+    lbound = (H + 8) * U32 * (np.abs(xs.astype(np.float64)) @ np.abs(wr.astype(np.float64)).T)
+    if bias is not None:
+        lbound += U32 * np.abs(np.asarray(bias, np.float64))[None, :]
     gids = np.ascontiguousarray(dev["ids"][tokens]).astype(np.int32)
-    near, hard = _routing(gids, rids, gap, logits)
+    lerr = None
+    if "logits" in dev:
+        l_dev = np.asarray(dev["logits"][tokens], np.float64)
+        lerr = np.abs(l_dev - logits)
+        if (lerr > lbound).any():
+            t, e = np.unravel_index(np.argmax(lerr - lbound), lerr.shape)
+            fails.append(f"logit of token {int(tokens[t])} expert {e}: |dl| {lerr[t, e]:.3e} > bound {lbound[t, e]:.3e}")
+    # a selection may differ only where the oracle's gap is below NEAR_TIE or
+    # below twice the device's own (bounded) logit error of that token
+    tie = NEAR_TIE if lerr is None else np.maximum(NEAR_TIE, 2 * lerr.max(axis=1))
+    near, hard = _routing(gids, rids, gap, logits, tie)
     if len(hard):
         t = int(hard[0])
         fails.append(f"routing differs at token {int(tokens[t])} (gap {gap[t]:.3e}): gpu {gids[t]} oracle {rids[t]}")
     _, _, g_or, _ = route(xs, wr, bias, k, route_kind, forced_ids=gids)
     g_dev = np.asarray(dev["gates"][tokens], np.float64)
-    gerr = np.abs(g_dev - g_or) - (GATE_RTOL * np.abs(g_or) + GATE_ATOL)
-    if (gerr > 0).any():
-        fails.append(f"gates beyond {GATE_RTOL:g} rel: max |dg| {np.abs(g_dev - g_or).max():.3e}")
+    if lerr is not None:
+        dl = np.take_along_axis(lerr, gids, axis=1).max(axis=1, keepdims=True)
+        gtol = np.abs(g_or) * (2 * dl + 16 * U32) + GATE_ATOL
+    else:
+        gtol = GATE_RTOL * np.abs(g_or) + GATE_ATOL
+    if (np.abs(g_dev - g_or) > gtol).any():
+        t, s_ = np.unravel_index(np.argmax(np.abs(g_dev - g_or) - gtol), g_dev.shape)
+        fails.append(f"gate of token {int(tokens[t])} slot {s_}: |dg| {abs(g_dev[t, s_] - g_or[t, s_]):.3e} > "
+                     f"{gtol[t, s_]:.3e}")
     # bucketing of every token of the call, from the device's own ids
     _, _, rperm = bucket(np.ascontiguousarray(dev["ids"]).astype(np.int32), E, S)
     perm = np.asarray(dev["perm"], np.int64)[:P]
@@ -163,6 +194,7 @@ def check_layer(fmt, H, I, E, k, S, route_kind, experts, wr, bias, x, residual, 
         fails.append(f"token {int(tokens[t])}: max |d| / ||ref|| = {rel[t]:.3e} > {REL_TOL:g}")
     metrics = {
         "tokens": int(len(tokens)),
+        "max_logit_err": None if lerr is None else float(lerr.max()),
         "max_abs_err": float(err.max()),
         "max_rel_l2_err": float(rel.max()),
         "frac_within_1e-4": float((err <= ABS_TOL).mean()),
@@ -189,5 +221,7 @@ def merge(metrics):
     for key in ("max_abs_err", "max_rel_l2_err", "max_abs_ref", "y_err_over_u_C", "out_err_over_u_A"):
         out[key] = float(max(m[key] for m in metrics))
     out["frac_within_1e-4"] = float(min(m["frac_within_1e-4"] for m in metrics))
+    le = [m["max_logit_err"] for m in metrics if m.get("max_logit_err") is not None]
+    out["max_logit_err"] = float(max(le)) if le else None
     out["bucket_exact"] = all(m["bucket_exact"] for m in metrics)
     return out

@@ -270,6 +270,7 @@ def test_layer_forward(moe, case):
     np.testing.assert_array_equal(hd, rd)
     # per-slot y and the output within the fp32 forward-error bound, h-code flips counted
     devd = dict(xq=layer.ws_view("xq", torch.int8, (T, H)).cpu().numpy(), ids=gids, gates=gates.cpu().numpy(),
+                logits=layer.ws_view("logits", torch.float32, (T, E)).cpu().numpy(),
                 perm=layer.ws_view("perm", torch.int32, (P,)).cpu().numpy(), h=h,
                 y=layer.ws_view("y", torch.float32, (P, H)).cpu().numpy(), out=out.cpu().numpy())
     tokens = np.arange(T) if T <= 64 else np.unique(np.linspace(0, T - 1, 64).round().astype(np.int64))
@@ -476,3 +477,39 @@ def test_bounded_wait_runs_out_and_reports(moe):
     out = layer.forward(dev(x)).cpu().numpy()
     ref, _, _, _ = oracle.layer_forward(FMT_Q4K, 512, 256, 8, 2, 0, 0, ex, wr, None, x)
     assert_close_rows(out, ref)
+
+
+# ------------------------------------------------------- tensor-core integer sums
+
+@pytest.mark.parametrize("fmt,N,K,T", [(FMT_Q4K, 256, 512, 200), (FMT_Q2K, 128, 768, 130), (FMT_Q4K, 128, 256, 16),
+                                       (FMT_Q2K, 256, 256, 1)])
+def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
+    """S = sum_j sc_j isum_j and M = sum_j mn_j bsum_j of every (token, row, super-block), as the tcgen05
+    GEMM forms them in TMEM, equal the oracle's int64 sums bit for bit.  Rows 0-31 carry an all-extreme
+    first super-block (largest codes, scales and mins); tokens 0-2 carry activation codes +127, -127 and
+    127 with one 126 there, so that Q4_K sums reach 63*15*127*256 > 2^24, one of them odd.  T = 200 and
+    130 leave a ragged second token tile."""
+    rng = np.random.default_rng(N + K + T + fmt)
+    q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
+    qmax, smax = (15, 63) if fmt == FMT_Q4K else (3, 15)
+    q[:32, 0] = qmax
+    sc[:32, 0] = smax
+    mn[:32, 0] = smax
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    if T >= 3:
+        x[0, :256] = 127.0
+        x[1, :256] = -127.0
+        x[2, :256] = 127.0
+        x[2, 5] = 126.0
+    xq, xd, bs = oracle.q8k_quantize(x)
+    S = torch.empty((T, N, K // 256), dtype=torch.int32, device="cuda")
+    M = torch.empty_like(S)
+    ws = torch.zeros(moe.moe_debug_prefill_sums_workspace_size(N, K, T), dtype=torch.uint8, device="cuda")
+    moe.moe_debug_prefill_sums(fmt, dev(w), N, K, dev(xq), dev(xd), dev(bs), S, M, ws)
+    torch.cuda.synchronize()
+    Sr, Mr = oracle.superblock_sums(w, fmt, N, K, xq)
+    np.testing.assert_array_equal(S.cpu().numpy(), Sr)
+    np.testing.assert_array_equal(M.cpu().numpy(), Mr)
+    if fmt == FMT_Q4K and T >= 3:
+        assert Sr[0, 0, 0] == 63 * 15 * 127 * 256 and Sr[2, 0, 0] % 2 == 1 and Sr[2, 0, 0] > 2 ** 24

@@ -91,6 +91,7 @@ def check_stack_layer(moe, wl, run, l):
     lay = moe.moe_stack_layer_layout(run["desc"], wl.layers, T, l)
     v = lambda off, dt, shape: moe.ws_view(run["ws"], off, dt, shape)
     dev = dict(xq=v(lay.xq, torch.int8, (T, H)).cpu().numpy(),
+               logits=v(lay.logits, torch.float32, (T, wl.E)).cpu().numpy(),
                ids=v(lay.ids, torch.int32, (T, k)).cpu().numpy(),
                gates=v(lay.gates, torch.float32, (T, k)).cpu().numpy(),
                perm=v(lay.slot, torch.int32, (P,)).cpu().numpy(),

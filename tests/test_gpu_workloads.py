@@ -87,6 +87,7 @@ def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0, tile_rows=False):
     need = sorted(set(gids[sel].reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
     experts = _host_experts(wl, layer, need)
     devd = dict(xq=lay.ws_view("xq", torch.int8, (T, wl.H)).cpu().numpy(), ids=gids, gates=gates.cpu().numpy(),
+                logits=lay.ws_view("logits", torch.float32, (T, wl.E)).cpu().numpy(),
                 perm=perm, h=Rows(lay.ws_view("h", torch.float32, (P, wl.I))),
                 y=Rows(lay.ws_view("y", torch.float32, (P, wl.H))), out=out.cpu().numpy())
     metrics, fails = parity.check_layer(wl.fmt, wl.H, wl.I, wl.E, wl.k, wl.S, wl.route, experts, wr, bias, x, x,

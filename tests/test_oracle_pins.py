@@ -169,6 +169,39 @@ def test_extreme_codes_stay_exact():
 
 
 @pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+def test_superblock_sums_from_fields(fmt):
+    """S = sum_j sc_j isum_j and M = sum_j mn_j bsum_j, recomputed with numpy from the encoded fields;
+    and y = sum_b d_a (d S - dmin M) reproduces qmatvec."""
+    rng = np.random.default_rng(71 + fmt)
+    N, K, T = 256, 512, 3
+    q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    xq, xd, _ = oracle.q8k_quantize(x)
+    S, M = oracle.superblock_sums(w, fmt, N, K, xq)
+    sl = 32 if fmt == FMT_Q4K else 16
+    ns = 256 // sl
+    qa = xq.reshape(T, K // 256, ns, sl).astype(np.int64)
+    qw = np.asarray(q, np.int64).reshape(N, K // 256, ns, sl)
+    isum = np.einsum("nbjs,tbjs->tnbj", qw, qa)
+    bsum = qa.sum(axis=3)
+    np.testing.assert_array_equal(S, np.einsum("nbj,tnbj->tnb", np.asarray(sc, np.int64), isum))
+    np.testing.assert_array_equal(M, np.einsum("nbj,tbj->tnb", np.asarray(mn, np.int64), bsum))
+    y = (xd.astype(np.float64)[:, None, :] * (d.astype(np.float64)[None] * S - dmin.astype(np.float64)[None] * M)).sum(axis=2)
+    np.testing.assert_allclose(oracle.qmatvec(w, fmt, N, K, xq, xd), y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
+
+
+def test_superblock_sums_extreme_block():
+    """q = 15, scale 63, min 63, activation codes all +127: S = 63 * 15 * 127 * 256 (above 2^24), M = 63 * 127 * 256."""
+    fmt, N, K = FMT_Q4K, 256, 256
+    w = fieldpack.pack_fields(fmt, N, K, np.full((N, 1, 256), 15), np.full((N, 1, 8), 63), np.full((N, 1, 8), 63),
+                              np.full((N, 1), 1.0, np.float16), np.full((N, 1), 0.5, np.float16))
+    S, M = oracle.superblock_sums(w, fmt, N, K, np.full((2, K), 127, np.int8))
+    assert (S == 63 * 15 * 127 * 256).all() and S[0, 0, 0] > 2 ** 24
+    assert (M == 63 * 127 * 256).all()
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
 def test_absterms_from_fields_brute_force(fmt):
     """qmatvec_absterms = sum over super-blocks of |d_a| (|d| |S_b| + |dmin| |M_b|), with S_b and M_b
     recomputed here from the encoded fields by plain loops; and it bounds |qmatvec| (triangle inequality)."""

@@ -102,7 +102,7 @@ def test_wrong_gate_is_reported():
     def mutate(dev, c):
         dev["gates"][1, 0] *= np.float32(1.001)
     fails = _fails_after(mutate)
-    assert any(f.startswith("gates") for f in fails)
+    assert any(f.startswith("gate of token 1 slot 0") for f in fails)
 
 
 def test_output_beyond_fp32_bound_is_reported():
