@@ -112,17 +112,17 @@ def measured_tensor_peak():
         return 1700.0, "fallback (sustained)"
 
 
-# translation unit defining each profiled kernel (plus the shared headers)
-KERNEL_SOURCES = {"decode_fused_kernel": "moe_decode.cu", "decode_stack_kernel": "moe_decode.cu",
-                  "prefill_gemm_kernel": "moe_prefill.cu",
-                  "gateup_kernel": "moe_ffn.cu"}
+# the files defining each profiled kernel (plus the shared headers)
+KERNEL_SOURCES = {"decode_fused_kernel": ["moe_decode_kernels.cuh"], "decode_stack_kernel": ["moe_decode_kernels.cuh"],
+                  "prefill_gemm_kernel": ["moe_prefill.cu"], "router_gemm_kernel": ["moe_route.cu"],
+                  "gateup_kernel": ["moe_ffn.cu"]}
 
 
 def kernel_source_hash(kernel):
     """Hash of the sources a kernel is built from, to tell whether a profile still applies."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_routed_gb300", "csrc")
-    for f in [KERNEL_SOURCES[kernel], "moe_device.cuh", "moe_internal.h"]:
+    for f in KERNEL_SOURCES[kernel] + ["moe_device.cuh", "moe_internal.h"]:
         h.update(open(os.path.join(csrc, f), "rb").read())
     h.update(open(os.path.join(ROOT, "include", "moe_q8k.h"), "rb").read())
     return h.hexdigest()[:16]
@@ -666,7 +666,7 @@ def run_ours(args, wl, T):
                   if path == moe.PATH_TENSOR_PREFILL else "int8 x int4/int2 -> int32 (dp4a) + fp32"),
         "data": "synthetic",
         "config": {"workload": wl.name, "layers": L, "T": T, "H": wl.H, "I": wl.I, "E": wl.E, "top_k": wl.k,
-                   "n_shared": wl.S, "route": ["softmax", "sigmoid"][wl.route], "fmt": ["q4_k", "q2_k"][wl.fmt],
+                   "n_shared": wl.S, "route": ["softmax", "sigmoid"][wl.route], "fmt": synth.layout.NAMES[wl.fmt],
                    "parallelism": f"replicas{world}",
                    "l2": "inputs larger than L2: each step streams %.0f MB of distinct expert weights "
                          "plus %.0f MB of router weights (L2 129 MB)" % (

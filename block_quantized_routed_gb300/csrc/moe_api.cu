@@ -43,7 +43,7 @@ bool desc_valid(const moe_layer_desc* d, int* why) {
   if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->E) return false;
   if (d->n_shared < 0 || d->n_shared > MOE_MAX_SHARED) return false;
   if (d->route != MOE_ROUTE_SOFTMAX && d->route != MOE_ROUTE_SIGMOID) return false;
-  if (d->fmt != MOE_FMT_Q4K && d->fmt != MOE_FMT_Q2K) return false;
+  if (d->fmt < MOE_FMT_Q4K || d->fmt > MOE_FMT_Q6K) return false;
   if (d->T_max < 1 || (int64_t)d->T_max * (d->top_k + d->n_shared) > (int64_t)1 << 28) return false;
   return true;
 }
@@ -97,7 +97,7 @@ WsPlan plan_workspace(const moe_layer_desc& d) {
     p.route_pub = c.take(4 * decode_route_bytes((int)T, (int)k, (int)S));
     p.route_flag = c.take(8);
   }
-  if (prefill_path(d.T_max, d.top_k, d.E) && prefill_fits(d.T_max, d)) {
+  if (prefill_path(d.T_max, d.top_k, d.E, d.fmt) && prefill_fits(d.T_max, d)) {
     p.max_pitems = (int)prefill_item_capacity((int64_t)P, d.E, d.n_shared, d.H, d.I);
     p.pitems = c.take((size_t)p.max_pitems * sizeof(PItem));
     p.n_pitems = c.take(16);
@@ -389,7 +389,7 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
   }
   if (record_error(launch_q8k_quantize(x, T, H, xq, xd, xbs, s)) != cudaSuccess) return MOE_ERR_CUDA;
   if (record_error(launch_router(x, w_router, router_bias, T, H, E, logits, s)) != cudaSuccess) return MOE_ERR_CUDA;
-  const bool use_prefill = prefill_path(T, k, E) && prefill_fits(desc->T_max, *desc);  // buffers sized by T_max
+  const bool use_prefill = prefill_path(T, k, E, desc->fmt) && prefill_fits(desc->T_max, *desc);  // buffers sized by T_max
   if (use_prefill) {
     // prefill chunk: top-k, bucketing, then the tcgen05 grouped GEMMs
     if (record_error(launch_topk(logits, T, E, k, desc->route, ids, gates, gap, s)) != cudaSuccess) return MOE_ERR_CUDA;
@@ -652,7 +652,8 @@ int moe_layer_path(const moe_layer_desc* desc, int32_t T) {
   if (T <= kDecodeMaxT && (int64_t)T * k <= kSmallPairs &&
       decode_smem_bytes(T, desc->H, desc->I, desc->E, k, desc->n_shared) <= kDecodeSmemMax)
     return MOE_PATH_DECODE_FUSED;
-  return prefill_path(T, k, desc->E) && prefill_fits(desc->T_max, *desc) ? MOE_PATH_TENSOR_PREFILL : MOE_PATH_GEMV;
+  return prefill_path(T, k, desc->E, desc->fmt) && prefill_fits(desc->T_max, *desc) ? MOE_PATH_TENSOR_PREFILL
+                                                                                      : MOE_PATH_GEMV;
 }
 
 int moe_stack_kernel(const moe_layer_desc* desc, int32_t n_layers, int32_t T, int32_t n_sms) {
@@ -677,7 +678,7 @@ int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream) {
 
 int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, int32_t T,
                             int32_t* isum, int32_t* bsum, void* stream) {
-  if (fmt != MOE_FMT_Q4K && fmt != MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED;
+  if (fmt < MOE_FMT_Q4K || fmt > MOE_FMT_Q6K) return MOE_ERR_UNSUPPORTED;
   if (N <= 0 || K <= 0 || N % 256 || K % 256 || T < 1 || T > 16) return MOE_ERR_UNSUPPORTED;
   if (!w || !q || !isum || !bsum) return MOE_ERR_INVALID_ARG;
   if (!aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;
@@ -692,7 +693,7 @@ size_t moe_debug_prefill_sums_workspace_size(int32_t N, int32_t K, int32_t T) {
 int moe_debug_prefill_sums(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, const float* d,
                            const int16_t* bsum16, int32_t T, int32_t* S, int32_t* M, void* ws, size_t ws_bytes,
                            void* stream) {
-  if (fmt != MOE_FMT_Q4K && fmt != MOE_FMT_Q2K) return MOE_ERR_UNSUPPORTED;
+  if (!prefill_format(fmt)) return MOE_ERR_UNSUPPORTED;
   if (N <= 0 || K <= 0 || T < 1) return MOE_ERR_INVALID_ARG;
   if (N % 128 || K % 256 || N > MOE_MAX_DIM || K > MOE_MAX_DIM || (int64_t)T * (K / 256) * 2 >= ((int64_t)1 << 31))
     return MOE_ERR_UNSUPPORTED;

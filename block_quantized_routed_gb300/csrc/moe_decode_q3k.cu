@@ -1,0 +1,9 @@
+// The single-launch decode kernels instantiated for the Q3_K-style format.
+#include "moe_decode_kernels.cuh"
+
+namespace moe {
+
+cudaError_t launch_decode_fused_q3k(const DecodeArgs& a, cudaStream_t s) { return launch_decode_t<kQ3K>(a, s); }
+cudaError_t launch_decode_stack_q3k(const DecodeArgs& a, cudaStream_t s) { return launch_stack_t<kQ3K>(a, s); }
+
+}  // namespace moe

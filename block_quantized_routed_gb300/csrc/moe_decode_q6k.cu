@@ -1,0 +1,9 @@
+// The single-launch decode kernels instantiated for the Q6_K-style format.
+#include "moe_decode_kernels.cuh"
+
+namespace moe {
+
+cudaError_t launch_decode_fused_q6k(const DecodeArgs& a, cudaStream_t s) { return launch_decode_t<kQ6K>(a, s); }
+cudaError_t launch_decode_stack_q6k(const DecodeArgs& a, cudaStream_t s) { return launch_stack_t<kQ6K>(a, s); }
+
+}  // namespace moe

@@ -25,31 +25,37 @@ namespace moe {
 
 constexpr int kQ4K = MOE_FMT_Q4K;
 constexpr int kQ2K = MOE_FMT_Q2K;
+constexpr int kQ5K = MOE_FMT_Q5K;
+constexpr int kQ3K = MOE_FMT_Q3K;
+constexpr int kQ6K = MOE_FMT_Q6K;
+
+// Field sizes of a format (per row of a 32-row slab): header (d | dmin << 16,
+// or d alone), scale/min bytes, code bytes; the slab places the 32 headers,
+// then the 32 scale/min records, then the 16-byte code lines.  kOff: the
+// code offset o of the symmetric formats (weight = d * sc * (q - o)).
+template <int HB, int SMB, int CB, int NSUB, int OFF>
+struct FmtBase {
+  static constexpr int kHdrBytes = HB;
+  static constexpr int kSmBytes = SMB;
+  static constexpr int kSbBytes = HB + SMB + CB;
+  static constexpr int kSlabBytes = 32 * kSbBytes;
+  static constexpr int kNSub = NSUB;
+  static constexpr int kSubLen = 256 / NSUB;
+  static constexpr int kLines = CB / 16;       // 16-byte code lines per row
+  static constexpr int kSmOff = 32 * HB;
+  static constexpr int kCodeOff = 32 * (HB + SMB);
+  static constexpr int kOff = OFF;
+  static constexpr bool kSym = OFF != 0;
+  static constexpr int kSmWords = (SMB + 3) / 4;
+};
 
 template <int FMT>
 struct Fmt;
-
-template <>
-struct Fmt<kQ4K> {
-  static constexpr int kSbBytes = 144;
-  static constexpr int kSlabBytes = 32 * 144;  // 4608
-  static constexpr int kNSub = 8;
-  static constexpr int kSubLen = 32;
-  static constexpr int kLines = 8;             // 16-byte code lines per row
-  static constexpr int kSmOff = 128;
-  static constexpr int kCodeOff = 512;
-};
-
-template <>
-struct Fmt<kQ2K> {
-  static constexpr int kSbBytes = 84;
-  static constexpr int kSlabBytes = 32 * 84;   // 2688
-  static constexpr int kNSub = 16;
-  static constexpr int kSubLen = 16;
-  static constexpr int kLines = 4;
-  static constexpr int kSmOff = 128;
-  static constexpr int kCodeOff = 640;
-};
+template <> struct Fmt<kQ4K> : FmtBase<4, 12, 128, 8, 0> {};   // 144 B, slab 4608
+template <> struct Fmt<kQ2K> : FmtBase<4, 16, 64, 16, 0> {};   // 84 B, slab 2688
+template <> struct Fmt<kQ5K> : FmtBase<4, 12, 160, 8, 0> {};   // 176 B, slab 5632
+template <> struct Fmt<kQ3K> : FmtBase<2, 12, 96, 16, 4> {};   // 110 B, slab 3520
+template <> struct Fmt<kQ6K> : FmtBase<2, 16, 192, 16, 32> {}; // 210 B, slab 6720
 
 // ---- streaming loads of weight bytes (read once: keep them out of L1) ------
 __device__ __forceinline__ uint4 ld_stream128(const void* p) {
@@ -65,22 +71,30 @@ __device__ __forceinline__ uint32_t ld_stream32(const void* p) {
   return v;
 }
 
+__device__ __forceinline__ uint32_t ld_stream16(const void* p) {
+  unsigned short v;
+  asm volatile("ld.global.nc.L1::no_allocate.u16 %0, [%1];" : "=h"(v) : "l"(p));
+  return v;
+}
+
 // ---- one row's super-block, held in registers ------------------------------
 template <int FMT>
 struct SbRegs {
   uint4 code[Fmt<FMT>::kLines];
-  uint32_t dm;                 // d | dmin << 16 (fp16 bits)
-  uint32_t sm[FMT == kQ4K ? 3 : 4];
+  uint32_t dm;                 // d | dmin << 16 (fp16 bits); d alone for the symmetric formats
+  uint32_t sm[Fmt<FMT>::kSmWords];
 };
 
-// Load super-block b of lane r's row from a slab (slab = matrix + (rg*nb + b) * kSlabBytes).
+// The header of lane r's row, the scale/min words and the code lines from a
+// slab in global memory (slab = matrix + (rg*nb + b) * kSlabBytes).
 template <int FMT>
 __device__ __forceinline__ void load_sb(const uint8_t* slab, int r, SbRegs<FMT>& s) {
   using F = Fmt<FMT>;
 #pragma unroll
   for (int l = 0; l < F::kLines; ++l) s.code[l] = ld_stream128(slab + F::kCodeOff + 512 * l + 16 * r);
-  s.dm = ld_stream32(slab + 4 * r);
-  if constexpr (FMT == kQ4K) {
+  if constexpr (F::kHdrBytes == 4) s.dm = ld_stream32(slab + 4 * r);
+  else s.dm = ld_stream16(slab + 2 * r);
+  if constexpr (F::kSmBytes == 12) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) s.sm[i] = ld_stream32(slab + F::kSmOff + 12 * r + 4 * i);
   } else {
@@ -89,24 +103,60 @@ __device__ __forceinline__ void load_sb(const uint8_t* slab, int r, SbRegs<FMT>&
   }
 }
 
-// scale and min of sub-block j
+// The same fields from a slab staged in shared memory (code lines are read
+// where they are used).
+template <int FMT>
+__device__ __forceinline__ void load_sb_head(const uint8_t* slab, int r, SbRegs<FMT>& s) {
+  using F = Fmt<FMT>;
+  if constexpr (F::kHdrBytes == 4) s.dm = *reinterpret_cast<const uint32_t*>(slab + 4 * r);
+  else s.dm = *reinterpret_cast<const uint16_t*>(slab + 2 * r);
+  if constexpr (F::kSmBytes == 12) {
+#pragma unroll
+    for (int i = 0; i < 3; ++i) s.sm[i] = *reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * r + 4 * i);
+  } else {
+    const uint4 v = *reinterpret_cast<const uint4*>(slab + F::kSmOff + 16 * r);
+    s.sm[0] = v.x; s.sm[1] = v.y; s.sm[2] = v.z; s.sm[3] = v.w;
+  }
+}
+
+// Scale and min-term coefficient of sub-block j in the raw-code form
+//   y_b = d_a * (d * sum_j sc_j * isum_j - m_scale * sum_j mn_j * bsum_j)
+// (isum_j over the raw codes): mn_j is the min (m_scale = dmin) or, for the
+// symmetric formats, o * sc_j (m_scale = d).
 template <int FMT>
 __device__ __forceinline__ void sb_scale_min(const SbRegs<FMT>& s, int j, int& sc, int& mn) {
-  if constexpr (FMT == kQ4K) {
-    // 96-bit little-endian string: scale j = bits 6j.., min j = bits 48+6j..
+  if constexpr (FMT == kQ4K || FMT == kQ5K || FMT == kQ3K) {
+    // 96-bit little-endian string: field f = bits 6f..6f+5 (Q4_K/Q5_K: scale
+    // j = field j, min j = field 8 + j; Q3_K: u_j = field j, scale u_j - 32)
     uint64_t lo = (uint64_t)s.sm[0] | ((uint64_t)s.sm[1] << 32);
     uint64_t hi = (uint64_t)(s.sm[1] >> 16) | ((uint64_t)s.sm[2] << 16);
-    sc = (int)((lo >> (6 * j)) & 63);
-    mn = (int)((hi >> (6 * j)) & 63);
-  } else {
+    if constexpr (FMT == kQ3K) {
+      const uint64_t bits = j < 8 ? lo >> (6 * j) : hi >> (6 * (j - 8));
+      sc = (int)(bits & 63) - 32;
+      mn = 4 * sc;
+    } else {
+      sc = (int)((lo >> (6 * j)) & 63);
+      mn = (int)((hi >> (6 * j)) & 63);
+    }
+  } else if constexpr (FMT == kQ2K) {
     uint32_t byte = (s.sm[j >> 2] >> (8 * (j & 3))) & 0xFF;
     sc = (int)(byte & 15);
     mn = (int)(byte >> 4);
+  } else {  // Q6_K: int8 scales
+    sc = (int)(int8_t)((s.sm[j >> 2] >> (8 * (j & 3))) & 0xFF);
+    mn = 32 * sc;
   }
 }
 
 __device__ __forceinline__ float half_lo(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w & 0xFFFF))); }
 __device__ __forceinline__ float half_hi(uint32_t w) { return __half2float(__ushort_as_half((unsigned short)(w >> 16))); }
+
+// d and the min-term scale (dmin, or d for the symmetric formats) of a header
+template <int FMT>
+__device__ __forceinline__ void sb_d_mscale(uint32_t dm, float& d, float& ms) {
+  d = half_lo(dm);
+  ms = Fmt<FMT>::kSym ? d : half_hi(dm);
+}
 
 // ---- the integer sub-block dot, shared by every kernel and the test hook ----
 // Q4_K-style code line j: byte i = code i (low nibble) | code i+16 (high
@@ -150,18 +200,118 @@ __device__ __forceinline__ int isum_q2k(const uint32_t (&w)[4], const int4 a) {
   return i;
 }
 
-// Integer dot of sub-block j with the 256 activation codes of the same block.
+// The raw codes of sub-block j as bytes of 32-bit words, in the order of the
+// activation codes they meet (word k = codes 4k..4k+3 of the sub-block; for
+// 32-code sub-blocks words 0-3 are codes 0..15 and words 4-7 codes 16..31).
+// line(l) gives the row's 16-byte code line l (from registers or shared
+// memory).  The bit placement is that of synth/layout.py.
+template <int FMT, class Line>
+__device__ __forceinline__ void sub_words(Line line, int j, uint32_t (&w)[Fmt<FMT>::kSubLen / 4]) {
+  if constexpr (FMT == kQ4K || FMT == kQ5K) {
+    uint32_t lo[4], hi[4];
+    mask_q4k(line(j), lo, hi);
+    if constexpr (FMT == kQ5K) {  // 5th bits: line 8 + j/4, bit 2(j%4) + h of byte i -> code i + 16h
+      const uint4 h = line(8 + (j >> 2));
+      const uint32_t hw[4] = {h.x, h.y, h.z, h.w};
+      const int sh = 2 * (j & 3);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        lo[k] |= ((hw[k] >> sh) & 0x01010101u) << 4;
+        hi[k] |= ((hw[k] >> (sh + 1)) & 0x01010101u) << 4;
+      }
+    }
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      w[k] = lo[k];
+      w[4 + k] = hi[k];
+    }
+  } else if constexpr (FMT == kQ2K || FMT == kQ3K) {
+    mask_q2k(line(j >> 2), j, w);
+    if constexpr (FMT == kQ3K) {  // 3rd bits: word (j/2)%4 of line 4 + j/8, bit p + 4(j%2) of byte m -> code 4p + m
+      const uint4 h = line(4 + (j >> 3));
+      const int wi = (j >> 1) & 3;
+      const uint32_t hv = wi == 0 ? h.x : wi == 1 ? h.y : wi == 2 ? h.z : h.w;
+      const int sh = 4 * (j & 1);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) w[p] |= ((hv >> (p + sh)) & 0x01010101u) << 2;
+    }
+  } else {  // Q6_K: low nibbles in line j/2 (nibble j%2), high 2 bits in line 8 + j/4 (bits 2(j%4)..)
+    const uint4 lo = line(j >> 1), hi = line(8 + (j >> 2));
+    const uint32_t lw[4] = {lo.x, lo.y, lo.z, lo.w}, hw[4] = {hi.x, hi.y, hi.z, hi.w};
+    const int sl = 4 * (j & 1), sh = 2 * (j & 3);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) w[k] = ((lw[k] >> sl) & 0x0F0F0F0Fu) | (((hw[k] >> sh) & 0x03030303u) << 4);
+  }
+}
+
+// dp4a of a sub-block's code words with its activation codes (a: the first
+// code of the sub-block, 16-byte aligned)
+template <int NW>
+__device__ __forceinline__ int words_dot(const uint32_t (&w)[NW], const int8_t* a) {
+  int i = 0;
+#pragma unroll
+  for (int k = 0; k < NW; k += 4) {
+    const int4 v = *reinterpret_cast<const int4*>(a + 4 * k);
+    i = __dp4a((int)w[k], v.x, i);
+    i = __dp4a((int)w[k + 1], v.y, i);
+    i = __dp4a((int)w[k + 2], v.z, i);
+    i = __dp4a((int)w[k + 3], v.w, i);
+  }
+  return i;
+}
+
+// Integer dot of sub-block j (raw codes) with the 256 activation codes of the same block.
 template <int FMT>
 __device__ __forceinline__ int sub_isum(const SbRegs<FMT>& s, int j, const int8_t* act) {
-  if constexpr (FMT == kQ4K) {
-    uint32_t lo[4], hi[4];
-    mask_q4k(s.code[j], lo, hi);
-    return isum_q4k(lo, hi, *reinterpret_cast<const int4*>(act + 32 * j),
-                    *reinterpret_cast<const int4*>(act + 32 * j + 16));
-  } else {
-    uint32_t w[4];
-    mask_q2k(s.code[j >> 2], j, w);
-    return isum_q2k(w, *reinterpret_cast<const int4*>(act + 16 * j));
+  using F = Fmt<FMT>;
+  uint32_t w[F::kSubLen / 4];
+  sub_words<FMT>([&](int l) { return s.code[l]; }, j, w);
+  return words_dot(w, act + F::kSubLen * j);
+}
+
+// Sum of the 16-code sums of sub-block j (one or two of them)
+template <int FMT>
+__device__ __forceinline__ int sub_bsum(const int16_t* bsp, int j) {
+  if constexpr (Fmt<FMT>::kSubLen == 32) return (int)bsp[2 * j] + (int)bsp[2 * j + 1];
+  else return (int)bsp[j];
+}
+
+// One super-block's contribution to `cnt` tokens for the Q5_K/Q3_K/Q6_K-style
+// formats; the code words of every sub-block come from line(l) once per
+// super-block.  Asymmetric: d_a (d sum sc isum - dmin sum mn bsum); symmetric:
+// d_a d sum_j sc_j (isum_j - o bsum_j), the offset applied in integers.
+template <int FMT, class Line>
+__device__ __forceinline__ void sb_accum_words(Line line, const SbRegs<FMT>& s, const int8_t* act, const int16_t* bs,
+                                               const float* d, const int* act_off, int b, int cnt, float* acc,
+                                               int lane) {
+  using F = Fmt<FMT>;
+  constexpr int NW = F::kSubLen / 4;
+  int sc[F::kNSub], mn[F::kNSub];
+#pragma unroll
+  for (int j = 0; j < F::kNSub; ++j) sb_scale_min<FMT>(s, j, sc[j], mn[j]);
+  float dw, ms;
+  sb_d_mscale<FMT>(s.dm, dw, ms);
+  uint32_t wd[F::kNSub][NW];
+#pragma unroll
+  for (int j = 0; j < F::kNSub; ++j) sub_words<FMT>(line, j, wd[j]);
+#pragma unroll 1
+  for (int t = 0; t < cnt; ++t) {
+    const int o = act_off[t];
+    const int8_t* a = act + o + 256 * b;
+    const int16_t* bsp = bs + o / 16 + 16 * b;
+    int S = 0, M = 0;
+#pragma unroll
+    for (int j = 0; j < F::kNSub; ++j) {
+      const int isum = words_dot(wd[j], a + F::kSubLen * j);
+      if constexpr (F::kSym) {
+        S += sc[j] * (isum - F::kOff * sub_bsum<FMT>(bsp, j));
+      } else {
+        S += sc[j] * isum;
+        M += mn[j] * sub_bsum<FMT>(bsp, j);
+      }
+    }
+    if constexpr (F::kSym) acc[t * 32 + lane] += d[o / 256 + b] * (dw * (float)S);
+    else acc[t * 32 + lane] += d[o / 256 + b] * fmaf(dw, (float)S, -ms * (float)M);
   }
 }
 
@@ -178,6 +328,9 @@ template <int FMT>
 __device__ __forceinline__ void sb_accum(const SbRegs<FMT>& s, const int8_t* act, const int16_t* bs, const float* d,
                                          const int* act_off, int b, int cnt, float* acc, int lane) {
   using F = Fmt<FMT>;
+  if constexpr (FMT != kQ4K && FMT != kQ2K) {
+    sb_accum_words<FMT>([&](int l) { return s.code[l]; }, s, act, bs, d, act_off, b, cnt, acc, lane);
+  } else {
   int sc[F::kNSub], mn[F::kNSub];
 #pragma unroll
   for (int j = 0; j < F::kNSub; ++j) sb_scale_min<FMT>(s, j, sc[j], mn[j]);
@@ -218,6 +371,7 @@ __device__ __forceinline__ void sb_accum(const SbRegs<FMT>& s, const int8_t* act
       }
       acc[t * 32 + lane] += d[o / 256 + b] * fmaf(dw, (float)S, -dmin * (float)M);
     }
+  }
   }
 }
 

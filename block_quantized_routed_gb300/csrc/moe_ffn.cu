@@ -304,7 +304,14 @@ int pick_tile_tokens(int T, int H) {
 }
 
 cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
-  return a.fmt == kQ4K ? launch_ffn_t<kQ4K>(a, s) : launch_ffn_t<kQ2K>(a, s);
+  switch (a.fmt) {
+    case kQ4K: return launch_ffn_t<kQ4K>(a, s);
+    case kQ2K: return launch_ffn_t<kQ2K>(a, s);
+    case kQ5K: return launch_ffn_t<kQ5K>(a, s);
+    case kQ3K: return launch_ffn_t<kQ3K>(a, s);
+    case kQ6K: return launch_ffn_t<kQ6K>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 cudaError_t launch_combine(const float* y, const float* gates, int T, int H, int k, int S, const float* residual,
@@ -342,10 +349,14 @@ cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t
                               int32_t* bsum, cudaStream_t s) {
   const int blocks = (N / 32) * (K / 256);
   note_launch();
-  if (fmt == kQ4K)
-    debug_dots_kernel<kQ4K><<<blocks, 32, 0, s>>>(static_cast<const uint8_t*>(w), N, K, q, T, isum, bsum);
-  else
-    debug_dots_kernel<kQ2K><<<blocks, 32, 0, s>>>(static_cast<const uint8_t*>(w), N, K, q, T, isum, bsum);
+  const uint8_t* wb = static_cast<const uint8_t*>(w);
+  switch (fmt) {
+    case kQ4K: debug_dots_kernel<kQ4K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    case kQ2K: debug_dots_kernel<kQ2K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    case kQ5K: debug_dots_kernel<kQ5K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    case kQ3K: debug_dots_kernel<kQ3K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    default: debug_dots_kernel<kQ6K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+  }
   return cudaGetLastError();
 }
 

@@ -165,6 +165,17 @@ struct RouteFields {
 };
 RouteFields route_fields(int T, int k, int S);
 cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s);
+// the same two launches per weight format (moe_decode_<fmt>.cu)
+cudaError_t launch_decode_fused_q4k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_q2k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_q5k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_q3k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_q6k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_q4k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_q2k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_q5k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_q3k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_q6k(const DecodeArgs& a, cudaStream_t s);
 // largest token count of the single-launch decode path
 constexpr int kDecodeMaxT = 16;
 
@@ -172,8 +183,14 @@ constexpr int kDecodeMaxT = 16;
 // Experts must average at least this many routed tokens for the tcgen05
 // grouped GEMM to beat the dp4a GEMV kernels.
 constexpr int kPrefillMinTokensPerExpert = 16;
-inline bool prefill_path(int64_t T, int k, int E) {
-  return T * k > kSmallPairs && T * k >= (int64_t)kPrefillMinTokensPerExpert * E;
+// Formats the tensor-core path takes: their scale * code products are exact
+// fp16 integers (|sc * q| <= 2048) and their half super-block sums stay
+// below 2^24 (Q4_K/Q2_K/Q3_K-style).  The Q5_K-style (63 * 31 * 127 * 128
+// > 2^24 per half) and Q6_K-style (|127 * 63| > 2048) formats run their
+// large batches on the dp4a GEMV kernels.
+inline bool prefill_format(int fmt) { return fmt == MOE_FMT_Q4K || fmt == MOE_FMT_Q2K || fmt == MOE_FMT_Q3K; }
+inline bool prefill_path(int64_t T, int k, int E, int fmt) {
+  return prefill_format(fmt) && T * k > kSmallPairs && T * k >= (int64_t)kPrefillMinTokensPerExpert * E;
 }
 // TMA coordinates are 32-bit: the code-sum plane has (max(H, I)/256) * 2 * P rows
 inline bool prefill_fits(int64_t T, const moe_layer_desc& d) {

@@ -5,7 +5,7 @@
 // block-quantized in HBM and are expanded on chip; the arithmetic is exact
 // integer arithmetic carried by fp16 operands:
 //
-//   A (weights)     sc_j * q  for each weight of sub-block j   (<= 945: exact in fp16)
+//   A (weights)     sc_j * q  for each weight of sub-block j   (|.| <= 945: exact in fp16)
 //   B (activations) the q8_K codes of the tokens               (|q| <= 127: exact)
 //   S[m, n, b] = sum over the 256 columns of super-block b of A * B
 //
@@ -33,7 +33,12 @@
 // pages' prefill design reaches it with int8 MMA (Pulsar README, "What it
 // does today"; Strata, 0.1.13 prefill notes: grouped int8 tensor-core expert
 // GEMM that unpacks super-blocks to shared memory and rescales per block).
-// tcgen05 offers no int8 kind on sm_103a, hence exact-integer fp16.
+// tcgen05 offers no int8 kind on sm_103a, hence exact-integer fp16.  The
+// Q4_K, Q2_K and Q3_K-style formats run here; for the Q3_K-style format
+// (weight = d * sc * (q - 4), sc = u - 32) A = sc * q and the min term
+// carries 4 * sc with scale d.  (Q5_K-style products reach 63 * 31 per
+// weight and 3.2e7 per half super-block, Q6_K-style 127 * 63 per weight:
+// beyond the exact range, so those formats take the dp4a GEMV kernels.)
 //
 // Kernel organisation (one persistent CTA per SM, 832 threads, warp roles):
 //   warp 24      producer: cp.async.bulk of the raw weight slabs and TMA
@@ -572,8 +577,9 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         uint8_t* a2 = sm + kSmA2 + rs * 4096;
         // scales and mins, extracted on demand (no per-thread arrays)
         uint64_t sm_lo, sm_hi;
-        if constexpr (FMT == kQ4K) {
-          // 96-bit string: scale j = bits 6j.., min j = bits 48 + 6j..
+        if constexpr (FMT == kQ4K || FMT == kQ3K) {
+          // 96-bit string of 6-bit fields: field f = bits 6f.. (Q4_K: scale j = f j,
+          // min j = f 8 + j; Q3_K: u_j = f j, scale u_j - 32); sm_hi = bits 48..
           const uint32_t* smw = reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * lr);
           sm_lo = (uint64_t)smw[0] | ((uint64_t)smw[1] << 32);
           sm_hi = (uint64_t)(smw[1] >> 16) | ((uint64_t)smw[2] << 16);
@@ -585,10 +591,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         }
         auto scale_of = [&](int j) -> int {
           if constexpr (FMT == kQ4K) return (int)((sm_lo >> (6 * j)) & 63);
+          else if constexpr (FMT == kQ3K) return (int)(((j < 8 ? sm_lo >> (6 * j) : sm_hi >> (6 * (j - 8)))) & 63) - 32;
           else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7))) & 15);
         };
+        // the min-term coefficient: the min, or o * scale (Q3_K-style, o = 4)
         auto min_of = [&](int j) -> int {
           if constexpr (FMT == kQ4K) return (int)((sm_hi >> (6 * j)) & 63);
+          else if constexpr (FMT == kQ3K) return 4 * scale_of(j);
           else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7) + 4)) & 15);
         };
         {
@@ -626,11 +635,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             }
           } else {
             const uint4 line = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * (2 * c + hx) + 16 * lr);
+            uint4 hline = make_uint4(0u, 0u, 0u, 0u);  // Q3_K-style: the 3rd bits of sub-blocks 8c .. 8c + 7
+            if constexpr (FMT == kQ3K) hline = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * (4 + c) + 16 * lr);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               const int j = 8 * c + 4 * hx + q;  // sub-block of 16 codes
               uint32_t w[4];
               mask_q2k(line, q, w);
+              if constexpr (FMT == kQ3K) {
+                // word (j/2) % 4 = 2 hx + q/2 of the line; bit p + 4 (j % 2) of byte m -> code 4p + m
+                const int wi = 2 * hx + (q >> 1);
+                const uint32_t hv = wi == 0 ? hline.x : wi == 1 ? hline.y : wi == 2 ? hline.z : hline.w;
+#pragma unroll
+                for (int p = 0; p < 4; ++p) w[p] |= ((hv >> (p + 4 * (q & 1))) & 0x01010101u) << 2;
+              }
               const float scf = (float)scale_of(j);
               const __half2 sc2 = __float2half2_rn(scf);
               const __half2 off2 = __float2half2_rn(-1024.0f * scf);
@@ -718,14 +736,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       else ep = a.table[it.expert];
       const int ntok = it.count;
       const int N = (ntok + 15) / 16 * 16;
-      const uint8_t* hdr;  // d/dmin word of this row's super-block 0
+      const uint8_t* hdr;  // header (d | dmin, or d) of this row's super-block 0
       if (MODE == 0) {
         const int i = it.wtile * 64 + (m >> 1);
-        hdr = static_cast<const uint8_t*>((m & 1) ? ep.up : ep.gate) + (size_t)(i >> 5) * nb * slab_bytes + 4 * (i & 31);
+        hdr = static_cast<const uint8_t*>((m & 1) ? ep.up : ep.gate) + (size_t)(i >> 5) * nb * slab_bytes +
+              F::kHdrBytes * (i & 31);
       } else {
         const int i = it.wtile * 128 + m;
-        hdr = static_cast<const uint8_t*>(ep.down) + (size_t)(i >> 5) * nb * slab_bytes + 4 * (i & 31);
+        hdr = static_cast<const uint8_t*>(ep.down) + (size_t)(i >> 5) * nb * slab_bytes + F::kHdrBytes * (i & 31);
       }
+      auto ld_hdr = [&](const uint8_t* p) -> uint32_t {
+        if constexpr (F::kHdrBytes == 4) return __ldg(reinterpret_cast<const uint32_t*>(p));
+        else return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
+      };
       unsigned long long acc[16];  // pairs of local tokens (2i, 2i+1)
 #pragma unroll
       for (int j = 0; j < 16; ++j) acc[j] = 0ull;
@@ -735,21 +758,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       const int slot = (MODE == 1 && vt) ? __ldg(a.perm + it.start + tk) : 0;  // down: its slot row
       const float* dgp = a.dg + it.start + tk;
       // the scales of block b + 1 are loaded while block b is processed
-      uint32_t dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr));
+      uint32_t dm_n = ld_hdr(hdr);
       float da_n = vt ? __ldg(dgp) : 0.0f;
       for (int b = 0; b < nb; ++b) {
         const int ab = tb & 1;
         const uint32_t dm = dm_n;
         const float da = da_n;
         if (b + 1 < nb) {
-          dm_n = __ldg(reinterpret_cast<const uint32_t*>(hdr + (size_t)(b + 1) * slab_bytes));
+          dm_n = ld_hdr(hdr + (size_t)(b + 1) * slab_bytes);
           da_n = vt ? __ldg(dgp + (int64_t)(b + 1) * a.P) : 0.0f;
         }
         if (!(ok = warp_wait(tfull(ab), (tb >> 1) & 1, abort_flag, a.status, w0, kEpilogueSleepNs))) break;
         tc_fence_after();
         s_da[lane] = da;
         __syncwarp();
-        const float dw = half_lo(dm), dmin = half_hi(dm);
+        float dw, dmin;  // d and the min-term scale (dmin, or d for the Q3_K-style format)
+        sb_d_mscale<FMT>(dm, dw, dmin);
         const unsigned long long dw2 = f2_pack(dw, dw), ndm2 = f2_pack(-dmin, -dmin);
         const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
         const uint32_t tS0 = tl + tmem_region(3 * tb), tS1 = tl + tmem_region(3 * tb + 1),
@@ -1021,7 +1045,12 @@ SumsPlan sums_plan(int N, int K, int T) {
 }
 
 cudaError_t launch_prefill_sums(const SumsArgs& a, cudaStream_t s) {
-  return a.fmt == kQ4K ? launch_sums_t<kQ4K>(a, s) : launch_sums_t<kQ2K>(a, s);
+  switch (a.fmt) {
+    case kQ4K: return launch_sums_t<kQ4K>(a, s);
+    case kQ2K: return launch_sums_t<kQ2K>(a, s);
+    case kQ3K: return launch_sums_t<kQ3K>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I) {
@@ -1030,7 +1059,12 @@ size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I) {
 }
 
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s) {
-  return a.fmt == kQ4K ? launch_prefill_fmt<kQ4K>(a, s) : launch_prefill_fmt<kQ2K>(a, s);
+  switch (a.fmt) {
+    case kQ4K: return launch_prefill_fmt<kQ4K>(a, s);
+    case kQ2K: return launch_prefill_fmt<kQ2K>(a, s);
+    case kQ3K: return launch_prefill_fmt<kQ3K>(a, s);
+    default: return cudaErrorInvalidValue;
+  }
 }
 
 }  // namespace moe

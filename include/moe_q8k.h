@@ -23,16 +23,24 @@
  *  - Results are deterministic: no floating-point atomics; every sum is taken
  *    in a fixed order.
  *
- * Matrix byte format (both formats): W[N, K] with N, K multiples of 256 is a
+ * Matrix byte format (every format): W[N, K] with N, K multiples of 256 is a
  * sequence of "slabs", one per (row group of 32 rows, 256-column super-block),
  * row-group-major.  A slab holds the super-blocks of its 32 rows field by
- * field: 32 x {fp16 d, fp16 dmin} words, then the 32 scale/min records, then
- * the code lines (16 bytes per row per line).  Full bit-level description:
- * synth/layout.py.  Q4_K-style: 144 bytes per super-block, 4-bit codes,
- * eight 32-weight sub-blocks with 6-bit scale and min.  Q2_K-style: 84 bytes
- * per super-block, 2-bit codes, sixteen 16-weight sub-blocks with 4-bit scale
- * and min.  weight = d * scale_j * q - dmin * min_j.  Every matrix pointer
- * must be 16-byte aligned.
+ * field: 32 headers ({fp16 d, fp16 dmin} words, or fp16 d alone), then the
+ * 32 scale/min records, then the code lines (16 bytes per row per line).
+ * Full bit-level description: synth/layout.py.
+ *   Q4_K-style: 144 bytes per super-block, 4-bit codes, eight 32-weight
+ *     sub-blocks with 6-bit scale and min; weight = d*scale_j*q - dmin*min_j.
+ *   Q2_K-style: 84 bytes, 2-bit codes, sixteen 16-weight sub-blocks with
+ *     4-bit scale and min; weight = d*scale_j*q - dmin*min_j.
+ *   Q5_K-style: 176 bytes, as Q4_K-style with 5-bit codes.
+ *   Q3_K-style: 110 bytes, 3-bit codes, sixteen sub-blocks with 6-bit scales
+ *     u_j; weight = d*(u_j - 32)*(q - 4).
+ *   Q6_K-style: 210 bytes, 6-bit codes, sixteen sub-blocks with int8 scales;
+ *     weight = d*scale_j*(q - 32).
+ * (Pulsar README, "What it does today": Q4_K/Q6_K matmuls on q8_K
+ * activations; "Get a model": q3_K/q5_K/q6_K tensors; the "-style" layouts
+ * are this library's own.)  Every matrix pointer must be 16-byte aligned.
  */
 #ifndef MOE_Q8K_H
 #define MOE_Q8K_H
@@ -59,7 +67,13 @@ extern "C" {
 #define MOE_MAX_TOPK 16      /* top_k                                      */
 #define MOE_MAX_DIM 16384    /* H and I                                    */
 
-typedef enum { MOE_FMT_Q4K = 0, MOE_FMT_Q2K = 1 } moe_wfmt;
+typedef enum {
+  MOE_FMT_Q4K = 0, /* Q4_K-style: 144 B per super-block                            */
+  MOE_FMT_Q2K = 1, /* Q2_K-style: 84 B                                             */
+  MOE_FMT_Q5K = 2, /* Q5_K-style: 176 B (Q4_K-style with 5-bit codes)             */
+  MOE_FMT_Q3K = 3, /* Q3_K-style: 110 B, 3-bit codes, signed 6-bit scales, no min  */
+  MOE_FMT_Q6K = 4  /* Q6_K-style: 210 B, 6-bit codes, int8 scales, no min          */
+} moe_wfmt;
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID = 1 } moe_route_kind;
 
 /* Shape of one MoE layer. */
@@ -117,7 +131,8 @@ typedef struct {
                       holding the gate/up of layer L-2: [0] stage start, [3]
                       x staged, [4] gate/up, [6] down of the layer before,
                       [1] router of layer+2, [8] combine, [12] next layer's
-                      routing taken and its experts prefetched             */
+                      routing taken and its experts prefetched; [14] the
+                      grid size (CTAs) of the single-launch kernel         */
   size_t total;    /* bytes required                                           */
 } moe_ws_layout;
 

@@ -26,9 +26,12 @@ _lib = None
 
 FMT_Q4K = 0
 FMT_Q2K = 1
+FMT_Q5K = 2
+FMT_Q3K = 3
+FMT_Q6K = 4
 ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID = 1
-N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16}
+N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16}
 
 
 def build(force: bool = False) -> str:
@@ -100,7 +103,8 @@ def half_to_double(bits: int) -> float:
 
 
 def unpack_sb(w: np.ndarray, fmt: int, N: int, K: int, n: int, b: int):
-    """Fields of super-block (row n, block b): (q[256], sc[ns], mn[ns], d, dmin)."""
+    """Fields of super-block (row n, block b): (q[256], sc[ns], mn[ns], d, dmin);
+    mn and dmin are 0 for the formats without a min."""
     w = _c(w, np.uint8)
     q = np.zeros(256, np.int32)
     sc = np.zeros(N_SUB[fmt], np.int32)

@@ -31,7 +31,14 @@
 // super-block fields (fp16 d, fp16 dmin, per-sub-block scale and min, codes;
 // w = d*scale*q - dmin*min), the q8_K rule (d = max|x|/127 in fp32,
 // q = round-half-away(x/d)) and the byte placement (synth/layout.py) are the
-// workload definitions this oracle follows.
+// workload definitions this oracle follows.  The Q5_K/Q3_K/Q6_K-style
+// formats (Pulsar README, "What it does today": Q4_K/Q6_K matmuls; "Get a
+// model": q3_K/q5_K/q6_K tensors) are this project's reading of those names:
+// Q5_K-style = Q4_K-style with 5-bit codes; Q3_K-style: 16 sub-blocks, 3-bit
+// codes, 6-bit signed scales, w = d*scale*(q - 4); Q6_K-style: 16
+// sub-blocks, 6-bit codes, int8 scales, w = d*scale*(q - 32).  In general
+// w = d*scale*(q - o) - dmin*min, with o = 0 and a min for the first three
+// formats and o = 4 / 32 and no min (no dmin) for the last two.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -43,10 +50,28 @@ namespace {
 
 constexpr int kQ4K = 0;
 constexpr int kQ2K = 1;
+constexpr int kQ5K = 2;
+constexpr int kQ3K = 3;
+constexpr int kQ6K = 4;
 
-int n_sub(int fmt) { return fmt == kQ4K ? 8 : 16; }
-int sub_len(int fmt) { return fmt == kQ4K ? 32 : 16; }
-int64_t slab_bytes(int fmt) { return fmt == kQ4K ? 4608 : 2688; }
+// Per format: sub-blocks, header bytes per row (d|dmin or d), scale/min
+// bytes per row, code bytes per row, code offset o.  A slab holds the 32
+// rows' headers, then their scale/min bytes, then the code lines.
+int n_sub(int fmt) { return (fmt == kQ4K || fmt == kQ5K) ? 8 : 16; }
+int sub_len(int fmt) { return 256 / n_sub(fmt); }
+int hdr_bytes(int fmt) { return (fmt == kQ3K || fmt == kQ6K) ? 2 : 4; }
+int sm_bytes(int fmt) { return (fmt == kQ2K || fmt == kQ6K) ? 16 : 12; }
+int code_bytes(int fmt) {
+  switch (fmt) {
+    case kQ4K: return 128;
+    case kQ2K: return 64;
+    case kQ5K: return 160;
+    case kQ3K: return 96;
+    default: return 192;
+  }
+}
+int code_offset(int fmt) { return fmt == kQ3K ? 4 : fmt == kQ6K ? 32 : 0; }
+int64_t slab_bytes(int fmt) { return 32 * (int64_t)(hdr_bytes(fmt) + sm_bytes(fmt) + code_bytes(fmt)); }
 
 // IEEE 754 binary16 -> double, written out from the format definition.
 double half_to_double(uint16_t h) {
@@ -78,9 +103,10 @@ int read_bits(const uint8_t* p, int start, int len) {
 }
 
 struct SuperBlock {
-  int q[256];   // codes
-  int sc[16];   // per-sub-block scale
-  int mn[16];   // per-sub-block min
+  int q[256];   // codes (unsigned)
+  int sc[16];   // per-sub-block scale (signed for Q3_K/Q6_K-style)
+  int mn[16];   // per-sub-block min (0 where the format has none)
+  int off;      // code offset o: w = d * sc * (q - o) - dmin * mn
   double d, dmin;
 };
 
@@ -89,34 +115,68 @@ void unpack_sb(const uint8_t* w, int fmt, int64_t nb, int64_t n, int64_t b, Supe
   int64_t rg = n / 32;
   int r = (int)(n % 32);
   const uint8_t* slab = w + (rg * nb + b) * slab_bytes(fmt);
-  uint32_t dm = read_le32(slab + 4 * r);
-  o->d = half_to_double((uint16_t)(dm & 0xFFFF));
-  o->dmin = half_to_double((uint16_t)(dm >> 16));
-  if (fmt == kQ4K) {
-    const uint8_t* sm = slab + 128 + 12 * r;
+  const int hb = hdr_bytes(fmt), smb = sm_bytes(fmt);
+  const uint8_t* sm = slab + 32 * hb + smb * r;
+  // code line l of this row
+  auto line = [&](int l) { return slab + 32 * (hb + smb) + 512 * l + 16 * r; };
+  if (hb == 4) {
+    uint32_t dm = read_le32(slab + 4 * r);
+    o->d = half_to_double((uint16_t)(dm & 0xFFFF));
+    o->dmin = half_to_double((uint16_t)(dm >> 16));
+  } else {
+    o->d = half_to_double((uint16_t)(slab[2 * r] | (slab[2 * r + 1] << 8)));
+    o->dmin = 0.0;
+  }
+  o->off = code_offset(fmt);
+  for (int j = 0; j < 16; ++j) o->mn[j] = 0;
+  if (fmt == kQ4K || fmt == kQ5K) {
     for (int j = 0; j < 8; ++j) {
       o->sc[j] = read_bits(sm, 6 * j, 6);
       o->mn[j] = read_bits(sm, 48 + 6 * j, 6);
     }
-    for (int j = 0; j < 8; ++j) {
-      const uint8_t* line = slab + 512 + 512 * j + 16 * r;
+    for (int j = 0; j < 8; ++j)
       for (int i = 0; i < 16; ++i) {
-        o->q[32 * j + i] = line[i] & 15;
-        o->q[32 * j + 16 + i] = line[i] >> 4;
+        o->q[32 * j + i] = line(j)[i] & 15;
+        o->q[32 * j + 16 + i] = line(j)[i] >> 4;
       }
-    }
-  } else {
-    const uint8_t* sm = slab + 128 + 16 * r;
+    if (fmt == kQ5K)  // 5th bits: line 8 + j/4, byte i, bit 2*(j%4) + h -> code i + 16h of sub-block j
+      for (int j = 0; j < 8; ++j)
+        for (int i = 0; i < 16; ++i)
+          for (int h = 0; h < 2; ++h)
+            o->q[32 * j + 16 * h + i] |= ((line(8 + j / 4)[i] >> (2 * (j % 4) + h)) & 1) << 4;
+  } else if (fmt == kQ2K || fmt == kQ3K) {
+    if (fmt == kQ2K)
+      for (int j = 0; j < 16; ++j) {
+        o->sc[j] = sm[j] & 15;
+        o->mn[j] = sm[j] >> 4;
+      }
+    else
+      for (int j = 0; j < 16; ++j) o->sc[j] = read_bits(sm, 6 * j, 6) - 32;
+    // low 2 bits: sub-block j in line j/4, bytes 4*(j%4)..: bits 2p.. of byte m = code 4p + m
     for (int j = 0; j < 16; ++j) {
-      o->sc[j] = sm[j] & 15;
-      o->mn[j] = sm[j] >> 4;
-    }
-    for (int j = 0; j < 16; ++j) {
-      const uint8_t* base = slab + 640 + 512 * (j / 4) + 16 * r + 4 * (j % 4);
+      const uint8_t* base = line(j / 4) + 4 * (j % 4);
       for (int c = 0; c < 16; ++c) o->q[16 * j + c] = (base[c % 4] >> (2 * (c / 4))) & 3;
     }
+    if (fmt == kQ3K)  // 3rd bits: line 4 + j/8, bytes 4*((j/2)%4)..: bit p + 4*(j%2) of byte m -> code 4p + m
+      for (int j = 0; j < 16; ++j) {
+        const uint8_t* base = line(4 + j / 8) + 4 * ((j / 2) % 4);
+        for (int c = 0; c < 16; ++c) o->q[16 * j + c] |= ((base[c % 4] >> (c / 4 + 4 * (j % 2))) & 1) << 2;
+      }
+  } else {  // Q6_K-style
+    for (int j = 0; j < 16; ++j) o->sc[j] = (int)(int8_t)sm[j];
+    for (int j = 0; j < 16; ++j)
+      for (int i = 0; i < 16; ++i) {
+        const int lo = (line(j / 2)[i] >> (4 * (j % 2))) & 15;
+        const int hi = (line(8 + j / 4)[i] >> (2 * (j % 4))) & 3;
+        o->q[16 * j + i] = lo | (hi << 4);
+      }
   }
 }
+
+// The min-term coefficient of sub-block j and its scale in the raw-code
+// decomposition: mn_j with dmin, or o * sc_j with d for the symmetric formats.
+int m_coef(const SuperBlock& sb, int j) { return sb.off ? sb.off * sb.sc[j] : sb.mn[j]; }
+double m_scale(const SuperBlock& sb) { return sb.off ? sb.d : sb.dmin; }
 
 // Run f(i) for i in [0, n) on up to nthreads threads (contiguous ranges).
 template <class F>
@@ -156,7 +216,7 @@ void q8k_block(const float* x, int8_t* q, float* d) {
 
 // y[n] for one activation row (codes qa[K], scales da[K/256]):
 //   y[n] = sum_b da[b] * (d_w * sum_j sc_j * isum_j  -  dmin * sum_j mn_j * bsum_j)
-// with isum_j = sum over sub-block j of q_w * q_a and bsum_j = sum of q_a.
+// with isum_j = sum over sub-block j of (q_w - o) * q_a and bsum_j = sum of q_a.
 double row_dot(const uint8_t* w, int fmt, int64_t nb, int64_t n, const int8_t* qa, const float* da) {
   SuperBlock sb;
   double acc = 0.0;
@@ -168,7 +228,7 @@ double row_dot(const uint8_t* w, int fmt, int64_t nb, int64_t n, const int8_t* q
       int64_t isum = 0, bsum = 0;
       for (int i = 0; i < sl; ++i) {
         int k = j * sl + i;
-        isum += (int64_t)sb.q[k] * qa[256 * b + k];
+        isum += (int64_t)(sb.q[k] - sb.off) * qa[256 * b + k];
         bsum += qa[256 * b + k];
       }
       S += (int64_t)sb.sc[j] * isum;
@@ -227,7 +287,7 @@ void orc_unpack_sb(const uint8_t* w, int fmt, int64_t N, int64_t K, int64_t n, i
   dd[1] = sb.dmin;
 }
 
-// Dequantized matrix W[N, K] in fp64: w = d * sc_j * q - dmin * mn_j.
+// Dequantized matrix W[N, K] in fp64: w = d * sc_j * (q - o) - dmin * mn_j.
 void orc_dequant_matrix(const uint8_t* w, int fmt, int64_t N, int64_t K, double* out) {
   int64_t nb = K / 256;
   int sl = sub_len(fmt);
@@ -237,7 +297,7 @@ void orc_dequant_matrix(const uint8_t* w, int fmt, int64_t N, int64_t K, double*
       unpack_sb(w, fmt, nb, n, b, &sb);
       for (int k = 0; k < 256; ++k) {
         int j = k / sl;
-        out[n * K + 256 * b + k] = sb.d * sb.sc[j] * sb.q[k] - sb.dmin * sb.mn[j];
+        out[n * K + 256 * b + k] = sb.d * sb.sc[j] * (sb.q[k] - sb.off) - sb.dmin * sb.mn[j];
       }
     }
 }
@@ -284,9 +344,14 @@ void orc_subblock_dots(const uint8_t* w, int fmt, int64_t N, int64_t K, const in
     }
 }
 
-// Integer super-block sums of activation rows qa[T, K] against W[N, K], the
-// integer part of row_dot before the scales are applied:
-//   S[t][n][b] = sum_j sc_j * isum_j,  M[t][n][b] = sum_j mn_j * bsum_j  (int64)
+// Integer super-block sums of activation rows qa[T, K] against W[N, K] on the
+// raw codes, the integer part of row_dot before the scales are applied:
+//   S[t][n][b] = sum_j sc_j * isum_j  (isum_j = sum of q_w * q_a, raw codes)
+//   M[t][n][b] = sum_j m_j * bsum_j   (int64)
+// with m_j = mn_j for the formats with a min, and m_j = o * sc_j for the
+// symmetric formats; then y = sum_b da * (d * S - m_scale * M), m_scale =
+// dmin or d.  (The same value as row_dot: sum_j sc_j sum_i (q - o) a =
+// S - o * sum_j sc_j bsum_j.)
 void orc_superblock_sums(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, int64_t T,
                          int64_t* S, int64_t* M) {
   int64_t nb = K / 256;
@@ -305,7 +370,7 @@ void orc_superblock_sums(const uint8_t* w, int fmt, int64_t N, int64_t K, const 
             bsum += q[j * sl + i];
           }
           s += (int64_t)sb.sc[j] * isum;
-          m += (int64_t)sb.mn[j] * bsum;
+          m += (int64_t)m_coef(sb, j) * bsum;
         }
         S[(t * N + n) * nb + b] = s;
         M[(t * N + n) * nb + b] = m;
@@ -324,9 +389,9 @@ void orc_qmatvec(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* 
 
 // Magnitude of the terms that orc_qmatvec sums into y[t][n], for
 // floating-point error bounds of an implementation that sums them in fp32:
-//   a[t][n] = sum_b |da[b]| * (|d_w| * |S_b| + |dmin| * |M_b|),
-// S_b = sum_j sc_j * isum_j and M_b = sum_j mn_j * bsum_j of super-block b
-// (the integer sums of row_dot).  |y[t][n]| <= a[t][n], with equality when
+//   a[t][n] = sum_b |da[b]| * (|d_w| * |S_b| + |m_scale| * |M_b|),
+// S_b and M_b the raw-code sums of orc_superblock_sums (m_scale = dmin, or
+// d for the symmetric formats).  |y[t][n]| <= a[t][n], with equality when
 // no term cancels another.
 void orc_qmatvec_absterms(const uint8_t* w, int fmt, int64_t N, int64_t K, const int8_t* qa, const float* da,
                           int64_t T, double* a, int nthreads) {
@@ -347,10 +412,10 @@ void orc_qmatvec_absterms(const uint8_t* w, int fmt, int64_t N, int64_t K, const
             bsum += q[256 * b + j * sl + i];
           }
           S += (int64_t)sb.sc[j] * isum;
-          M += (int64_t)sb.mn[j] * bsum;
+          M += (int64_t)m_coef(sb, j) * bsum;
         }
         acc += std::fabs((double)da[t * nb + b]) *
-               (std::fabs(sb.d) * std::fabs((double)S) + std::fabs(sb.dmin) * std::fabs((double)M));
+               (std::fabs(sb.d) * std::fabs((double)S) + std::fabs(m_scale(sb)) * std::fabs((double)M));
       }
       a[t * N + n] = acc;
     }

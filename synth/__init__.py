@@ -13,13 +13,18 @@ pseudorandom number generators", OOPSLA 2014: state += 0x9E3779B97F4A7C15,
 then the variant-13 finaliser).  Because the code and scale fields are plain
 bit fields, uniformly random bytes give exactly the required distributions:
 4-bit codes ~U{0..15}, 6-bit scales/mins ~U{0..63} (Q4_K-style), 2-bit codes
-~U{0..3}, 4-bit scales/mins ~U{0..15} (Q2_K-style).  The two fp16 fields are
-drawn as d ~ U(1e-4, 1e-3) and dmin ~ U(0, 5e-4): a 24-bit integer u gives
-f = u * 2^-24 in fp32 (exact), then ``lo + f * (hi - lo)`` with one fp32
-multiply and one fp32 add, each rounded to nearest even, then fp32 -> fp16
-round-to-nearest-even.  ``synth/csrc/synth_gen.cu`` implements the same
-generator on the GPU (weights of the large workloads, tens of GB, are made
-on the device); a test checks the two byte-for-byte.
+~U{0..3}, 4-bit scales/mins ~U{0..15} (Q2_K-style), 5-bit codes ~U{0..31}
+(Q5_K-style), 3-bit codes ~U{0..7} and 6-bit scales ~U{-32..31} (Q3_K-style),
+6-bit codes ~U{0..63} and int8 scales ~U{-128..127} (Q6_K-style).  Draws of
+one SB, in order: the code bytes (8 per draw, little-endian), two draws of
+scale/min bytes (the first 12 or 16 bytes used), one for d, then (formats
+with a dmin) one for dmin.  The fp16 fields are drawn as d ~ U(1e-4, 1e-3)
+and dmin ~ U(0, 5e-4): a 24-bit integer u gives f = u * 2^-24 in fp32
+(exact), then ``lo + f * (hi - lo)`` with one fp32 multiply and one fp32
+add, each rounded to nearest even, then fp32 -> fp16 round-to-nearest-even.
+``synth/csrc/synth_gen.cu`` implements the same generator on the GPU
+(weights of the large workloads, tens of GB, are made on the device); a test
+checks the two byte-for-byte.
 
 Random floats (activations, router weights, router bias) come from numpy's
 ``default_rng`` seeded with ``[seed, tag, layer, ...]`` on the host, and are
@@ -30,15 +35,15 @@ from __future__ import annotations
 import numpy as np
 
 from . import layout
-from .layout import FMT_Q4K, FMT_Q2K, sb_bytes, matrix_bytes
+from .layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, sb_bytes, matrix_bytes
 
 MASK64 = (1 << 64) - 1
 GAMMA = 0x9E3779B97F4A7C15
 
 # draws per super-block: codes, then scale/min bytes, then d, then dmin
-_N_CODE_DRAWS = {FMT_Q4K: 16, FMT_Q2K: 8}
+_N_CODE_DRAWS = {f: layout.CODE_BYTES[f] // 8 for f in layout.FORMATS}   # 16, 8, 20, 12, 24
 _N_SM_DRAWS = 2
-DRAWS_PER_SB = 32          # counter stride per super-block (only 20 / 12 used)
+DRAWS_PER_SB = 32          # counter stride per super-block (at most 28 used)
 
 # stream tags for the host float draws
 TAG_X = 1
@@ -106,16 +111,18 @@ def _dmin_bits(draw: np.ndarray) -> np.ndarray:
 def gen_sb_fields(fmt: int, key: int, sb_index: np.ndarray):
     """Raw per-super-block bytes (logical order) for the given SB indices.
 
-    Returns (code_bytes [n, 128|64] uint8, sm_bytes [n, 12|16] uint8,
-    d_bits [n] uint16, dmin_bits [n] uint16).
+    Returns (code_bytes [n, code bytes] uint8, sm_bytes [n, 12|16] uint8,
+    d_bits [n] uint16, dmin_bits [n] uint16 or None for the formats without
+    a dmin).
     """
     nc = _N_CODE_DRAWS[fmt]
-    dr = sb_draws(key, sb_index, nc + _N_SM_DRAWS + 2)
+    has_dmin = layout.HAS_DMIN[fmt]
+    dr = sb_draws(key, sb_index, nc + _N_SM_DRAWS + (2 if has_dmin else 1))
     code_bytes = np.ascontiguousarray(dr[:, :nc].astype('<u8')).view(np.uint8).reshape(len(sb_index), nc * 8)
     sm_all = np.ascontiguousarray(dr[:, nc:nc + 2].astype('<u8')).view(np.uint8).reshape(len(sb_index), 16)
     sm_bytes = sm_all[:, :layout.SM_BYTES[fmt]].copy()
     d_bits = _d_bits(dr[:, nc + 2])
-    dmin_bits = _dmin_bits(dr[:, nc + 3])
+    dmin_bits = _dmin_bits(dr[:, nc + 3]) if has_dmin else None
     return code_bytes, sm_bytes, d_bits, dmin_bits
 
 
@@ -127,7 +134,7 @@ def gen_matrix(fmt: int, N: int, K: int, seed: int, layer: int, expert: int, mat
     sb = np.arange(N * nb, dtype=np.int64)            # sb = row * nb + b
     code_bytes, sm_bytes, d_bits, dmin_bits = gen_sb_fields(fmt, key, sb)
     return layout.pack(fmt, N, K, code_bytes.reshape(N, nb, -1), sm_bytes.reshape(N, nb, -1),
-                       d_bits.reshape(N, nb), dmin_bits.reshape(N, nb))
+                       d_bits.reshape(N, nb), None if dmin_bits is None else dmin_bits.reshape(N, nb))
 
 
 def normal_f32(shape, std: float, seed: int, tag: int, *idx: int) -> np.ndarray:
@@ -151,6 +158,6 @@ def router_bias(E: int, std: float, seed: int, layer: int = 0) -> np.ndarray:
 
 
 __all__ = [
-    "layout", "FMT_Q4K", "FMT_Q2K", "sb_bytes", "matrix_bytes", "matrix_key", "sb_draws",
+    "layout", "FMT_Q4K", "FMT_Q2K", "FMT_Q5K", "FMT_Q3K", "FMT_Q6K", "sb_bytes", "matrix_bytes", "matrix_key", "sb_draws",
     "gen_sb_fields", "gen_matrix", "activations", "router_weight", "router_bias", "normal_f32",
 ]

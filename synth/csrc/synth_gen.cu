@@ -83,25 +83,61 @@ __global__ void fill_q2k(uint8_t* __restrict__ w, int64_t N, int64_t nb, uint64_
   *reinterpret_cast<uint32_t*>(slab + 4 * r) = dm;
 }
 
+// The other formats, one thread per super-block: NCODE code draws fill the
+// code lines in order (line L = draws 2L, 2L+1, the planes one after the
+// other), two draws the scale/min bytes (SMB of them), then d and, with a
+// 4-byte header, dmin.  Field offsets: header HB bytes per row, then SMB.
+template <int NCODE, int HB, int SMB>
+__global__ void fill_generic(uint8_t* __restrict__ w, int64_t N, int64_t nb, uint64_t key) {
+  constexpr int kSlab = 32 * (HB + SMB + 8 * NCODE);
+  constexpr int kSmOff = 32 * HB, kCodeOff = 32 * (HB + SMB);
+  int64_t sb = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (sb >= N * nb) return;
+  int64_t n = sb / nb, b = sb % nb;
+  int64_t rg = n >> 5;
+  int r = (int)(n & 31);
+  uint8_t* slab = w + (rg * nb + b) * kSlab;
+#pragma unroll
+  for (int l = 0; l < NCODE / 2; ++l)
+    *reinterpret_cast<uint4*>(slab + kCodeOff + 512 * l + 16 * r) =
+        line_of(draw(key, (uint64_t)sb, 2 * l), draw(key, (uint64_t)sb, 2 * l + 1));
+  const uint64_t s0 = draw(key, sb, NCODE), s1 = draw(key, sb, NCODE + 1);
+  uint32_t* sm = reinterpret_cast<uint32_t*>(slab + kSmOff + SMB * r);
+  sm[0] = (uint32_t)s0;
+  sm[1] = (uint32_t)(s0 >> 32);
+  sm[2] = (uint32_t)s1;
+  if (SMB == 16) sm[3] = (uint32_t)(s1 >> 32);
+  const uint16_t db = d_bits(draw(key, sb, NCODE + 2));
+  if (HB == 4)
+    *reinterpret_cast<uint32_t*>(slab + 4 * r) = (uint32_t)db | ((uint32_t)dmin_bits(draw(key, sb, NCODE + 3)) << 16);
+  else
+    *reinterpret_cast<uint16_t*>(slab + 2 * r) = db;
+}
+
 }  // namespace
 
 extern "C" {
 
 // Fill one [N, K] matrix at dst (device pointer, 16-byte aligned) with the
-// stream of `key`.  fmt 0 = Q4_K-style, 1 = Q2_K-style.  Returns 0 on success,
-// 1 on a bad argument, 2 on a CUDA launch error.
+// stream of `key`.  fmt 0 = Q4_K-style, 1 = Q2_K-style, 2 = Q5_K-style,
+// 3 = Q3_K-style, 4 = Q6_K-style.  Returns 0 on success, 1 on a bad argument,
+// 2 on a CUDA launch error.
 int synth_fill_matrix(void* dst, int fmt, int64_t N, int64_t K, uint64_t key, void* stream) {
-  if (!dst || N <= 0 || K <= 0 || N % 256 || K % 256 || (fmt != 0 && fmt != 1)) return 1;
+  if (!dst || N <= 0 || K <= 0 || N % 256 || K % 256 || fmt < 0 || fmt > 4) return 1;
   if (reinterpret_cast<uintptr_t>(dst) & 15) return 1;
   int64_t nb = K / 256;
   int64_t total = N * nb;
   int threads = 256;
   unsigned blocks = (unsigned)((total + threads - 1) / threads);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  if (fmt == 0)
-    fill_q4k<<<blocks, threads, 0, s>>>(static_cast<uint8_t*>(dst), N, nb, key);
-  else
-    fill_q2k<<<blocks, threads, 0, s>>>(static_cast<uint8_t*>(dst), N, nb, key);
+  uint8_t* w = static_cast<uint8_t*>(dst);
+  switch (fmt) {
+    case 0: fill_q4k<<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    case 1: fill_q2k<<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    case 2: fill_generic<20, 4, 12><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    case 3: fill_generic<12, 2, 12><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    default: fill_generic<24, 2, 16><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+  }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }
 

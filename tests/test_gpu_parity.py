@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from synth.layout import FMT_Q4K, FMT_Q2K
+from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FORMATS, N_SUB
 from tests import fieldpack
 from oracle import parity
 from tests.gpu_util import assert_close_rows, routing_ok, to_dev
@@ -74,19 +74,37 @@ def test_q8k_golden_blocks(moe):
 
 # ------------------------------------------------------------------ integer dots
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("N,K,T", [(256, 256, 1), (512, 1024, 3), (256, 2048, 16)])
 def test_subblock_dots_bit_exact(moe, fmt, N, K, T):
     w = synth.gen_matrix(fmt, N, K, 5, 0, 1, 0)
     x = synth.activations(T, K, 5)
     xq, _, _ = oracle.q8k_quantize(x)
-    ns = 8 if fmt == FMT_Q4K else 16
+    ns = N_SUB[fmt]
     isum = torch.empty((T, N, K // 256, ns), dtype=torch.int32, device="cuda")
     bsum = torch.empty((T, K // 256, ns), dtype=torch.int32, device="cuda")
     moe.moe_debug_subblock_dots(fmt, dev(w), N, K, dev(xq), isum, bsum)
     risum, rbsum = oracle.subblock_dots(w, fmt, N, K, xq)
     np.testing.assert_array_equal(isum.cpu().numpy(), risum)
     np.testing.assert_array_equal(bsum.cpu().numpy(), rbsum)
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q5K, FMT_Q3K, FMT_Q6K])
+def test_subblock_dots_extreme_fields(moe, fmt):
+    """Every code at its largest value (every high bit set) against q_a = -127 and +127."""
+    N, K = 256, 512
+    ns = N_SUB[fmt]
+    q = np.full((N, 2, 256), fieldpack.QMAX[fmt])
+    sc = np.full((N, 2, ns), fieldpack.SCALE_RANGE[fmt][1])
+    mn = np.full((N, 2, ns), fieldpack.MIN_RANGE[fmt][1])
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, np.ones((N, 2), np.float16), np.ones((N, 2), np.float16))
+    xq = np.stack([np.full(K, -127, np.int8), np.full(K, 127, np.int8)])
+    isum = torch.empty((2, N, 2, ns), dtype=torch.int32, device="cuda")
+    bsum = torch.empty((2, 2, ns), dtype=torch.int32, device="cuda")
+    moe.moe_debug_subblock_dots(fmt, dev(w), N, K, dev(xq), isum, bsum)
+    sl = 256 // ns
+    want = np.array([-127, 127])[:, None, None, None] * sl * fieldpack.QMAX[fmt]
+    np.testing.assert_array_equal(isum.cpu().numpy(), np.broadcast_to(want, isum.shape))
 
 
 def test_subblock_dots_extreme_codes(moe):
@@ -186,7 +204,7 @@ def _experts_host(fmt, E, H, I, seed, layer=0):
              synth.gen_matrix(fmt, H, I, seed, layer, e, 2)) for e in range(E)]
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 @pytest.mark.parametrize("T,H,I,E,k,S", [(4, 512, 256, 16, 2, 0), (5, 768, 512, 8, 3, 1), (17, 256, 256, 4, 2, 1)])
 def test_expert_ffn_and_combine(moe, fmt, T, H, I, E, k, S):
     ex = _experts_host(fmt, E + S, H, I, seed=21)
@@ -234,6 +252,15 @@ CASES = [
     (FMT_Q4K, 0, 512, 256, 8, 2, 1, 512, False),
     (FMT_Q2K, 1, 768, 512, 16, 4, 0, 300, True),     # skewed router: some experts far above 128 tokens
     (FMT_Q4K, 1, 1024, 256, 4, 1, 2, 257, False),    # two shared experts, one routed slot per token
+    # the Q5_K/Q3_K/Q6_K-style formats: decode (single launch), the GEMV path, a prefill chunk
+    (FMT_Q5K, 0, 2048, 512, 64, 8, 1, 1, False),
+    (FMT_Q3K, 1, 1024, 512, 64, 10, 1, 4, False),
+    (FMT_Q6K, 0, 768, 512, 32, 8, 0, 16, True),
+    (FMT_Q6K, 1, 512, 256, 40, 10, 1, 40, False),    # 400 pairs: the GEMV path
+    (FMT_Q5K, 1, 512, 256, 40, 10, 1, 40, False),
+    (FMT_Q3K, 0, 512, 256, 8, 2, 1, 512, False),     # tensor-core prefill
+    (FMT_Q5K, 0, 512, 256, 8, 2, 1, 512, False),     # a prefill-size chunk on the GEMV path
+    (FMT_Q6K, 1, 768, 512, 16, 4, 0, 300, True),
 ]
 
 
@@ -481,8 +508,8 @@ def test_bounded_wait_runs_out_and_reports(moe):
 
 # ------------------------------------------------------- tensor-core integer sums
 
-@pytest.mark.parametrize("fmt,N,K,T", [(FMT_Q4K, 256, 512, 200), (FMT_Q2K, 128, 768, 130), (FMT_Q4K, 128, 256, 16),
-                                       (FMT_Q2K, 256, 256, 1)])
+@pytest.mark.parametrize("fmt,N,K,T", [(FMT_Q4K, 256, 512, 200), (FMT_Q2K, 256, 768, 130), (FMT_Q4K, 512, 256, 16),
+                                       (FMT_Q2K, 256, 256, 1), (FMT_Q3K, 256, 512, 200), (FMT_Q3K, 512, 256, 3)])
 def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     """S = sum_j sc_j isum_j and M = sum_j mn_j bsum_j of every (token, row, super-block), as the tcgen05
     GEMM forms them in TMEM, equal the oracle's int64 sums bit for bit.  Rows 0-31 carry an all-extreme
@@ -491,10 +518,9 @@ def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     130 leave a ragged second token tile."""
     rng = np.random.default_rng(N + K + T + fmt)
     q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
-    qmax, smax = (15, 63) if fmt == FMT_Q4K else (3, 15)
-    q[:32, 0] = qmax
-    sc[:32, 0] = smax
-    mn[:32, 0] = smax
+    q[:32, 0] = fieldpack.QMAX[fmt]
+    sc[:32, 0] = fieldpack.SCALE_RANGE[fmt][0] if fmt == FMT_Q3K else fieldpack.SCALE_RANGE[fmt][1]
+    mn[:32, 0] = fieldpack.MIN_RANGE[fmt][1]
     w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
     x = rng.standard_normal((T, K)).astype(np.float32)
     if T >= 3:
@@ -513,3 +539,44 @@ def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     np.testing.assert_array_equal(M.cpu().numpy(), Mr)
     if fmt == FMT_Q4K and T >= 3:
         assert Sr[0, 0, 0] == 63 * 15 * 127 * 256 and Sr[2, 0, 0] % 2 == 1 and Sr[2, 0, 0] > 2 ** 24
+
+
+def test_workspace_shared_by_launches_of_different_grid_sizes(moe):
+    """One workspace used in turn by the single-layer decode kernel (one CTA per SM, three grid barriers)
+    and the stack kernel (two CTAs per SM): every result equals, bit for bit, the same call on a fresh
+    workspace, and the device status stays clear (a grid barrier keeps no count across launches)."""
+    fmt, H, I, E, k, S, T, L = FMT_Q4K, 1024, 512, 64, 8, 1, 1, 2
+    ex = _experts_host(fmt, E + S, H, I, 17)
+    table = moe.expert_table([tuple(dev(m) for m in e) for e in ex])
+    wr = dev(synth.router_weight(E, H, 17))
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=0, fmt=fmt, T_max=T)
+    xs = [dev(synth.activations(T, H, 17, l)) for l in range(L)]
+    outs = [torch.empty_like(xs[0]) for _ in range(L)]
+    rows = [dict(table=table, w_router=wr, x=xs[l], residual=xs[l], out=outs[l]) for l in range(L)]
+    stack = moe.stack_pointer_table(rows)
+    size = moe.moe_stack_workspace_size(desc, L)
+    layout = moe.moe_workspace_layout(desc)
+
+    def run_layer(ws):
+        out = torch.empty_like(xs[0])
+        moe.moe_layer_forward(desc, table, wr, None, xs[0], xs[0], out, None, None, ws)
+        return out.cpu().numpy()
+
+    def run_stack(ws):
+        moe.moe_stack_forward(desc, stack, T, ws)
+        return np.stack([o.cpu().numpy() for o in outs])
+
+    def grid(ws):
+        return int(moe.MoeLayer.ws_view_of(ws, layout, "phase_ns", torch.int64, (16,))[14].item())
+
+    want_layer = run_layer(torch.zeros(size, dtype=torch.uint8, device="cuda"))
+    want_stack = run_stack(torch.zeros(size, dtype=torch.uint8, device="cuda"))
+    ws = torch.zeros(size, dtype=torch.uint8, device="cuda")
+    grids = set()
+    for _ in range(3):
+        np.testing.assert_array_equal(run_layer(ws).view(np.uint32), want_layer.view(np.uint32))
+        grids.add(grid(ws))
+        np.testing.assert_array_equal(run_stack(ws).view(np.uint32), want_stack.view(np.uint32))
+        grids.add(grid(ws))
+        assert moe.moe_get_status(ws) == 0
+    assert len(grids) == 2, grids          # the two kernels ran with different grid sizes

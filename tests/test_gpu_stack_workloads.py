@@ -113,6 +113,26 @@ def check_stack_layer(moe, wl, run, l):
     return metrics
 
 
+@pytest.mark.parametrize("fmt", [synth.FMT_Q5K, synth.FMT_Q3K, synth.FMT_Q6K], ids=["q5k", "q3k", "q6k"])
+def test_decode_stack_other_formats(moe, fmt):
+    """The decode workload's shape (40 layers, H 2048, 256 experts top-8 + shared, I 512, 1 token) with
+    Q5_K/Q3_K/Q6_K-style weights made on the device, as one moe_stack_forward."""
+    import dataclasses
+
+    import synth.gpu
+    wl = dataclasses.replace(WORKLOADS[DECODE], fmt=fmt)
+    bank = synth.gpu.ExpertBank(wl.fmt, wl.H, wl.I, wl.E + wl.S, wl.layers, wl.seed)
+    run = run_stack(moe, wl, bank, [])
+    L = wl.layers
+    summary = parity.merge([check_stack_layer(moe, wl, run, l) for l in sorted({0, L // 2, L - 1})])
+    print(f"\n{synth.layout.NAMES[fmt]} decode stack: {summary}")
+    assert summary["bucket_exact"]
+    del run, bank
+    gc.collect()
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("chained", [False, True], ids=["independent", "chained"])
 @pytest.mark.parametrize("name", [DECODE, VERIFY])
 def test_stack_at_bench_shape(moe, name, chained):

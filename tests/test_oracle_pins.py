@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from synth.layout import FMT_Q4K, FMT_Q2K
+from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FORMATS
 from tests import fieldpack
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -79,7 +79,7 @@ def test_half_decode(bits, value):
     assert oracle.half_to_double(bits) == pytest.approx(value, rel=0, abs=1e-16)
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_unpack_recovers_encoded_fields(fmt):
     rng = np.random.default_rng(11 + fmt)
     N, K = 256, 512
@@ -96,7 +96,7 @@ def test_unpack_recovers_encoded_fields(fmt):
                                   fieldpack.dequant_fields(fmt, q, sc, mn, d, dmin))
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_one_hot_activation_reads_one_weight(fmt):
     """x = c * e_i  ->  q8_K gives d = c/127, q_i = 127, so y[n] = fp32(c/127) * 127 * w[n, i]."""
     rng = np.random.default_rng(21 + fmt)
@@ -113,7 +113,7 @@ def test_one_hot_activation_reads_one_weight(fmt):
         np.testing.assert_allclose(y, scale * W[:, i], rtol=1e-12, atol=1e-15)
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_integer_subblock_dot_equals_dense_dequantized_dot(fmt):
     """Brute force: sum_k w[n,k] * (d_a q_a[k]) in fp64 equals the sub-block integer form."""
     rng = np.random.default_rng(31 + fmt)
@@ -129,7 +129,7 @@ def test_integer_subblock_dot_equals_dense_dequantized_dot(fmt):
     np.testing.assert_allclose(y, y_dense, rtol=1e-11, atol=1e-11 * np.abs(y_dense).max())
     # the integer sums themselves, against their definition on the fields
     isum, bsum = oracle.subblock_dots(w, fmt, N, K, xq)
-    sl = 32 if fmt == FMT_Q4K else 16
+    sl = synth.layout.SUB_LEN[fmt]
     ns = 256 // sl
     qa = xq.reshape(T, K // 256, ns, sl).astype(np.int64)
     np.testing.assert_array_equal(bsum, qa.sum(axis=3))
@@ -137,7 +137,7 @@ def test_integer_subblock_dot_equals_dense_dequantized_dot(fmt):
     np.testing.assert_array_equal(isum, np.einsum("nbjs,tbjs->tnbj", qw, qa))
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_zero_scale_and_min_give_zero(fmt):
     rng = np.random.default_rng(41)
     N, K = 256, 256
@@ -168,7 +168,7 @@ def test_extreme_codes_stay_exact():
     assert (y == 1.0 * (1.0 * S - 0.5 * M)).all()
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_superblock_sums_from_fields(fmt):
     """S = sum_j sc_j isum_j and M = sum_j mn_j bsum_j, recomputed with numpy from the encoded fields;
     and y = sum_b d_a (d S - dmin M) reproduces qmatvec."""
@@ -179,15 +179,19 @@ def test_superblock_sums_from_fields(fmt):
     x = rng.standard_normal((T, K)).astype(np.float32)
     xq, xd, _ = oracle.q8k_quantize(x)
     S, M = oracle.superblock_sums(w, fmt, N, K, xq)
-    sl = 32 if fmt == FMT_Q4K else 16
+    sl = synth.layout.SUB_LEN[fmt]
     ns = 256 // sl
     qa = xq.reshape(T, K // 256, ns, sl).astype(np.int64)
     qw = np.asarray(q, np.int64).reshape(N, K // 256, ns, sl)
     isum = np.einsum("nbjs,tbjs->tnbj", qw, qa)
     bsum = qa.sum(axis=3)
+    # the min term: mn_j (scale dmin), or offset * scale_j (scale d) for the symmetric formats
+    sym = fmt in fieldpack.SYMMETRIC
+    m = fieldpack.OFFSET[fmt] * np.asarray(sc, np.int64) if sym else np.asarray(mn, np.int64)
+    mscale = d if sym else dmin
     np.testing.assert_array_equal(S, np.einsum("nbj,tnbj->tnb", np.asarray(sc, np.int64), isum))
-    np.testing.assert_array_equal(M, np.einsum("nbj,tbj->tnb", np.asarray(mn, np.int64), bsum))
-    y = (xd.astype(np.float64)[:, None, :] * (d.astype(np.float64)[None] * S - dmin.astype(np.float64)[None] * M)).sum(axis=2)
+    np.testing.assert_array_equal(M, np.einsum("nbj,tbj->tnb", m, bsum))
+    y = (xd.astype(np.float64)[:, None, :] * (d.astype(np.float64)[None] * S - mscale.astype(np.float64)[None] * M)).sum(axis=2)
     np.testing.assert_allclose(oracle.qmatvec(w, fmt, N, K, xq, xd), y, rtol=1e-12, atol=1e-12 * np.abs(y).max())
 
 
@@ -201,7 +205,7 @@ def test_superblock_sums_extreme_block():
     assert (M == 63 * 127 * 256).all()
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_absterms_from_fields_brute_force(fmt):
     """qmatvec_absterms = sum over super-blocks of |d_a| (|d| |S_b| + |dmin| |M_b|), with S_b and M_b
     recomputed here from the encoded fields by plain loops; and it bounds |qmatvec| (triangle inequality)."""
@@ -212,17 +216,21 @@ def test_absterms_from_fields_brute_force(fmt):
     x = rng.standard_normal((T, K)).astype(np.float32)
     xq, xd, _ = oracle.q8k_quantize(x)
     a = oracle.qmatvec_absterms(w, fmt, N, K, xq, xd)
-    sl = 32 if fmt == FMT_Q4K else 16
+    sl = synth.layout.SUB_LEN[fmt]
     ns = 256 // sl
+    sym = fmt in fieldpack.SYMMETRIC
     want = np.zeros((T, N))
     for t in range(T):
         for n in range(N):
             for b in range(K // 256):
                 qa = xq[t, 256 * b:256 * b + 256].astype(np.int64).reshape(ns, sl)
                 qw = np.asarray(q[n, b], np.int64).reshape(ns, sl)
-                S = int((sc[n, b] * (qw * qa).sum(axis=1)).sum())
-                M = int((mn[n, b] * qa.sum(axis=1)).sum())
-                want[t, n] += abs(float(xd[t, b])) * (abs(float(d[n, b])) * abs(S) + abs(float(dmin[n, b])) * abs(M))
+                scb = np.asarray(sc[n, b], np.int64)
+                S = int((scb * (qw * qa).sum(axis=1)).sum())
+                m = fieldpack.OFFSET[fmt] * scb if sym else np.asarray(mn[n, b], np.int64)
+                M = int((m * qa.sum(axis=1)).sum())
+                mscale = float(d[n, b]) if sym else float(dmin[n, b])
+                want[t, n] += abs(float(xd[t, b])) * (abs(float(d[n, b])) * abs(S) + abs(mscale) * abs(M))
     np.testing.assert_allclose(a, want, rtol=1e-13)
     y = oracle.qmatvec(w, fmt, N, K, xq, xd)
     assert (np.abs(y) <= a * (1 + 1e-12)).all()
@@ -240,6 +248,27 @@ def test_absterms_equal_output_when_nothing_cancels():
     x = np.abs(rng.standard_normal((3, K))).astype(np.float32)
     xq, xd, _ = oracle.q8k_quantize(x)
     np.testing.assert_array_equal(oracle.qmatvec_absterms(w, fmt, N, K, xq, xd), oracle.qmatvec(w, fmt, N, K, xq, xd))
+
+
+@pytest.mark.parametrize("fmt", [FMT_Q5K, FMT_Q3K, FMT_Q6K])
+def test_extreme_fields_closed_form(fmt):
+    """Every code at its largest value, the scale at its extreme, activation codes all -127 (d_a = 1):
+    y = -127 * 256 * d * scale * (qmax - o) + 127 * 256 * dmin * min, computed here from the definition."""
+    N, K = 256, 256
+    qmax = fieldpack.QMAX[fmt]
+    scale = fieldpack.SCALE_RANGE[fmt][0] if fmt in fieldpack.SYMMETRIC else fieldpack.SCALE_RANGE[fmt][1]
+    mn = fieldpack.MIN_RANGE[fmt][1]
+    ns = synth.layout.N_SUB[fmt]
+    w = fieldpack.pack_fields(fmt, N, K, np.full((N, 1, 256), qmax), np.full((N, 1, ns), scale),
+                              np.full((N, 1, ns), mn), np.full((N, 1), 0.5, np.float16), np.full((N, 1), 0.25, np.float16))
+    x = np.full((1, K), -127.0, np.float32)
+    xq, xd, _ = oracle.q8k_quantize(x)
+    off = fieldpack.OFFSET.get(fmt, 0)
+    dmin = 0.25 if fmt not in fieldpack.SYMMETRIC else 0.0
+    want = -127 * 256 * 0.5 * scale * (qmax - off) + 127 * 256 * dmin * mn
+    assert (oracle.qmatvec(w, fmt, N, K, xq, xd) == want).all()
+    q, sc, m, dd, dm = oracle.unpack_sb(w, fmt, N, K, 5, 0)
+    assert (q == qmax).all() and (sc == scale).all() and dd == 0.5
 
 
 # ---------------------------------------------------------------- routing

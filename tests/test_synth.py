@@ -5,10 +5,11 @@ import pytest
 
 import oracle
 import synth
-from synth.layout import FMT_Q4K, FMT_Q2K
+from synth.layout import FMT_Q4K, FMT_Q2K, FORMATS
+from tests import fieldpack
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_matrix_generator_is_deterministic_and_keyed(fmt):
     a = synth.gen_matrix(fmt, 256, 512, 1, 0, 3, 0)
     b = synth.gen_matrix(fmt, 256, 512, 1, 0, 3, 0)
@@ -19,11 +20,14 @@ def test_matrix_generator_is_deterministic_and_keyed(fmt):
     assert (a != c).mean() > 0.9 and (a != d).mean() > 0.9
 
 
-@pytest.mark.parametrize("fmt", [FMT_Q4K, FMT_Q2K])
+@pytest.mark.parametrize("fmt", FORMATS)
 def test_generated_fields_follow_the_workload_distributions(fmt):
+    """Codes, scales and mins uniform over their ranges (signed scales for the symmetric formats),
+    d ~ U(1e-4, 1e-3), dmin ~ U(0, 5e-4) where the format has one."""
     N, K = 512, 1024
     w = synth.gen_matrix(fmt, N, K, 0, 0, 0, 0)
-    qmax, smax = (15, 63) if fmt == FMT_Q4K else (3, 15)
+    qmax = fieldpack.QMAX[fmt]
+    slo, shi = fieldpack.SCALE_RANGE[fmt]
     qs, scs, mns, ds, dms = [], [], [], [], []
     for n in range(0, N, 7):
         for b in range(K // 256):
@@ -31,14 +35,21 @@ def test_generated_fields_follow_the_workload_distributions(fmt):
             qs.append(q); scs.append(sc); mns.append(mn); ds.append(d); dms.append(dmin)
     q = np.concatenate(qs); sc = np.concatenate(scs); mn = np.concatenate(mns)
     ds = np.array(ds); dms = np.array(dms)
-    for v, top in [(q, qmax), (sc, smax), (mn, smax)]:
-        hist = np.bincount(v, minlength=top + 1)
-        assert hist.size == top + 1
-        expect = v.size / (top + 1)
+    checks = [(q, 0, qmax), (sc, slo, shi)]
+    if fmt not in fieldpack.SYMMETRIC:
+        checks.append((mn, 0, fieldpack.MIN_RANGE[fmt][1]))
+    else:
+        assert (mn == 0).all() and (dms == 0).all()
+    for v, lo, top in checks:
+        hist = np.bincount(v - lo, minlength=top - lo + 1)
+        assert hist.size == top - lo + 1
+        expect = v.size / (top - lo + 1)
         assert np.abs(hist - expect).max() < 6 * np.sqrt(expect) + 3
     assert ds.min() >= 1e-4 * 0.999 and ds.max() <= 1e-3 * 1.001
-    assert dms.min() >= 0 and dms.max() <= 5e-4 * 1.001
-    assert abs(ds.mean() - 5.5e-4) < 3e-5 and abs(dms.mean() - 2.5e-4) < 2e-5
+    assert abs(ds.mean() - 5.5e-4) < 3e-5
+    if fmt not in fieldpack.SYMMETRIC:
+        assert dms.min() >= 0 and dms.max() <= 5e-4 * 1.001
+        assert abs(dms.mean() - 2.5e-4) < 2e-5
 
 
 def test_float_streams():
