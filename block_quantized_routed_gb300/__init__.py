@@ -26,7 +26,7 @@ __all__ = [
     "moe_debug_subblock_dots", "moe_trace_events", "moe_trace_used", "moe_kernel_launch_count", "moe_layer_path",
     "PATH_DECODE_FUSED", "PATH_GEMV", "PATH_TENSOR_PREFILL", "expert_table", "MoeLayer",
     "moe_stack_kernel", "STACK_PIPELINED", "STACK_DATAFLOW", "StackLayerLayout", "moe_stack_layer_layout",
-    "ws_view", "moe_debug_prefill_sums", "moe_debug_prefill_sums_workspace_size",
+    "ws_view", "moe_debug_prefill_sums", "moe_debug_prefill_sums_workspace_size", "moe_prefill_tile_tokens",
 ]
 
 FMT_Q4K = 0
@@ -117,6 +117,7 @@ def load():
         "moe_last_cuda_error": (ctypes.c_int, []),
         "moe_debug_wait_timeout": (ctypes.c_int, [P, I32, P]),
         "moe_layer_path": (ctypes.c_int, [D, I32]),
+        "moe_prefill_tile_tokens": (ctypes.c_int, []),
         "moe_stack_kernel": (ctypes.c_int, [D, I32, I32, I32]),
         "moe_stack_layer_layout": (ctypes.c_int, [D, I32, I32, I32, ctypes.POINTER(StackLayerLayout)]),
         "moe_debug_prefill_sums_workspace_size": (SZ, [I32, I32, I32]),
@@ -317,6 +318,12 @@ def moe_layer_path(desc, T) -> int:
     if rc < 0:
         raise MoeError(rc, "moe_layer_path")
     return rc
+
+
+def moe_prefill_tile_tokens() -> int:
+    """Token tile n of the tensor-core prefill path: an expert with c tokens gets ceil(c / n) tiles of
+    balanced size."""
+    return int(load().moe_prefill_tile_tokens())
 
 
 def moe_stack_kernel(desc, n_layers, T, n_sms=0) -> int:

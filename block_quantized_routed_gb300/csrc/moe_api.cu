@@ -667,6 +667,8 @@ int moe_stack_kernel(const moe_layer_desc* desc, int32_t n_layers, int32_t T, in
   return stack_takes_pipelined(*desc, n_layers, T, n_sms) ? MOE_STACK_PIPELINED : MOE_STACK_DATAFLOW;
 }
 
+int moe_prefill_tile_tokens(void) { return prefill_tile_tokens(); }
+
 int32_t moe_trace_used(void) { return g_trace_events || g_trace_next > 0 ? g_trace_next : 0; }
 
 int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream) {

@@ -205,6 +205,7 @@ struct PItem {
   int count;   // tokens in the tile (<= 128)
   int wtile;   // gate/up: 64-row group of I (its gate and up rows); down: 128-row group of H
 };
+int prefill_tile_tokens();
 size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I);
 struct PrefillArgs {
   int fmt, H, I, E, S, T, k;

@@ -25,10 +25,12 @@
 //
 //   D[m, n] = sum_b d_a[n, b] * (d_w[m, b] * (S0 + S1)[m, n, b] - dmin[m, b] * M[m, n, b])
 //
-// TMEM holds four regions of 128 columns used as a ring: super-block
-// number tb of a CTA writes S0, S1, M to regions 3tb, 3tb+1, 3tb+2 (mod 4),
-// so the MMAs of the next super-block start while the epilogue still reads
-// this one.
+// TMEM's 512 columns are a ring of slots of kTileN columns (five of 96):
+// super-block number tb of a CTA writes S0, S1, M to slots 3tb, 3tb+1,
+// 3tb+2 (mod the slot count), so all MMAs of a super-block but its min MMA
+// run while the epilogue still reads the super-block before.  A token tile
+// therefore holds at most kTileN tokens; an expert's tokens are split into
+// tiles of balanced size.
 // This is the same contraction the GEMV kernels compute with dp4a; the
 // pages' prefill design reaches it with int8 MMA (Pulsar README, "What it
 // does today"; Strata, 0.1.13 prefill notes: grouped int8 tensor-core expert
@@ -49,13 +51,16 @@
 //                that half's TMEM region, the min MMA with the last half;
 //                commits are grouped (a commit costs the issuing thread
 //                several hundred cycles, so each group carries 8+ MMAs)
-//   warps 0-15   epilogue: TMEM -> registers, per-block rescale, output
+//   warps 0-15   epilogue: TMEM -> registers in 8-token column blocks (three
+//                loads, one wait per block), per-block rescale, output
 // (26 warps at 72 registers: the register file is split between the SM's
 // four sub-partitions, so the warp count bounds the registers per thread.)
 // Rings: 3 activation stages and 2 expanded-weight stages of 128 K each
-// (two 128-byte swizzle atoms), 2 raw stages of one super-block column.
-// A work item is (expert, token tile of <= 128 bucket rows, weight tile of
-// 128 rows); the items of a launch are laid out by a plan kernel.
+// (two 128-byte swizzle atoms), 3 raw stages of one super-block column; the
+// producer prefetches the weight rows of the CTA's next item into L2 (the
+// raw ring alone holds less than a DRAM round trip of MMA work).
+// A work item is (expert, token tile of <= kTileN bucket rows, weight tile
+// of 128 rows); the items of a launch are laid out by a plan kernel.
 //   gate/up: the 128 rows interleave 64 gate rows and the same 64 up rows
 //            (even tile row: gate, odd: up), so a lane pair of the epilogue
 //            holds G and U of one (row, token): SwiGLU is a shuffle, and h is
@@ -79,12 +84,20 @@ namespace moe {
 namespace {
 
 constexpr int kTileM = 128;                          // weight rows per tile (MMA M)
-constexpr int kTileN = 128;                          // tokens per tile (MMA N <= 128)
+#ifndef MOE_PREFILL_TILE_N
+#define MOE_PREFILL_TILE_N 96
+#endif
+constexpr int kTileN = MOE_PREFILL_TILE_N;           // tokens per tile (MMA N <= kTileN)
+static_assert(kTileN % 32 == 0 && kTileN >= 32 && kTileN <= 128, "token tile: whole TMA boxes, N <= 128");
+// TMEM: 512 columns as a ring of kSlots slots of kTileN columns; a super-block
+// takes three (S0, S1, M), so with five or six slots the MMAs of a super-block
+// run while the epilogue still reads the one before.
+constexpr int kSlots = 512 / kTileN < 6 ? 512 / kTileN : 6;
 constexpr int kStageK = 128;                         // K of one A or B stage: half a super-block
 constexpr int kAtomK = 64;                           // K of one 128-byte swizzle atom (fp16)
 constexpr int kStagesA = 2;                          // expanded-weight stages
 constexpr int kStagesB = 3;                          // activation stages
-constexpr int kRaw = 2;                              // raw stages (one super-block column each)
+constexpr int kRaw = 3;                              // raw stages (one super-block column each)
 constexpr int kBoxRows = 32;                         // token rows per TMA box
 constexpr int kEpiWarps = 16, kExpWarps = 8;        // epilogue: 32 tokens per warp; expanders: two threads per row
 constexpr int kWarpProducer = kEpiWarps + kExpWarps; // 24
@@ -93,9 +106,11 @@ constexpr int kPThreads = 32 * (kWarpMma + 1);       // 832
 constexpr long long kWaitCycles = 2000000000ll;      // ~1 s at 2 GHz: a wait that long has failed
 
 // shared memory (offsets from a 1024-byte aligned base).  A stage holds two
-// swizzle atoms of 128 rows x 64 fp16 (16 KB each), K-major, 128-byte swizzle.
+// swizzle atoms of 128 rows x 64 fp16 (16 KB each), K-major, 128-byte swizzle;
+// a B stage two atoms of kTileN token rows.
 constexpr int kAtomBytes = 128 * 128;
-constexpr int kBStage = 2 * kAtomBytes;              // 32 KB: 128 token rows x 128 codes
+constexpr int kAtomBytesB = kTileN * 128;
+constexpr int kBStage = 2 * kAtomBytesB;             // kTileN token rows x 128 codes
 constexpr int kAStage = 2 * kAtomBytes;              // 32 KB: 128 weight rows x 128 (sc * q)
 constexpr int kRawBytes = 4 * 4608;                  // four slabs (Q4_K size; Q2_K uses less)
 constexpr int kSmB = 0;
@@ -188,7 +203,7 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-constexpr int kEpilogueSleepNs = 256;  // the 16 epilogue warps wait a whole tile's MMAs at a time
+constexpr int kEpilogueSleepNs = 64;  // the epilogue warps poll with a short back-off (they wait a super-block of MMAs)
 
 // Bounded wait for phase `parity`.  Gives up when another role has aborted,
 // or after about a second, recording a timeout; false = abort.
@@ -233,6 +248,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                : "memory");
 }
 
+// bulk prefetch of global bytes into L2 (16-byte aligned, a multiple of 16 bytes)
+__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
@@ -252,18 +272,7 @@ __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsig
   return r;
 }
 
-// 32 lanes x 16 consecutive fp32 columns of TMEM into 16 registers of each lane
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
-        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
-}
+// 32 lanes x 8 consecutive fp32 columns of TMEM into 8 registers of each lane
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
   uint32_t r[8];
   asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
@@ -272,18 +281,10 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&v)[8]) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
-__device__ __forceinline__ void tmem_ld4(uint32_t taddr, float (&v)[4]) {
-  uint32_t r[4];
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x4.b32 {%0,%1,%2,%3}, [%4];"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-               : "r"(taddr));
-#pragma unroll
-  for (int i = 0; i < 4; ++i) v[i] = __uint_as_float(r[i]);
-}
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 
-// TMEM column of region i (0..3, 128 columns each) of the ring
-__device__ __forceinline__ uint32_t tmem_region(uint32_t i) { return 128u * (i & 3u); }
+// TMEM column of slot i of the ring (kSlots slots of kTileN columns)
+__device__ __forceinline__ uint32_t tmem_slot(uint32_t i) { return (uint32_t)kTileN * (i % (uint32_t)kSlots); }
 
 // byte offset of element (row, k) in a K-major canonical tile without
 // swizzle, kc core matrices along K (16-bit elements)
@@ -324,7 +325,7 @@ __device__ __forceinline__ uint4 scaled8(uint32_t w0, uint32_t w1, __half2 sc2, 
 
 // ---------------------------------------------------------------- planning
 // One CTA: per expert with tokens and a present gate pointer, its token tiles
-// (ceil(c/128) tiles of balanced size) x weight tiles, expert by expert.
+// (ceil(c/kTileN) tiles of balanced size) x weight tiles, expert by expert.
 __global__ void __launch_bounds__(1024) prefill_plan_kernel(const int32_t* counts, const int32_t* offsets, int EpS,
                                                             const moe_expert_ptrs* table, int n_wtiles, PItem* items,
                                                             int32_t* n_items, int max_items) {
@@ -514,14 +515,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       int bs = 0;
       uint32_t pb = 0;
       bool ok = true;
-      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
-        const PItem it = a.items[item];
+      // the four row groups of an item's weight tile: gate/up -> gate 2w, 2w+1,
+      // up 2w, 2w+1; down -> 4w .. 4w+3 (each nb slabs, contiguous)
+      auto rows_of = [&](const PItem& it, const uint8_t* (&src)[4]) {
         moe_expert_ptrs ep;
         if (MODE == 2) ep.gate = ep.up = ep.down = a.dbg_w;
         else ep = a.table[it.expert];
-        const int nbox = (it.count + kBoxRows - 1) / kBoxRows;
-        // the four row groups of the tile: gate/up -> gate 2w, 2w+1, up 2w, 2w+1; down -> 4w .. 4w+3
-        const uint8_t* src[4];
 #pragma unroll
         for (int g = 0; g < 4; ++g) {
           if (MODE == 0) {
@@ -531,6 +530,20 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
             src[g] = static_cast<const uint8_t*>(ep.down) + (size_t)(it.wtile * 4 + g) * nb * slab_bytes;
           }
         }
+      };
+      // The raw ring holds three super-block columns, less than a DRAM round
+      // trip of MMA work: the weight rows of the CTA's next item are
+      // prefetched into L2 a whole item ahead, so the ring's loads hit L2.
+      auto prefetch_rows = [&](const uint8_t* const (&src)[4]) {
+#pragma unroll
+        for (int g = 0; g < 4; ++g) prefetch_l2(src[g], (uint32_t)(nb * slab_bytes));
+      };
+      for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
+        const PItem it = a.items[item];
+        const uint8_t* src[4];
+        rows_of(it, src);
+        if (item == (int)blockIdx.x) prefetch_rows(src);
+        const int nbox = (it.count + kBoxRows - 1) / kBoxRows;
         for (int b = 0; b < nb && ok; ++b) {
           const int rs = ri % kRaw;
           if (!(ok = wait_bar(empty_raw(rs), ((ri / kRaw) & 1) ^ 1, abort_flag, a.status, w0))) break;
@@ -543,13 +556,19 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           tma_load_2d(b2, &a.map_s, 0, (int)((2 * b) * a.P + it.start), full_raw(rs));
           tma_load_2d(b2 + 2048, &a.map_s, 0, (int)((2 * b + 1) * a.P + it.start), full_raw(rs));
           ++ri;
+          // (after the item's first copies are on their way: the lookups take two L2 round trips)
+          if (b == 0 && item + (int)gridDim.x < n_items) {
+            const uint8_t* nsrc[4];
+            rows_of(a.items[item + gridDim.x], nsrc);
+            prefetch_rows(nsrc);
+          }
           for (int c = 0; c < 256 / kStageK && ok; ++c) {
             if (!(ok = wait_bar(empty_b(bs), pb ^ 1, abort_flag, a.status, w1))) break;
             mbar_expect_tx(full_b(bs), 2 * nbox * kBoxRows * 128);
             const uint32_t bdst = sbase + kSmB + bs * kBStage;
             for (int at = 0; at < 2; ++at)
               for (int i = 0; i < nbox; ++i)
-                tma_load_2d(bdst + at * kAtomBytes + i * kBoxRows * 128, &a.map_x, 256 * b + kStageK * c + kAtomK * at,
+                tma_load_2d(bdst + at * kAtomBytesB + i * kBoxRows * 128, &a.map_x, 256 * b + kStageK * c + kAtomK * at,
                             it.start + kBoxRows * i, full_b(bs));
             if (++bs == kStagesB) { bs = 0; pb ^= 1; }
           }
@@ -670,18 +689,32 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     }
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
-    // Per block: stage 0 (8 MMAs, one commit group), stage 1 (8 MMAs + the
-    // min MMA, one commit group).  The first commit after a run of MMAs
-    // costs the issuing thread a few hundred cycles, so commits are grouped
-    // behind as much MMA work as possible.
+    // Per super-block: stage 0 (8 MMAs into S0, one commit group), stage 1
+    // (8 MMAs into S1, then the min MMA into M, one commit group).  The first
+    // commit after a run of MMAs costs the issuing thread a few hundred
+    // cycles, so commits are grouped behind as much MMA work as possible.
     if (lane == 0) {
       const uint64_t dA0 = desc_sw128(sbase + kSmA), dB0 = desc_sw128(sbase + kSmB);
       const uint64_t dA2 = desc_plain(sbase + kSmA2, 128, 256), dB2 = desc_plain(sbase + kSmB2, 2048, 128);
       uint32_t ri = 0, tb = 0;
+      uint32_t rel = 0;  // super-blocks whose TMEM slots the epilogue has released (seen in order)
       int as = 0, bs = 0;
       uint32_t pa = 0, pb = 0;
       bool ok = true;
-      static_assert(256 / kStageK == 2, "one TMEM region per half super-block");
+      static_assert(256 / kStageK == 2, "one TMEM slot per half super-block");
+      // TMEM slot j of super-block tb is ring slot 3 tb + j; before writing
+      // it, wait until the epilogue has released the super-block that used
+      // it last, (3 tb + j - kSlots) / 3.  Releases are taken in order, one
+      // phase of tempty[sb & 1] per super-block sb.
+      auto free_slot = [&](uint32_t slot) -> bool {
+        if (slot < (uint32_t)kSlots) return true;
+        const uint32_t last = (slot - kSlots) / 3;
+        while (rel <= last) {
+          if (!wait_bar(tempty(rel & 1), (rel >> 1) & 1, abort_flag, a.status, w0)) return false;
+          ++rel;
+        }
+        return true;
+      };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const PItem it = a.items[item];
         const int N = (it.count + 15) / 16 * 16;
@@ -690,21 +723,22 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           const int ab = tb & 1;
           const int rs = ri % kRaw;
           for (int c = 0; c < 2 && ok; ++c) {
-            // S0 of super-block tb reuses the region of super-block tb-2's M;
-            // S1 and M reuse tb-1's S0 and S1: wait until the epilogue has
-            // read that super-block (tempty[j & 1] completes phase j >> 1)
-            const int done = (int)tb - 2 + c;
-            if (done >= 0 && !(ok = wait_bar(tempty(done & 1), (done >> 1) & 1, abort_flag, a.status, w0))) break;
+            if (!(ok = free_slot(3 * tb + c))) break;
             if (!(ok = wait_bar(full_a(as), pa, abort_flag, a.status, w1))) break;
             if (!(ok = wait_bar(full_b(bs), pb, abort_flag, a.status, w1))) break;
             const bool last = c == 1;
             if (last && !(ok = wait_bar(full_raw(rs), (ri / kRaw) & 1, abort_flag, a.status, w1))) break;
             tc_fence_after();
-            const uint32_t dS = tmem + tmem_region(3 * tb + c), dM = tmem + tmem_region(3 * tb + 2);
+            const uint32_t dS = tmem + tmem_slot(3 * tb + c);
             const uint64_t da = dA0 + (uint64_t)((as * kAStage) >> 4), db = dB0 + (uint64_t)((bs * kBStage) >> 4);
             mma_stage4(dS, da, db, idesc, false);
-            mma_stage4(dS, da + (kAtomBytes >> 4), db + (kAtomBytes >> 4), idesc, true);
-            if (last) mma_f16(dM, dA2 + (uint64_t)((rs * 4096) >> 4), dB2 + (uint64_t)((rs * 4096) >> 4), idesc, false);
+            mma_stage4(dS, da + (kAtomBytes >> 4), db + (kAtomBytesB >> 4), idesc, true);
+            if (last) {
+              if (!(ok = free_slot(3 * tb + 2))) break;
+              tc_fence_after();
+              mma_f16(tmem + tmem_slot(3 * tb + 2), dA2 + (uint64_t)((rs * 4096) >> 4),
+                      dB2 + (uint64_t)((rs * 4096) >> 4), idesc, false);
+            }
             mma_commit(empty_a(as));
             mma_commit(empty_b(bs));
             if (last) {
@@ -721,9 +755,12 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     }
   } else {
     // ------------------------------------------------------------ epilogue (warps 0-15)
-    // Warp (qd, cg) owns TMEM lanes 32*qd.. (tile rows) and the 16-token
-    // chunks cg and cg + 4 (local token index 16*kl + j is token
-    // 16*(4*kl + cg) + j), so the four column groups share short tiles evenly.
+    // Warp (qd, cg) owns TMEM lanes 32*qd.. (tile rows) and the 8-token
+    // column blocks cg, cg + 4, cg + 8, .. (block kb of the warp is block
+    // cg + 4 kb), so short tiles spread evenly over the four column groups.
+    // Per super-block and block: three 8-column TMEM loads (S0, S1, M), one
+    // wait, then the rescale into the block's accumulators.
+    constexpr int kBlocksPerWarp = (kTileN / 8 + 3) / 4;
     const int qd = warp & 3, cg = warp >> 2;
     const int m = 32 * qd + lane;             // tile row
     float* s_da = reinterpret_cast<float*>(sm + kSmDa) + 32 * warp;
@@ -735,7 +772,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
       if (MODE == 2) ep.gate = ep.up = ep.down = a.dbg_w;
       else ep = a.table[it.expert];
       const int ntok = it.count;
-      const int N = (ntok + 15) / 16 * 16;
+      const int nblk = (ntok + 7) / 8;
       const uint8_t* hdr;  // header (d | dmin, or d) of this row's super-block 0
       if (MODE == 0) {
         const int i = it.wtile * 64 + (m >> 1);
@@ -749,11 +786,13 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         if constexpr (F::kHdrBytes == 4) return __ldg(reinterpret_cast<const uint32_t*>(p));
         else return (uint32_t)__ldg(reinterpret_cast<const unsigned short*>(p));
       };
-      unsigned long long acc[16];  // pairs of local tokens (2i, 2i+1)
+      unsigned long long acc[kBlocksPerWarp][4];  // block kb: pairs of tokens (2i, 2i+1)
 #pragma unroll
-      for (int j = 0; j < 16; ++j) acc[j] = 0ull;
-      // this lane's token: local index `lane`
-      const int tk = 16 * (4 * (lane >> 4) + cg) + (lane & 15);
+      for (int kb = 0; kb < kBlocksPerWarp; ++kb)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[kb][j] = 0ull;
+      // this lane's token (for the block scales and the down slot): i = lane % 8 of block lane / 8
+      const int tk = 8 * (cg + 4 * (lane >> 3)) + (lane & 7);
       const bool vt = tk < ntok;
       const int slot = (MODE == 1 && vt) ? __ldg(a.perm + it.start + tk) : 0;  // down: its slot row
       const float* dgp = a.dg + it.start + tk;
@@ -776,41 +815,36 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         sb_d_mscale<FMT>(dm, dw, dmin);
         const unsigned long long dw2 = f2_pack(dw, dw), ndm2 = f2_pack(-dmin, -dmin);
         const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
-        const uint32_t tS0 = tl + tmem_region(3 * tb), tS1 = tl + tmem_region(3 * tb + 1),
-                       tM = tl + tmem_region(3 * tb + 2);
+        const uint32_t tS0 = tl + tmem_slot(3 * tb), tS1 = tl + tmem_slot(3 * tb + 1), tM = tl + tmem_slot(3 * tb + 2);
 #pragma unroll
-        for (int kl = 0; kl < 2; ++kl) {
-          const int c = 4 * kl + cg;  // chunk of 16 tokens
-          if (16 * c < N) {
+        for (int kb = 0; kb < kBlocksPerWarp; ++kb) {
+          const int cb = cg + 4 * kb;  // column block (warp-uniform test)
+          if (cb < nblk) {
+            float S0v[8], S1v[8], Mv[8];
+            tmem_ld8(tS0 + 8 * cb, S0v);
+            tmem_ld8(tS1 + 8 * cb, S1v);
+            tmem_ld8(tM + 8 * cb, Mv);
+            tmem_wait_ld();
+            if constexpr (MODE == 2) {
+              // the integer sums of the super-block: S = S0 + S1 exactly (each half below 2^24)
+              const int row = it.wtile * kTileM + m;
 #pragma unroll
-            for (int q4 = 0; q4 < 4; ++q4) {
-              float S0v[4], S1v[4], Mv[4];
-              const uint32_t col = 16 * c + 4 * q4;
-              tmem_ld4(tS0 + col, S0v);
-              tmem_ld4(tS1 + col, S1v);
-              tmem_ld4(tM + col, Mv);
-              tmem_wait_ld();
-              if constexpr (MODE == 2) {
-                // the integer sums of the super-block: S = S0 + S1 exactly (each half below 2^24)
-                const int row = it.wtile * kTileM + m;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                  const int tok = col + i;
-                  if (tok < ntok) {
-                    const int64_t o = ((int64_t)(it.start + tok) * N_out + row) * nb + b;
-                    a.dbg_s[o] = (int32_t)S0v[i] + (int32_t)S1v[i];
-                    a.dbg_m[o] = (int32_t)Mv[i];
-                  }
+              for (int i = 0; i < 8; ++i) {
+                const int tok = 8 * cb + i;
+                if (tok < ntok) {
+                  const int64_t o = ((int64_t)(it.start + tok) * N_out + row) * nb + b;
+                  a.dbg_s[o] = (int32_t)S0v[i] + (int32_t)S1v[i];
+                  a.dbg_m[o] = (int32_t)Mv[i];
                 }
-              } else {
+              }
+            } else {
 #pragma unroll
-                for (int j = 0; j < 2; ++j) {
-                  // S0 + S1: both exact integers, so the fp32 sum rounds the exact S once
-                  const float2 d2 = *reinterpret_cast<const float2*>(s_da + 16 * kl + 4 * q4 + 2 * j);
-                  const unsigned long long S2 = f2_pack(S0v[2 * j] + S1v[2 * j], S0v[2 * j + 1] + S1v[2 * j + 1]);
-                  const unsigned long long t = f2_fma(dw2, S2, f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
-                  acc[8 * kl + 2 * q4 + j] = f2_fma(f2_pack(d2.x, d2.y), t, acc[8 * kl + 2 * q4 + j]);
-                }
+              for (int j = 0; j < 4; ++j) {
+                // S0 + S1: both exact integers, so the fp32 sum rounds the exact S once
+                const float2 d2 = *reinterpret_cast<const float2*>(s_da + 8 * kb + 2 * j);
+                const unsigned long long S2 = f2_pack(S0v[2 * j] + S1v[2 * j], S0v[2 * j + 1] + S1v[2 * j + 1]);
+                const unsigned long long t = f2_fma(dw2, S2, f2_mul(ndm2, f2_pack(Mv[2 * j], Mv[2 * j + 1])));
+                acc[kb][j] = f2_fma(f2_pack(d2.x, d2.y), t, acc[kb][j]);
               }
             }
           }
@@ -821,26 +855,31 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         ++tb;
       }
       if (!ok) break;
-      if constexpr (MODE == 2) continue;
+      if constexpr (MODE != 2) {
 #pragma unroll
-      for (int p = 0; p < 16; ++p) {
-        const int kl = p >> 3, j = 2 * (p & 7);
-        const int l = 16 * kl + j;                // local index of tokens tok, tok + 1
-        const int tok = 16 * (4 * kl + cg) + j;
-        const float lo = __uint_as_float((uint32_t)acc[p]), hi = __uint_as_float((uint32_t)(acc[p] >> 32));
-        if (MODE == 0) {
-          // lane pairs hold gate (even lane) and up (odd lane) of one row: SwiGLU in registers
-          const float G0 = __shfl_sync(0xffffffffu, lo, lane & ~1), G1 = __shfl_sync(0xffffffffu, hi, lane & ~1);
-          float* hcol = a.h + (int64_t)(it.start + tok) * N_out + it.wtile * 64 + (m >> 1);
-          if (lane & 1) {
-            if (tok < ntok) hcol[0] = __fdividef(G0, 1.0f + __expf(-G0)) * lo;
-            if (tok + 1 < ntok) hcol[N_out] = __fdividef(G1, 1.0f + __expf(-G1)) * hi;
+        for (int kb = 0; kb < kBlocksPerWarp; ++kb) {
+          const int cb = cg + 4 * kb;
+          if (cb >= nblk) continue;  // warp-uniform
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            const int tok = 8 * cb + 2 * j;  // tokens tok, tok + 1 of the tile
+            const float lo = __uint_as_float((uint32_t)acc[kb][j]), hi = __uint_as_float((uint32_t)(acc[kb][j] >> 32));
+            if (MODE == 0) {
+              // lane pairs hold gate (even lane) and up (odd lane) of one row: SwiGLU in registers
+              const float G0 = __shfl_sync(0xffffffffu, lo, lane & ~1), G1 = __shfl_sync(0xffffffffu, hi, lane & ~1);
+              float* hcol = a.h + (int64_t)(it.start + tok) * N_out + it.wtile * 64 + (m >> 1);
+              if (lane & 1) {
+                if (tok < ntok) hcol[0] = __fdividef(G0, 1.0f + __expf(-G0)) * lo;
+                if (tok + 1 < ntok) hcol[N_out] = __fdividef(G1, 1.0f + __expf(-G1)) * hi;
+              }
+            } else {
+              // the slot rows of the two tokens sit in lanes 8 kb + 2 j and 8 kb + 2 j + 1
+              const int s0 = __shfl_sync(0xffffffffu, slot, 8 * kb + 2 * j), s1 = __shfl_sync(0xffffffffu, slot, 8 * kb + 2 * j + 1);
+              const int col = it.wtile * 128 + m;
+              if (tok < ntok) a.y[(int64_t)s0 * N_out + col] = lo;
+              if (tok + 1 < ntok) a.y[(int64_t)s1 * N_out + col] = hi;
+            }
           }
-        } else {
-          const int s0 = __shfl_sync(0xffffffffu, slot, l), s1 = __shfl_sync(0xffffffffu, slot, l + 1);
-          const int col = it.wtile * 128 + m;
-          if (tok < ntok) a.y[(int64_t)s0 * N_out + col] = lo;
-          if (tok + 1 < ntok) a.y[(int64_t)s1 * N_out + col] = hi;
         }
       }
     }
@@ -973,7 +1012,7 @@ cudaError_t launch_prefill_fmt(const PrefillArgs& a, cudaStream_t s) {
   return cudaGetLastError();
 }
 
-// Items of the sums hook: token tiles of up to 128 rows x the 128-row weight tiles.
+// Items of the sums hook: token tiles of up to kTileN rows x the 128-row weight tiles.
 __global__ void sums_items_kernel(int T, int n_wtiles, PItem* items, int32_t* n_items) {
   const int nt = (T + kTileN - 1) / kTileN;
   for (int i = threadIdx.x; i < nt * n_wtiles; i += blockDim.x) {
@@ -1052,6 +1091,8 @@ cudaError_t launch_prefill_sums(const SumsArgs& a, cudaStream_t s) {
     default: return cudaErrorInvalidValue;
   }
 }
+
+int prefill_tile_tokens() { return kTileN; }
 
 size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I) {
   const int64_t EpS = E + S;

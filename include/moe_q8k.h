@@ -384,6 +384,13 @@ unsigned long long moe_kernel_launch_count(void);
 #define MOE_PATH_TENSOR_PREFILL 2
 int moe_layer_path(const moe_layer_desc* desc, int32_t T);
 
+/* Token tile of the tensor-core prefill path (MOE_PATH_TENSOR_PREFILL): an
+ * expert with c routed tokens gets t = ceil(c / n) token tiles of
+ * ceil(c / t) bucket rows each (the last one shorter), n the value
+ * returned.  Host-side only; launches nothing.  No counterpart on the pages
+ * (their prefill GEMM tiles are not specified). */
+int moe_prefill_tile_tokens(void);
+
 /* Which single-launch kernel moe_stack_forward runs for a stack of n_layers
  * layers of `desc` at T tokens on a device with n_sms SMs (n_sms <= 0: the
  * current device's).  Host-side only; launches nothing:

@@ -248,9 +248,9 @@ CASES = [
     (FMT_Q2K, 0, 256, 256, 8, 8, 1, 3, False),       # k = E
     (FMT_Q4K, 1, 256, 768, 1, 1, 0, 7, False),       # one expert
     (FMT_Q4K, 1, 512, 256, 40, 10, 1, 40, False),    # more than the single-CTA bucket (400 pairs)
-    # prefill chunks (tensor-core grouped GEMM): several 128-token tiles per expert, ragged tails
+    # prefill chunks (tensor-core grouped GEMM): several token tiles per expert, ragged tails
     (FMT_Q4K, 0, 512, 256, 8, 2, 1, 512, False),
-    (FMT_Q2K, 1, 768, 512, 16, 4, 0, 300, True),     # skewed router: some experts far above 128 tokens
+    (FMT_Q2K, 1, 768, 512, 16, 4, 0, 300, True),     # skewed router: some experts over several token tiles
     (FMT_Q4K, 1, 1024, 256, 4, 1, 2, 257, False),    # two shared experts, one routed slot per token
     # the Q5_K/Q3_K/Q6_K-style formats: decode (single launch), the GEMV path, a prefill chunk
     (FMT_Q5K, 0, 2048, 512, 64, 8, 1, 1, False),
@@ -515,7 +515,8 @@ def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     GEMM forms them in TMEM, equal the oracle's int64 sums bit for bit.  Rows 0-31 carry an all-extreme
     first super-block (largest codes, scales and mins); tokens 0-2 carry activation codes +127, -127 and
     127 with one 126 there, so that Q4_K sums reach 63*15*127*256 > 2^24, one of them odd.  T = 200 and
-    130 leave a ragged second token tile."""
+    130 span several token tiles with a ragged last one."""
+    assert 130 > moe.moe_prefill_tile_tokens() >= 32
     rng = np.random.default_rng(N + K + T + fmt)
     q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
     q[:32, 0] = fieldpack.QMAX[fmt]

@@ -55,8 +55,8 @@ class Rows:
 
 def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0, tile_rows=False):
     """Run one layer on the device and compare it with the oracle on `tokens`
-    (all if None); with tile_rows, also on the first and last rows of the
-    128-row token tiles of some experts (the tensor-core path's tile edges)."""
+    (all if None); with tile_rows, also on the first and last rows of every
+    token tile of some experts (the tensor-core path's tile edges)."""
     import synth.gpu  # noqa: F401
     dev = bank.buf.device
     wr = synth.router_weight(wl.E, wl.H, wl.seed, layer)
@@ -77,12 +77,17 @@ def _check_layer(moe, wl, bank, layer, T, tokens=None, rep=0, tile_rows=False):
     perm = lay.ws_view("perm", torch.int32, (P,)).cpu().numpy()
     sel = np.arange(T) if tokens is None else np.asarray(tokens)
     if tile_rows:
-        # first and last rows of the 128-row tiles of the experts with the most tokens
+        # first and last rows of the token tiles of the experts with the most tokens (and of the shared
+        # expert's first tiles): c tokens form ceil(c / n) tiles of ceil(c / tiles) rows
+        n = moe.moe_prefill_tile_tokens()
         edge = []
-        for e in np.argsort(-rc[:wl.E], kind="stable")[:6]:
-            for pos in (ro[e], ro[e] + 127, ro[e] + 128, ro[e + 1] - 1):
-                if ro[e] <= pos < ro[e + 1]:
-                    edge.append(int(perm[pos]) // wl.k)
+        for e in list(np.argsort(-rc[:wl.E], kind="stable")[:6]) + list(range(wl.E, wl.E + wl.S)):
+            c = int(rc[e])
+            per = -(-c // -(-c // n)) if c else 1
+            for t0 in range(0, min(c, 3 * per), per):
+                for pos in (ro[e] + t0, ro[e] + min(t0 + per, c) - 1):
+                    p_ = int(perm[pos])
+                    edge.append(p_ // wl.k if p_ < T * wl.k else (p_ - T * wl.k) % T)
         sel = np.unique(np.concatenate([sel, np.asarray(edge, np.int64)]))
     need = sorted(set(gids[sel].reshape(-1).tolist()) | set(range(wl.E, wl.E + wl.S)))
     experts = _host_experts(wl, layer, need)
