@@ -29,9 +29,10 @@ FMT_Q2K = 1
 FMT_Q5K = 2
 FMT_Q3K = 3
 FMT_Q6K = 4
+FMT_IQ2G = 5
 ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID = 1
-N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16}
+N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16, FMT_IQ2G: 8}
 
 
 def build(force: bool = False) -> str:
@@ -59,6 +60,8 @@ def _load():
             I = ctypes.c_int
             lib.orc_half_to_double.argtypes = [ctypes.c_uint16]
             lib.orc_half_to_double.restype = ctypes.c_double
+            lib.orc_iq2g_grid.argtypes = [P]
+            lib.orc_iq2g_grid.restype = None
             lib.orc_unpack_sb.argtypes = [P, I, I64, I64, I64, I64, P, P, P, P]
             lib.orc_unpack_sb.restype = None
             lib.orc_dequant_matrix.argtypes = [P, I, I64, I64, P]
@@ -100,6 +103,13 @@ def default_threads() -> int:
 
 def half_to_double(bits: int) -> float:
     return _load().orc_half_to_double(int(bits))
+
+
+def iq2g_grid() -> np.ndarray:
+    """The IQ2-style grid C as int32 [256, 8] (magnitudes 1, 3, 5)."""
+    out = np.zeros((256, 8), np.int32)
+    _load().orc_iq2g_grid(out.ctypes.data)
+    return out
 
 
 def unpack_sb(w: np.ndarray, fmt: int, N: int, K: int, n: int, b: int):

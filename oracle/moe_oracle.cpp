@@ -38,7 +38,15 @@
 // codes, 6-bit signed scales, w = d*scale*(q - 4); Q6_K-style: 16
 // sub-blocks, 6-bit codes, int8 scales, w = d*scale*(q - 32).  In general
 // w = d*scale*(q - o) - dmin*min, with o = 0 and a min for the first three
-// formats and o = 4 / 32 and no min (no dmin) for the last two.
+// formats and o = 4 / 32 and no min (no dmin) for Q3_K/Q6_K-style.
+// The pages also name i-quant codebook formats (Pulsar README, "What it does
+// today": IQ2_XXS builds; Strata engine article, finding 7: IQ3 codebook
+// lookups cost decode compute that K-quant shifts do not) without printing a
+// grid.  The IQ2-style grid format here is this project's own: per group of
+// 8 weights a grid index into 256 vectors of magnitudes {1, 3, 5} and 7 sign
+// bits (the 8th sign makes the minus signs even), per 32 weights a 4-bit
+// scale t (scale 2t + 1), fp16 d: w = d * (2t + 1) * sign * C[u][i].  In the
+// (q, sc) form above q is the signed grid value, o = 0, no min.
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
@@ -53,25 +61,62 @@ constexpr int kQ2K = 1;
 constexpr int kQ5K = 2;
 constexpr int kQ3K = 3;
 constexpr int kQ6K = 4;
+constexpr int kIQ2G = 5;
 
 // Per format: sub-blocks, header bytes per row (d|dmin or d), scale/min
 // bytes per row, code bytes per row, code offset o.  A slab holds the 32
 // rows' headers, then their scale/min bytes, then the code lines.
-int n_sub(int fmt) { return (fmt == kQ4K || fmt == kQ5K) ? 8 : 16; }
+int n_sub(int fmt) { return (fmt == kQ4K || fmt == kQ5K || fmt == kIQ2G) ? 8 : 16; }
 int sub_len(int fmt) { return 256 / n_sub(fmt); }
-int hdr_bytes(int fmt) { return (fmt == kQ3K || fmt == kQ6K) ? 2 : 4; }
-int sm_bytes(int fmt) { return (fmt == kQ2K || fmt == kQ6K) ? 16 : 12; }
+int hdr_bytes(int fmt) { return (fmt == kQ3K || fmt == kQ6K || fmt == kIQ2G) ? 2 : 4; }
+int sm_bytes(int fmt) { return fmt == kIQ2G ? 4 : (fmt == kQ2K || fmt == kQ6K) ? 16 : 12; }
 int code_bytes(int fmt) {
   switch (fmt) {
     case kQ4K: return 128;
     case kQ2K: return 64;
     case kQ5K: return 160;
     case kQ3K: return 96;
+    case kIQ2G: return 64;
     default: return 192;
   }
 }
 int code_offset(int fmt) { return fmt == kQ3K ? 4 : fmt == kQ6K ? 32 : 0; }
 int64_t slab_bytes(int fmt) { return 32 * (int64_t)(hdr_bytes(fmt) + sm_bytes(fmt) + code_bytes(fmt)); }
+
+// The IQ2-style grid: the 256 vectors of {1, 3, 5}^8 with the smallest sum
+// of squares, equal sums ordered by the base-3 number of the digits
+// (v_i - 1) / 2 (element 0 most significant); index = rank.  Built by
+// listing all 3^8 vectors in increasing base-3 order and sorting them
+// stably by their sum of squares.
+struct Grid {
+  int v[256][8];
+};
+const Grid& iq2g_grid() {
+  static const Grid g = [] {
+    std::vector<std::pair<int, int>> all;  // (sum of squares, base-3 number)
+    for (int t = 0; t < 6561; ++t) {
+      int x = t, ss = 0;
+      for (int i = 0; i < 8; ++i) {
+        const int v = 1 + 2 * (x % 3);
+        ss += v * v;
+        x /= 3;
+      }
+      all.push_back({ss, t});
+    }
+    std::stable_sort(all.begin(), all.end(),
+                     [](const std::pair<int, int>& a, const std::pair<int, int>& b) { return a.first < b.first; });
+    Grid out;
+    for (int u = 0; u < 256; ++u) {
+      int x = all[u].second;
+      for (int i = 7; i >= 0; --i) {  // the last digit is element 7
+        out.v[u][i] = 1 + 2 * (x % 3);
+        x /= 3;
+      }
+    }
+    return out;
+  }();
+  return g;
+}
 
 // IEEE 754 binary16 -> double, written out from the format definition.
 double half_to_double(uint16_t h) {
@@ -103,7 +148,7 @@ int read_bits(const uint8_t* p, int start, int len) {
 }
 
 struct SuperBlock {
-  int q[256];   // codes (unsigned)
+  int q[256];   // codes (unsigned; the signed grid values for the IQ2-style format)
   int sc[16];   // per-sub-block scale (signed for Q3_K/Q6_K-style)
   int mn[16];   // per-sub-block min (0 where the format has none)
   int off;      // code offset o: w = d * sc * (q - o) - dmin * mn
@@ -162,6 +207,19 @@ void unpack_sb(const uint8_t* w, int fmt, int64_t nb, int64_t n, int64_t b, Supe
         const uint8_t* base = line(4 + j / 8) + 4 * ((j / 2) % 4);
         for (int c = 0; c < 16; ++c) o->q[16 * j + c] |= ((base[c % 4] >> (c / 4 + 4 * (j % 2))) & 1) << 2;
       }
+  } else if (fmt == kIQ2G) {
+    // scales: nibble j of the 4 scale bytes; codes: index byte g in line g/16,
+    // sign byte g in line 2 + g/16 (byte g % 16 of each)
+    const Grid& C = iq2g_grid();
+    for (int j = 0; j < 8; ++j) o->sc[j] = 2 * ((sm[j / 2] >> (4 * (j % 2))) & 15) + 1;
+    for (int g = 0; g < 32; ++g) {
+      const int u = line(g / 16)[g % 16];
+      const int sb7 = line(2 + g / 16)[g % 16] & 127;
+      int neg = 0;
+      for (int i = 0; i < 7; ++i) neg ^= (sb7 >> i) & 1;  // the 8th sign: an even count of minus signs
+      const int signs = sb7 | (neg << 7);
+      for (int i = 0; i < 8; ++i) o->q[8 * g + i] = ((signs >> i) & 1) ? -C.v[u][i] : C.v[u][i];
+    }
   } else {  // Q6_K-style
     for (int j = 0; j < 16; ++j) o->sc[j] = (int)(int8_t)sm[j];
     for (int j = 0; j < 16; ++j)
@@ -270,6 +328,13 @@ extern "C" {
 
 // fp16 bit pattern -> double (exposed for the format pins).
 double orc_half_to_double(uint16_t h) { return half_to_double(h); }
+
+// The IQ2-style grid as 256 x 8 ints (exposed for the format pins).
+void orc_iq2g_grid(int32_t* out) {
+  const Grid& C = iq2g_grid();
+  for (int u = 0; u < 256; ++u)
+    for (int i = 0; i < 8; ++i) out[8 * u + i] = C.v[u][i];
+}
 
 // Unpack the fields of super-block (row n, block b) of a [N, K] matrix.
 // q: 256 ints, sc/mn: n_sub ints, dd: {d, dmin}.

@@ -15,10 +15,11 @@ bit fields, uniformly random bytes give exactly the required distributions:
 4-bit codes ~U{0..15}, 6-bit scales/mins ~U{0..63} (Q4_K-style), 2-bit codes
 ~U{0..3}, 4-bit scales/mins ~U{0..15} (Q2_K-style), 5-bit codes ~U{0..31}
 (Q5_K-style), 3-bit codes ~U{0..7} and 6-bit scales ~U{-32..31} (Q3_K-style),
-6-bit codes ~U{0..63} and int8 scales ~U{-128..127} (Q6_K-style).  Draws of
-one SB, in order: the code bytes (8 per draw, little-endian), two draws of
-scale/min bytes (the first 12 or 16 bytes used), one for d, then (formats
-with a dmin) one for dmin.  The fp16 fields are drawn as d ~ U(1e-4, 1e-3)
+6-bit codes ~U{0..63} and int8 scales ~U{-128..127} (Q6_K-style), grid
+indices ~U{0..255}, sign bits ~U{0,1} and 4-bit scales ~U{0..15} (IQ2-style
+grid format).  Draws of one SB, in order: the code bytes (8 per draw,
+little-endian), two draws of scale/min bytes (the first 4, 12 or 16 bytes
+used), one for d, then (formats with a dmin) one for dmin.  The fp16 fields are drawn as d ~ U(1e-4, 1e-3)
 and dmin ~ U(0, 5e-4): a 24-bit integer u gives f = u * 2^-24 in fp32
 (exact), then ``lo + f * (hi - lo)`` with one fp32 multiply and one fp32
 add, each rounded to nearest even, then fp32 -> fp16 round-to-nearest-even.
@@ -35,13 +36,13 @@ from __future__ import annotations
 import numpy as np
 
 from . import layout
-from .layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, sb_bytes, matrix_bytes
+from .layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FMT_IQ2G, sb_bytes, matrix_bytes
 
 MASK64 = (1 << 64) - 1
 GAMMA = 0x9E3779B97F4A7C15
 
 # draws per super-block: codes, then scale/min bytes, then d, then dmin
-_N_CODE_DRAWS = {f: layout.CODE_BYTES[f] // 8 for f in layout.FORMATS}   # 16, 8, 20, 12, 24
+_N_CODE_DRAWS = {f: layout.CODE_BYTES[f] // 8 for f in layout.FORMATS}   # 16, 8, 20, 12, 24, 8
 _N_SM_DRAWS = 2
 DRAWS_PER_SB = 32          # counter stride per super-block (at most 28 used)
 
@@ -111,7 +112,7 @@ def _dmin_bits(draw: np.ndarray) -> np.ndarray:
 def gen_sb_fields(fmt: int, key: int, sb_index: np.ndarray):
     """Raw per-super-block bytes (logical order) for the given SB indices.
 
-    Returns (code_bytes [n, code bytes] uint8, sm_bytes [n, 12|16] uint8,
+    Returns (code_bytes [n, code bytes] uint8, sm_bytes [n, 4|12|16] uint8,
     d_bits [n] uint16, dmin_bits [n] uint16 or None for the formats without
     a dmin).
     """
@@ -158,6 +159,6 @@ def router_bias(E: int, std: float, seed: int, layer: int = 0) -> np.ndarray:
 
 
 __all__ = [
-    "layout", "FMT_Q4K", "FMT_Q2K", "FMT_Q5K", "FMT_Q3K", "FMT_Q6K", "sb_bytes", "matrix_bytes", "matrix_key", "sb_draws",
+    "layout", "FMT_Q4K", "FMT_Q2K", "FMT_Q5K", "FMT_Q3K", "FMT_Q6K", "FMT_IQ2G", "sb_bytes", "matrix_bytes", "matrix_key", "sb_draws",
     "gen_sb_fields", "gen_matrix", "activations", "router_weight", "router_bias", "normal_f32",
 ]

@@ -104,8 +104,10 @@ __global__ void fill_generic(uint8_t* __restrict__ w, int64_t N, int64_t nb, uin
   const uint64_t s0 = draw(key, sb, NCODE), s1 = draw(key, sb, NCODE + 1);
   uint32_t* sm = reinterpret_cast<uint32_t*>(slab + kSmOff + SMB * r);
   sm[0] = (uint32_t)s0;
-  sm[1] = (uint32_t)(s0 >> 32);
-  sm[2] = (uint32_t)s1;
+  if (SMB >= 12) {
+    sm[1] = (uint32_t)(s0 >> 32);
+    sm[2] = (uint32_t)s1;
+  }
   if (SMB == 16) sm[3] = (uint32_t)(s1 >> 32);
   const uint16_t db = d_bits(draw(key, sb, NCODE + 2));
   if (HB == 4)
@@ -120,10 +122,10 @@ extern "C" {
 
 // Fill one [N, K] matrix at dst (device pointer, 16-byte aligned) with the
 // stream of `key`.  fmt 0 = Q4_K-style, 1 = Q2_K-style, 2 = Q5_K-style,
-// 3 = Q3_K-style, 4 = Q6_K-style.  Returns 0 on success, 1 on a bad argument,
+// 3 = Q3_K-style, 4 = Q6_K-style, 5 = IQ2-style grid format.  Returns 0 on success, 1 on a bad argument,
 // 2 on a CUDA launch error.
 int synth_fill_matrix(void* dst, int fmt, int64_t N, int64_t K, uint64_t key, void* stream) {
-  if (!dst || N <= 0 || K <= 0 || N % 256 || K % 256 || fmt < 0 || fmt > 4) return 1;
+  if (!dst || N <= 0 || K <= 0 || N % 256 || K % 256 || fmt < 0 || fmt > 5) return 1;
   if (reinterpret_cast<uintptr_t>(dst) & 15) return 1;
   int64_t nb = K / 256;
   int64_t total = N * nb;
@@ -136,7 +138,8 @@ int synth_fill_matrix(void* dst, int fmt, int64_t N, int64_t K, uint64_t key, vo
     case 1: fill_q2k<<<blocks, threads, 0, s>>>(w, N, nb, key); break;
     case 2: fill_generic<20, 4, 12><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
     case 3: fill_generic<12, 2, 12><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
-    default: fill_generic<24, 2, 16><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    case 4: fill_generic<24, 2, 16><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
+    default: fill_generic<8, 2, 4><<<blocks, threads, 0, s>>>(w, N, nb, key); break;
   }
   return cudaGetLastError() == cudaSuccess ? 0 : 2;
 }

@@ -20,6 +20,16 @@ into 256-wide super-blocks (SB): row n, SB b covers columns 256*b ..
   Q6_K-style (210 B per SB): fp16 d, sixteen 16-weight sub-blocks with an
     int8 scale each (16 B), 256 6-bit codes: the low 4 bits (128 B) and a
     plane of the high 2 bits (64 B); weight = d * scale_j * (q - 32).
+  IQ2-style grid format (70 B per SB, 2.19 bits per weight): fp16 d, eight
+    32-weight sub-blocks with a 4-bit scale t_j each (4 B), and per group
+    g of 8 weights (32 groups, sub-block j = groups 4j..4j+3) a grid index
+    u_g (1 B) and 7 sign bits (1 B; the 8th sign makes the number of minus
+    signs even); weight 8g + i = d * (2 t_j + 1) * s_{g,i} * C[u_g][i].
+    The grid C: the 256 vectors of {1, 3, 5}^8 with the smallest sum of
+    squares, equal sums in increasing order of the base-3 number whose
+    digits are (v_0 - 1)/2 .. (v_7 - 1)/2 (v_0 most significant); u = rank.
+    (The pages name i-quant codebook formats but print no grid: this grid
+    is this project's own.)
 
 Placement.  Rows are grouped 32 at a time (row group rg = n // 32, lane
 r = n % 32).  The matrix is the sequence of slabs (rg, b) in order
@@ -47,12 +57,17 @@ by field:
         code i of sub-block 2l (low nibble) and of sub-block 2l + 1 (high
         nibble); lines 8..11 (high 2 bits): line 8 + j // 4, byte i, bits
         2*(j % 4)..+1 are bits 4-5 of code i of sub-block j.
+  IQ2G: 2240 B; lines 0, 1: the grid indices, byte 16 l + i of the row =
+        u_{16 l + i} (so sub-block j's four indices are word j % 4 of line
+        j // 4); lines 2, 3: the sign bytes in the same order (bit i < 7 of
+        byte g is 1 when weight 8g + i is negative; bit 7 is ignored).
 
 Scale/min bytes: Q4_K/Q5_K: a 96-bit little-endian bit string; scale j is
 bits 6j..6j+5 and min j is bits 48+6j..48+6j+5 (bit i of the string is bit
 i%8 of byte i//8).  Q2_K: byte j = scale_j | min_j << 4.  Q3_K: the same
 96-bit string holding u_0..u_15 at bits 6j..6j+5.  Q6_K: byte j = scale_j
-as int8.
+as int8.  IQ2G: byte j // 2 holds t_j in its low (j even) or high (j odd)
+nibble.
 
 Logical SB bytes (what the generator draws): the code bytes of the planes in
 order (code byte i of a plane goes to line i // 16 of that plane, byte
@@ -71,18 +86,20 @@ FMT_Q2K = 1
 FMT_Q5K = 2
 FMT_Q3K = 3
 FMT_Q6K = 4
-FORMATS = (FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K)
-NAMES = {FMT_Q4K: "q4_k", FMT_Q2K: "q2_k", FMT_Q5K: "q5_k", FMT_Q3K: "q3_k", FMT_Q6K: "q6_k"}
+FMT_IQ2G = 5
+FORMATS = (FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FMT_IQ2G)
+NAMES = {FMT_Q4K: "q4_k", FMT_Q2K: "q2_k", FMT_Q5K: "q5_k", FMT_Q3K: "q3_k", FMT_Q6K: "q6_k", FMT_IQ2G: "iq2_g"}
 
-HDR_BYTES = {FMT_Q4K: 4, FMT_Q2K: 4, FMT_Q5K: 4, FMT_Q3K: 2, FMT_Q6K: 2}   # per row
+HDR_BYTES = {FMT_Q4K: 4, FMT_Q2K: 4, FMT_Q5K: 4, FMT_Q3K: 2, FMT_Q6K: 2, FMT_IQ2G: 2}   # per row
 HAS_DMIN = {f: HDR_BYTES[f] == 4 for f in FORMATS}
-SM_BYTES = {FMT_Q4K: 12, FMT_Q2K: 16, FMT_Q5K: 12, FMT_Q3K: 12, FMT_Q6K: 16}
-PLANES = {FMT_Q4K: (128,), FMT_Q2K: (64,), FMT_Q5K: (128, 32), FMT_Q3K: (64, 32), FMT_Q6K: (128, 64)}
+SM_BYTES = {FMT_Q4K: 12, FMT_Q2K: 16, FMT_Q5K: 12, FMT_Q3K: 12, FMT_Q6K: 16, FMT_IQ2G: 4}
+PLANES = {FMT_Q4K: (128,), FMT_Q2K: (64,), FMT_Q5K: (128, 32), FMT_Q3K: (64, 32), FMT_Q6K: (128, 64),
+          FMT_IQ2G: (32, 32)}
 CODE_BYTES = {f: sum(PLANES[f]) for f in FORMATS}
 SB_BYTES = {f: HDR_BYTES[f] + SM_BYTES[f] + CODE_BYTES[f] for f in FORMATS}
-N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16}
+N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16, FMT_IQ2G: 8}
 SUB_LEN = {f: 256 // N_SUB[f] for f in FORMATS}
-CODE_BITS = {FMT_Q4K: 4, FMT_Q2K: 2, FMT_Q5K: 5, FMT_Q3K: 3, FMT_Q6K: 6}
+CODE_BITS = {FMT_Q4K: 4, FMT_Q2K: 2, FMT_Q5K: 5, FMT_Q3K: 3, FMT_Q6K: 6, FMT_IQ2G: 2}
 SLAB_BYTES = {f: 32 * SB_BYTES[f] for f in FORMATS}
 SM_OFFSET = {f: 32 * HDR_BYTES[f] for f in FORMATS}
 CODE_OFFSET = {f: SM_OFFSET[f] + 32 * SM_BYTES[f] for f in FORMATS}

@@ -6,18 +6,23 @@ kernels: it encodes chosen codes/scales/mins/d/dmin by the layout rules
 fields.  The slab placement reuses synth.layout.pack (which only moves bytes).
 Scales are passed signed where the format's scale is signed (Q3_K-style:
 -32..31, Q6_K-style: -128..127); the symmetric formats have no min and no
-dmin (zeros are passed and ignored).
+dmin (zeros are passed and ignored).  For the IQ2-style grid format the
+"codes" are the signed weight values s * C[u][i] and the scale is 2t + 1;
+encoding finds each group's grid index in the grid the oracle exports (the
+grid itself is pinned by its own tests) and checks the sign parity rule.
 """
 from __future__ import annotations
 
 import numpy as np
 
 from synth import layout
-from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K
+from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FMT_IQ2G
 
-QMAX = {FMT_Q4K: 15, FMT_Q2K: 3, FMT_Q5K: 31, FMT_Q3K: 7, FMT_Q6K: 63}
-SCALE_RANGE = {FMT_Q4K: (0, 63), FMT_Q2K: (0, 15), FMT_Q5K: (0, 63), FMT_Q3K: (-32, 31), FMT_Q6K: (-128, 127)}
-MIN_RANGE = {FMT_Q4K: (0, 63), FMT_Q2K: (0, 15), FMT_Q5K: (0, 63), FMT_Q3K: (0, 0), FMT_Q6K: (0, 0)}
+QMAX = {FMT_Q4K: 15, FMT_Q2K: 3, FMT_Q5K: 31, FMT_Q3K: 7, FMT_Q6K: 63, FMT_IQ2G: 5}
+SCALE_RANGE = {FMT_Q4K: (0, 63), FMT_Q2K: (0, 15), FMT_Q5K: (0, 63), FMT_Q3K: (-32, 31), FMT_Q6K: (-128, 127),
+               FMT_IQ2G: (1, 31)}
+MIN_RANGE = {FMT_Q4K: (0, 63), FMT_Q2K: (0, 15), FMT_Q5K: (0, 63), FMT_Q3K: (0, 0), FMT_Q6K: (0, 0),
+             FMT_IQ2G: (0, 0)}
 OFFSET = {FMT_Q3K: 4, FMT_Q6K: 32}          # symmetric formats: weight = d * scale * (q - offset)
 SYMMETRIC = (FMT_Q3K, FMT_Q6K)
 
@@ -39,9 +44,40 @@ def _q2k_lines(q):
     return byte.reshape(*lead, 64)
 
 
+_GRID_INDEX = None
+
+
+def _grid_index():
+    """{tuple of 8 magnitudes: grid index} of the oracle's IQ2-style grid."""
+    global _GRID_INDEX
+    if _GRID_INDEX is None:
+        import oracle
+        _GRID_INDEX = {tuple(int(v) for v in row): u for u, row in enumerate(oracle.iq2g_grid())}
+    return _GRID_INDEX
+
+
+def _iq2g_planes(q):
+    """signed values [..., 256] -> 64 bytes: 32 grid indices, then 32 sign bytes (bits 0-6)."""
+    lead = q.shape[:-1]
+    grp = q.reshape(-1, 32, 8)
+    idx = np.zeros((grp.shape[0], 32), np.uint8)
+    sgn = np.zeros((grp.shape[0], 32), np.uint8)
+    gi = _grid_index()
+    for r in range(grp.shape[0]):
+        for g in range(32):
+            v = grp[r, g]
+            neg = (v < 0).astype(np.int64)
+            assert neg.sum() % 2 == 0, "an IQ2-style group has an even number of negative weights"
+            idx[r, g] = gi[tuple(int(x) for x in np.abs(v))]
+            sgn[r, g] = int((neg[:7] << np.arange(7)).sum())
+    return np.concatenate([idx, sgn], axis=1).reshape(*lead, 64)
+
+
 def encode_codes(fmt: int, q: np.ndarray) -> np.ndarray:
     """codes [..., 256] -> logical code bytes [..., CODE_BYTES] (the planes in order)."""
     q = np.asarray(q).astype(np.int64)
+    if fmt == FMT_IQ2G:
+        return _iq2g_planes(q)
     assert q.min() >= 0 and q.max() <= QMAX[fmt]
     lead = q.shape[:-1]
     if fmt == FMT_Q4K:
@@ -108,6 +144,10 @@ def encode_scales(fmt: int, sc: np.ndarray, mn: np.ndarray) -> np.ndarray:
         return _bits96(np.concatenate([sc, mn], axis=-1))
     if fmt == FMT_Q3K:
         return _bits96(sc + 32)
+    if fmt == FMT_IQ2G:
+        assert (sc % 2 == 1).all()
+        t = ((sc - 1) // 2).astype(np.uint8)
+        return (t[..., 0::2] | (t[..., 1::2] << 4)).astype(np.uint8)
     return sc.astype(np.int8).view(np.uint8)
 
 
@@ -126,8 +166,17 @@ def pack_fields(fmt: int, N: int, K: int, q, sc, mn, d, dmin) -> np.ndarray:
 def random_fields(fmt: int, N: int, K: int, rng: np.random.Generator):
     nb = K // 256
     ns = layout.N_SUB[fmt]
-    q = rng.integers(0, QMAX[fmt] + 1, (N, nb, 256))
-    sc = rng.integers(SCALE_RANGE[fmt][0], SCALE_RANGE[fmt][1] + 1, (N, nb, ns))
+    if fmt == FMT_IQ2G:
+        import oracle
+        grid = oracle.iq2g_grid().astype(np.int64)
+        u = rng.integers(0, 256, (N, nb, 32))
+        neg = rng.integers(0, 2, (N, nb, 32, 8))
+        neg[..., 7] = neg[..., :7].sum(axis=-1) % 2      # an even number of minus signs
+        q = (grid[u] * (1 - 2 * neg)).reshape(N, nb, 256)
+        sc = 2 * rng.integers(0, 16, (N, nb, ns)) + 1
+    else:
+        q = rng.integers(0, QMAX[fmt] + 1, (N, nb, 256))
+        sc = rng.integers(SCALE_RANGE[fmt][0], SCALE_RANGE[fmt][1] + 1, (N, nb, ns))
     mn = rng.integers(MIN_RANGE[fmt][0], MIN_RANGE[fmt][1] + 1, (N, nb, ns))
     d = rng.uniform(1e-4, 1e-3, (N, nb)).astype(np.float16)
     dmin = rng.uniform(0, 5e-4, (N, nb)).astype(np.float16) if layout.HAS_DMIN[fmt] else np.zeros((N, nb), np.float16)

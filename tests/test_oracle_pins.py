@@ -14,7 +14,7 @@ import pytest
 
 import oracle
 import synth
-from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FORMATS
+from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FMT_IQ2G, FORMATS
 from tests import fieldpack
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
@@ -137,7 +137,7 @@ def test_integer_subblock_dot_equals_dense_dequantized_dot(fmt):
     np.testing.assert_array_equal(isum, np.einsum("nbjs,tbjs->tnbj", qw, qa))
 
 
-@pytest.mark.parametrize("fmt", FORMATS)
+@pytest.mark.parametrize("fmt", [f for f in FORMATS if f != FMT_IQ2G])   # its scales 2t + 1 are never 0
 def test_zero_scale_and_min_give_zero(fmt):
     rng = np.random.default_rng(41)
     N, K = 256, 256
@@ -269,6 +269,75 @@ def test_extreme_fields_closed_form(fmt):
     assert (oracle.qmatvec(w, fmt, N, K, xq, xd) == want).all()
     q, sc, m, dd, dm = oracle.unpack_sb(w, fmt, N, K, 5, 0)
     assert (q == qmax).all() and (sc == scale).all() and dd == 0.5
+
+
+# ------------------------------------------------------- IQ2-style grid format
+
+def test_iq2g_grid_class_sizes_closed_form():
+    """A vector of {1, 3, 5}^8 with a threes and b fives has sum of squares 8 + 8a + 24b, and there are
+    C(8, a) C(8 - a, b) of them.  The grid takes every vector with a sum below 48 (1 + 8 + 28 + 64 + 126 =
+    227 of them) and the first 29 of sum 48."""
+    from math import comb
+    g = oracle.iq2g_grid()
+    assert g.shape == (256, 8) and set(np.unique(g)) <= {1, 3, 5}
+    ss = (g.astype(np.int64) ** 2).sum(axis=1)
+    want = {}
+    for a in range(9):
+        for b in range(9 - a):
+            n = 8 + 8 * a + 24 * b
+            want[n] = want.get(n, 0) + comb(8, a) * comb(8 - a, b)
+    got = {int(k): int(v) for k, v in zip(*np.unique(ss, return_counts=True))}
+    assert got == {8: want[8], 16: want[16], 24: want[24], 32: want[32], 40: want[40], 48: 29}
+    assert (want[8], want[16], want[24], want[32], want[40]) == (1, 8, 28, 64, 126)
+    assert (np.diff(ss) >= 0).all()                               # ordered by the sum of squares
+    assert len({tuple(r) for r in g.tolist()}) == 256              # distinct
+
+
+def test_iq2g_grid_entries_by_hand():
+    """Entries worked out from the rule: 0 is all ones; 1..8 put one 3 at element 7, 6, .., 0 (smallest
+    base-3 number first, element 0 most significant); 9 is the first sum-24 vector, threes at 6 and 7; 37 is
+    the first sum-32 vector: one 5 at element 7 (digit 2 = base-3 number 2, below three 3s = 13)."""
+    g = oracle.iq2g_grid()
+    assert (g[0] == 1).all()
+    for u in range(1, 9):
+        want = np.ones(8, np.int32)
+        want[8 - u] = 3
+        np.testing.assert_array_equal(g[u], want)
+    np.testing.assert_array_equal(g[9], [1, 1, 1, 1, 1, 1, 3, 3])
+    np.testing.assert_array_equal(g[37], [1, 1, 1, 1, 1, 1, 1, 5])
+
+
+def test_iq2g_grid_brute_force():
+    """The rule by brute force over all 3^8 vectors (itertools order is increasing base-3 order)."""
+    import itertools
+    allv = [(sum(v * v for v in vec), n, vec) for n, vec in enumerate(itertools.product((1, 3, 5), repeat=8))]
+    allv.sort()
+    np.testing.assert_array_equal(oracle.iq2g_grid(), np.array([vec for _, _, vec in allv[:256]]))
+
+
+def test_iq2g_closed_form_groups():
+    """Hand-derived outputs (activation codes all -127, d_a = 1, d = 0.5):
+    grid entry 0, no signs, t = 15 (scale 31): y = -127 * 256 * 0.5 * 31;
+    grid entry 1 (element 7 = 3) with sign bit 0 set: the 8th sign is then minus too, so each group sums
+    -1 + 6 * 1 - 3 = 2 and y = -127 * 32 * 2 * 0.5 * scale, with scales 1, 3, .., 15 over the sub-blocks."""
+    fmt, N, K = FMT_IQ2G, 256, 256
+    ones = np.ones(256, np.int64)
+    w = fieldpack.pack_fields(fmt, N, K, np.tile(ones, (N, 1, 1)), np.full((N, 1, 8), 31), np.zeros((N, 1, 8)),
+                              np.full((N, 1), 0.5, np.float16), np.zeros((N, 1), np.float16))
+    xq, xd, _ = oracle.q8k_quantize(np.full((1, K), -127.0, np.float32))
+    assert (oracle.qmatvec(w, fmt, N, K, xq, xd) == -127 * 256 * 0.5 * 31).all()
+    grp = np.array([-1, 1, 1, 1, 1, 1, 1, -3])
+    scales = np.arange(1, 17, 2)
+    w = fieldpack.pack_fields(fmt, N, K, np.tile(np.tile(grp, 32), (N, 1, 1)), np.tile(scales, (N, 1, 1)),
+                              np.zeros((N, 1, 8)), np.full((N, 1), 0.5, np.float16), np.zeros((N, 1), np.float16))
+    y = oracle.qmatvec(w, fmt, N, K, xq, xd)
+    assert (y == sum(-127 * 4 * 2 * 0.5 * s for s in scales)).all()
+    # the stored bytes of one row: index byte 1 per group, sign byte 0b0000001 per group, scale nibbles t = 0..7
+    slab = w[:synth.layout.SLAB_BYTES[fmt]]
+    codes = slab[synth.layout.CODE_OFFSET[fmt]:].reshape(4, 32, 16)
+    assert (codes[0:2, 3] == 1).all() and (codes[2:4, 3] == 1).all()
+    sm = slab[synth.layout.SM_OFFSET[fmt]:synth.layout.CODE_OFFSET[fmt]].reshape(32, 4)
+    np.testing.assert_array_equal(sm[3], [0x10, 0x32, 0x54, 0x76])
 
 
 # ---------------------------------------------------------------- routing

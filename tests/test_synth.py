@@ -36,7 +36,14 @@ def test_generated_fields_follow_the_workload_distributions(fmt):
     q = np.concatenate(qs); sc = np.concatenate(scs); mn = np.concatenate(mns)
     ds = np.array(ds); dms = np.array(dms)
     checks = [(q, 0, qmax), (sc, slo, shi)]
-    if fmt not in fieldpack.SYMMETRIC:
+    if fmt == synth.FMT_IQ2G:
+        # grid indices U{0..255}, scales 2t + 1 with t ~ U{0..15}, each sign a fair coin (bit 7: parity)
+        gi = fieldpack._grid_index()
+        grp = q.reshape(-1, 8)
+        idx = np.array([gi[tuple(int(x) for x in np.abs(r))] for r in grp])
+        checks = [(idx, 0, 255), ((sc - 1) // 2, 0, 15), ((grp[:, :7] < 0).astype(np.int64).reshape(-1), 0, 1)]
+        assert ((grp < 0).sum(axis=1) % 2 == 0).all()
+    elif fmt not in fieldpack.SYMMETRIC:
         checks.append((mn, 0, fieldpack.MIN_RANGE[fmt][1]))
     else:
         assert (mn == 0).all() and (dms == 0).all()
@@ -47,7 +54,7 @@ def test_generated_fields_follow_the_workload_distributions(fmt):
         assert np.abs(hist - expect).max() < 6 * np.sqrt(expect) + 3
     assert ds.min() >= 1e-4 * 0.999 and ds.max() <= 1e-3 * 1.001
     assert abs(ds.mean() - 5.5e-4) < 3e-5
-    if fmt not in fieldpack.SYMMETRIC:
+    if synth.layout.HAS_DMIN[fmt]:
         assert dms.min() >= 0 and dms.max() <= 5e-4 * 1.001
         assert abs(dms.mean() - 2.5e-4) < 2e-5
 
