@@ -49,6 +49,8 @@ def parse_args():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=DEFAULT_BENCH, choices=sorted(WORKLOADS))
     ap.add_argument("--T", type=int, default=None, help="tokens per layer (overrides the workload's)")
+    ap.add_argument("--fmt", default=None, choices=sorted(synth.layout.NAMES.values()),
+                    help="weight format (overrides the workload's, e.g. iq2_g for the grid format)")
     ap.add_argument("--layers", type=int, default=None,
                     help="layers (overrides the workload's; smaller cases for profiling captures)")
     ap.add_argument("--rotations", type=int, default=16, help="distinct input sets cycled through the steps")
@@ -705,6 +707,11 @@ def main():
     T = args.T or wl.T
     if args.T:
         wl = wl.with_T(T)
+    if args.fmt:
+        import dataclasses
+        fmt = {v: k for k, v in synth.layout.NAMES.items()}[args.fmt]
+        old = synth.layout.NAMES[wl.fmt].replace("_", "")
+        wl = dataclasses.replace(wl, fmt=fmt, name=wl.name.replace(old, args.fmt.replace("_", "")))
     if args.layers:
         import dataclasses
         wl = dataclasses.replace(wl, layers=args.layers, name=f"{wl.name}_l{args.layers}")

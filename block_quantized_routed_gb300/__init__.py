@@ -18,7 +18,8 @@ import os
 from . import _build
 
 __all__ = [
-    "MoeError", "LayerDesc", "WsLayout", "FMT_Q4K", "FMT_Q2K", "FMT_Q5K", "FMT_Q3K", "FMT_Q6K", "ROUTE_SOFTMAX",
+    "MoeError", "LayerDesc", "WsLayout", "FMT_Q4K", "FMT_Q2K", "FMT_Q5K", "FMT_Q3K", "FMT_Q6K", "FMT_IQ2G",
+    "ROUTE_SOFTMAX",
     "ROUTE_SIGMOID",
     "load", "lib", "moe_q8k_quantize", "moe_route_topk", "moe_bucket", "moe_bucket_workspace_size",
     "moe_expert_ffn", "moe_expert_ffn_workspace_size", "moe_combine", "moe_layer_forward",
@@ -34,10 +35,11 @@ FMT_Q2K = 1
 FMT_Q5K = 2
 FMT_Q3K = 3
 FMT_Q6K = 4
+FMT_IQ2G = 5
 ROUTE_SOFTMAX = 0
 ROUTE_SIGMOID = 1
-SB_BYTES = {FMT_Q4K: 144, FMT_Q2K: 84, FMT_Q5K: 176, FMT_Q3K: 110, FMT_Q6K: 210}
-N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16}
+SB_BYTES = {FMT_Q4K: 144, FMT_Q2K: 84, FMT_Q5K: 176, FMT_Q3K: 110, FMT_Q6K: 210, FMT_IQ2G: 70}
+N_SUB = {FMT_Q4K: 8, FMT_Q2K: 16, FMT_Q5K: 8, FMT_Q3K: 16, FMT_Q6K: 16, FMT_IQ2G: 8}
 
 PATH_DECODE_FUSED = 0
 PATH_GEMV = 1

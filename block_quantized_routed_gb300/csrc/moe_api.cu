@@ -43,7 +43,7 @@ bool desc_valid(const moe_layer_desc* d, int* why) {
   if (d->top_k < 1 || d->top_k > MOE_MAX_TOPK || d->top_k > d->E) return false;
   if (d->n_shared < 0 || d->n_shared > MOE_MAX_SHARED) return false;
   if (d->route != MOE_ROUTE_SOFTMAX && d->route != MOE_ROUTE_SIGMOID) return false;
-  if (d->fmt < MOE_FMT_Q4K || d->fmt > MOE_FMT_Q6K) return false;
+  if (d->fmt < MOE_FMT_Q4K || d->fmt > MOE_FMT_IQ2G) return false;
   if (d->T_max < 1 || (int64_t)d->T_max * (d->top_k + d->n_shared) > (int64_t)1 << 28) return false;
   return true;
 }
@@ -388,7 +388,8 @@ int moe_layer_forward(const moe_layer_desc* desc, const moe_expert_ptrs* table, 
     }
   }
   if (record_error(launch_q8k_quantize(x, T, H, xq, xd, xbs, s)) != cudaSuccess) return MOE_ERR_CUDA;
-  if (record_error(launch_router(x, w_router, router_bias, T, H, E, logits, s)) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record_error(launch_router(x, w_router, router_bias, T, H, E, logits, s, status)) != cudaSuccess)
+    return MOE_ERR_CUDA;
   const bool use_prefill = prefill_path(T, k, E, desc->fmt) && prefill_fits(desc->T_max, *desc);  // buffers sized by T_max
   if (use_prefill) {
     // prefill chunk: top-k, bucketing, then the tcgen05 grouped GEMMs
@@ -680,7 +681,7 @@ int moe_debug_wait_timeout(void* ws, int32_t limit_us, void* stream) {
 
 int moe_debug_subblock_dots(int32_t fmt, const void* w, int32_t N, int32_t K, const int8_t* q, int32_t T,
                             int32_t* isum, int32_t* bsum, void* stream) {
-  if (fmt < MOE_FMT_Q4K || fmt > MOE_FMT_Q6K) return MOE_ERR_UNSUPPORTED;
+  if (fmt < MOE_FMT_Q4K || fmt > MOE_FMT_IQ2G) return MOE_ERR_UNSUPPORTED;
   if (N <= 0 || K <= 0 || N % 256 || K % 256 || T < 1 || T > 16) return MOE_ERR_UNSUPPORTED;
   if (!w || !q || !isum || !bsum) return MOE_ERR_INVALID_ARG;
   if (!aligned(w, 16) || !aligned(q, 16)) return MOE_ERR_INVALID_ARG;

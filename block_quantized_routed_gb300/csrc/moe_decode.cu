@@ -21,6 +21,7 @@ cudaError_t launch_decode_fused(const DecodeArgs& a, cudaStream_t s) {
     case kQ5K: return launch_decode_fused_q5k(a, s);
     case kQ3K: return launch_decode_fused_q3k(a, s);
     case kQ6K: return launch_decode_fused_q6k(a, s);
+    case kIQ2G: return launch_decode_fused_iq2g(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -32,6 +33,7 @@ cudaError_t launch_decode_stack(const DecodeArgs& a, cudaStream_t s) {
     case kQ5K: return launch_decode_stack_q5k(a, s);
     case kQ3K: return launch_decode_stack_q3k(a, s);
     case kQ6K: return launch_decode_stack_q6k(a, s);
+    case kIQ2G: return launch_decode_stack_iq2g(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

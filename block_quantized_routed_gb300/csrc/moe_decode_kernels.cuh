@@ -749,6 +749,7 @@ __device__ bool layers_independent(const DecodeArgs& a, int n_layers) {
 template <int FMT>
 __global__ void __launch_bounds__(kDecThreads, 1) decode_fused_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
+  stage_format_tables<FMT>();
   Ctx<FMT> c(a, smem_raw);
   const int L = a.n_layers > 0 ? a.n_layers : 1;
   const bool pipelined = a.layers && L > 1 && a.pipeline_ok && layers_independent(a, L);
@@ -1749,6 +1750,7 @@ template <int FMT, bool kRing, int NW>
 __global__ void __launch_bounds__(32 * NW, NW == 4 ? 2 : 1) decode_stack_kernel(const __grid_constant__ DecodeArgs a) {
   extern __shared__ __align__(16) uint8_t smem_raw[];
   const long long t_launch = clock64();
+  stage_format_tables<FMT>();
   Ctx<FMT> c(a, smem_raw);
   // kRing: each warp's two weight stages after the decode buffers
   WarpRing<FMT> ring;
@@ -1927,7 +1929,7 @@ cudaError_t launch_stack_t(const DecodeArgs& a, cudaStream_t s) {
   cudaError_t err = cudaGetDevice(&dev);
   if (err == cudaSuccess) err = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (err != cudaSuccess) return err;
-  const size_t spare = 1024;  // the kernel's static shared variables
+  const size_t spare = 1024 + (FMT == kIQ2G ? kIq2gSmemBytes : 0);  // the kernel's static shared variables
   const size_t unit = (size_t)kRingStages * ring_unit_bytes<FMT>();
   const size_t ring4 = ring_offset(decode_smem(a.T, a.H, a.I, a.E, a.k, a.S, 4, nullptr, nullptr)) + 4 * unit;
   if (ring4 + spare <= (size_t)optin) {

@@ -28,6 +28,7 @@ constexpr int kQ2K = MOE_FMT_Q2K;
 constexpr int kQ5K = MOE_FMT_Q5K;
 constexpr int kQ3K = MOE_FMT_Q3K;
 constexpr int kQ6K = MOE_FMT_Q6K;
+constexpr int kIQ2G = MOE_FMT_IQ2G;
 
 // Field sizes of a format (per row of a 32-row slab): header (d | dmin << 16,
 // or d alone), scale/min bytes, code bytes; the slab places the 32 headers,
@@ -56,6 +57,60 @@ template <> struct Fmt<kQ2K> : FmtBase<4, 16, 64, 16, 0> {};   // 84 B, slab 268
 template <> struct Fmt<kQ5K> : FmtBase<4, 12, 160, 8, 0> {};   // 176 B, slab 5632
 template <> struct Fmt<kQ3K> : FmtBase<2, 12, 96, 16, 4> {};   // 110 B, slab 3520
 template <> struct Fmt<kQ6K> : FmtBase<2, 16, 192, 16, 32> {}; // 210 B, slab 6720
+template <> struct Fmt<kIQ2G> : FmtBase<2, 4, 64, 8, 0> {};     // 70 B, slab 2240 (no min: mn = 0)
+
+// The IQ2-style grid, built at compile time from its rule: the 256 vectors
+// of {1, 3, 5}^8 with the smallest sums of squares, equal sums in increasing
+// base-3 order of the digits (v - 1) / 2 with element 0 the most significant
+// digit.  Entry u packs element i into byte i.
+struct Iq2gGrid {
+  uint64_t v[256];
+};
+constexpr Iq2gGrid make_iq2g_grid() {
+  Iq2gGrid g{};
+  int sums[6561] = {};
+  uint64_t packed[6561] = {};
+  for (int t = 0; t < 6561; ++t) {
+    int x = t;
+    for (int i = 7; i >= 0; --i) {  // the lowest base-3 digit is element 7
+      const int v = 1 + 2 * (x % 3);
+      x /= 3;
+      sums[t] += v * v;
+      packed[t] |= (uint64_t)v << (8 * i);
+    }
+  }
+  int n = 0;
+  for (int ss = 8; n < 256; ss += 8)  // every sum of squares is 8 + 8a + 24b
+    for (int t = 0; t < 6561 && n < 256; ++t)
+      if (sums[t] == ss) g.v[n++] = packed[t];
+  return g;
+}
+__device__ const Iq2gGrid g_iq2g_grid = make_iq2g_grid();
+// A per-CTA copy in shared memory: the kernels of the grid format fill it
+// at their start (stage_format_tables) and the unpacker reads it there
+// (random 8-byte lookups conflict less in shared-memory banks than they
+// hit distinct L1 lines).
+__shared__ uint64_t s_iq2g_grid[256];
+// and the byte masks of the 128 sign bytes: byte i is 0xFF when element i is
+// negative, the 8th sign (byte 7) set when bits 0-6 hold an odd count
+__shared__ uint64_t s_iq2g_sign[128];
+constexpr int kIq2gSmemBytes = (256 + 128) * 8;
+
+// Every thread of the CTA calls this at the kernel's start (it ends with a barrier).
+template <int FMT>
+__device__ __forceinline__ void stage_format_tables() {
+  if constexpr (FMT == kIQ2G) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) s_iq2g_grid[i] = g_iq2g_grid.v[i];
+    for (int s7 = threadIdx.x; s7 < 128; s7 += blockDim.x) {
+      const uint32_t s8 = (uint32_t)s7 | ((uint32_t)(__popc(s7) & 1) << 7);
+      uint64_t m = 0;
+      for (int i = 0; i < 8; ++i)
+        if ((s8 >> i) & 1) m |= (uint64_t)0xFF << (8 * i);
+      s_iq2g_sign[s7] = m;
+    }
+    __syncthreads();
+  }
+}
 
 // ---- streaming loads of weight bytes (read once: keep them out of L1) ------
 __device__ __forceinline__ uint4 ld_stream128(const void* p) {
@@ -94,7 +149,9 @@ __device__ __forceinline__ void load_sb(const uint8_t* slab, int r, SbRegs<FMT>&
   for (int l = 0; l < F::kLines; ++l) s.code[l] = ld_stream128(slab + F::kCodeOff + 512 * l + 16 * r);
   if constexpr (F::kHdrBytes == 4) s.dm = ld_stream32(slab + 4 * r);
   else s.dm = ld_stream16(slab + 2 * r);
-  if constexpr (F::kSmBytes == 12) {
+  if constexpr (F::kSmBytes == 4) {
+    s.sm[0] = ld_stream32(slab + F::kSmOff + 4 * r);
+  } else if constexpr (F::kSmBytes == 12) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) s.sm[i] = ld_stream32(slab + F::kSmOff + 12 * r + 4 * i);
   } else {
@@ -110,7 +167,9 @@ __device__ __forceinline__ void load_sb_head(const uint8_t* slab, int r, SbRegs<
   using F = Fmt<FMT>;
   if constexpr (F::kHdrBytes == 4) s.dm = *reinterpret_cast<const uint32_t*>(slab + 4 * r);
   else s.dm = *reinterpret_cast<const uint16_t*>(slab + 2 * r);
-  if constexpr (F::kSmBytes == 12) {
+  if constexpr (F::kSmBytes == 4) {
+    s.sm[0] = *reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 4 * r);
+  } else if constexpr (F::kSmBytes == 12) {
 #pragma unroll
     for (int i = 0; i < 3; ++i) s.sm[i] = *reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * r + 4 * i);
   } else {
@@ -142,6 +201,9 @@ __device__ __forceinline__ void sb_scale_min(const SbRegs<FMT>& s, int j, int& s
     uint32_t byte = (s.sm[j >> 2] >> (8 * (j & 3))) & 0xFF;
     sc = (int)(byte & 15);
     mn = (int)(byte >> 4);
+  } else if constexpr (FMT == kIQ2G) {  // nibble j of the scale word: scale 2t + 1, no min
+    sc = 2 * (int)((s.sm[0] >> (4 * j)) & 15) + 1;
+    mn = 0;
   } else {  // Q6_K: int8 scales
     sc = (int)(int8_t)((s.sm[j >> 2] >> (8 * (j & 3))) & 0xFF);
     mn = 32 * sc;
@@ -234,6 +296,24 @@ __device__ __forceinline__ void sub_words(Line line, int j, uint32_t (&w)[Fmt<FM
       const int sh = 4 * (j & 1);
 #pragma unroll
       for (int p = 0; p < 4; ++p) w[p] |= ((hv >> (p + sh)) & 0x01010101u) << 2;
+    }
+  } else if constexpr (FMT == kIQ2G) {
+    // sub-block j = groups 4j..4j+3: their grid indices are word j%4 of line
+    // j/4, their sign bytes word j%4 of line 2 + j/4.  Each group's 8
+    // magnitudes come from the grid; a minus sign negates a byte as
+    // (v ^ 0xFF) - 0xFF, with the byte masks of the sign byte from a table
+    // (the 8th sign makes the count of minus signs even).
+    const uint4 li = line(j >> 2), ls = line(2 + (j >> 2));
+    const int ws = j & 3;
+    const uint32_t iw = ws == 0 ? li.x : ws == 1 ? li.y : ws == 2 ? li.z : li.w;
+    const uint32_t sw = ws == 0 ? ls.x : ws == 1 ? ls.y : ws == 2 ? ls.z : ls.w;
+#pragma unroll
+    for (int gg = 0; gg < 4; ++gg) {
+      const uint64_t v = s_iq2g_grid[(iw >> (8 * gg)) & 0xFF];
+      const uint64_t m = s_iq2g_sign[(sw >> (8 * gg)) & 0x7Fu];
+      const uint32_t mlo = (uint32_t)m, mhi = (uint32_t)(m >> 32);
+      w[2 * gg] = __vsub4((uint32_t)v ^ mlo, mlo);
+      w[2 * gg + 1] = __vsub4((uint32_t)(v >> 32) ^ mhi, mhi);
     }
   } else {  // Q6_K: low nibbles in line j/2 (nibble j%2), high 2 bits in line 8 + j/4 (bits 2(j%4)..)
     const uint4 lo = line(j >> 1), hi = line(8 + (j >> 2));

@@ -61,6 +61,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads, 2) gateup_kernel(FfnArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ __align__(16) uint8_t smem[];
+  stage_format_tables<FMT>();
   __shared__ int s_last;
   const int TT = a.TT;
   const int H = a.H, I = a.I, nbH = H / 256, nRG = I / 32, nIB = I / 256;
@@ -135,6 +136,7 @@ template <int FMT>
 __global__ void __launch_bounds__(kThreads, 2) down_kernel(FfnArgs a) {
   using F = Fmt<FMT>;
   extern __shared__ __align__(16) uint8_t smem[];
+  stage_format_tables<FMT>();
   const int TT = a.TT;
   const int H = a.H, I = a.I, nbI = I / 256, nQuad = H / 128;
   int8_t* s_act = reinterpret_cast<int8_t*>(smem);
@@ -215,6 +217,7 @@ template <int FMT>
 __global__ void debug_dots_kernel(const uint8_t* __restrict__ w, int N, int K, const int8_t* __restrict__ q, int T,
                                   int32_t* __restrict__ isum, int32_t* __restrict__ bsum) {
   using F = Fmt<FMT>;
+  stage_format_tables<FMT>();
   const int nb = K / 256;
   const int rg = blockIdx.x / nb, b = blockIdx.x % nb;
   const int lane = threadIdx.x;
@@ -310,6 +313,7 @@ cudaError_t launch_expert_ffn(const FfnArgs& a, cudaStream_t s) {
     case kQ5K: return launch_ffn_t<kQ5K>(a, s);
     case kQ3K: return launch_ffn_t<kQ3K>(a, s);
     case kQ6K: return launch_ffn_t<kQ6K>(a, s);
+    case kIQ2G: return launch_ffn_t<kIQ2G>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -355,7 +359,8 @@ cudaError_t launch_debug_dots(int fmt, const void* w, int N, int K, const int8_t
     case kQ2K: debug_dots_kernel<kQ2K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
     case kQ5K: debug_dots_kernel<kQ5K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
     case kQ3K: debug_dots_kernel<kQ3K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
-    default: debug_dots_kernel<kQ6K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    case kQ6K: debug_dots_kernel<kQ6K><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
+    default: debug_dots_kernel<kIQ2G><<<blocks, 32, 0, s>>>(wb, N, K, q, T, isum, bsum); break;
   }
   return cudaGetLastError();
 }

@@ -50,8 +50,13 @@ int pick_tile_tokens(int T, int H);
 // ---- launchers (return cudaGetLastError of the launch) ---------------------
 cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q, float* d, int16_t* bs,
                                 cudaStream_t s);
+// status: the workspace status word for the bounded waits of the tensor-core
+// router (nullable: a wait that runs out then only ends the kernel)
 cudaError_t launch_router(const float* x, const float* w, const float* bias, int T, int H, int E,
-                          float* logits, cudaStream_t s);
+                          float* logits, cudaStream_t s, int* status = nullptr);
+// the router GEMM on tcgen05 kind::tf32 (three-term split), H a multiple of 32
+cudaError_t launch_router_tc(const float* x, const float* w, const float* bias, int T, int H, int E,
+                             float* logits, int* status, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int T, int E, int k, int route, int32_t* ids, float* gates,
                         float* gap, cudaStream_t s);
 // single CTA: top-k (optional: logits != nullptr), bucketing, tile plan; T*k <= kSmallPairs
@@ -171,11 +176,13 @@ cudaError_t launch_decode_fused_q2k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused_q5k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused_q3k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_fused_q6k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_fused_iq2g(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_stack_q4k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_stack_q2k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_stack_q5k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_stack_q3k(const DecodeArgs& a, cudaStream_t s);
 cudaError_t launch_decode_stack_q6k(const DecodeArgs& a, cudaStream_t s);
+cudaError_t launch_decode_stack_iq2g(const DecodeArgs& a, cudaStream_t s);
 // largest token count of the single-launch decode path
 constexpr int kDecodeMaxT = 16;
 

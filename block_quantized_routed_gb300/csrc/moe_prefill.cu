@@ -56,9 +56,7 @@
 // (26 warps at 72 registers: the register file is split between the SM's
 // four sub-partitions, so the warp count bounds the registers per thread.)
 // Rings: 3 activation stages and 2 expanded-weight stages of 128 K each
-// (two 128-byte swizzle atoms), 3 raw stages of one super-block column; the
-// producer prefetches the weight rows of the CTA's next item into L2 (the
-// raw ring alone holds less than a DRAM round trip of MMA work).
+// (two 128-byte swizzle atoms), 3 raw stages of one super-block column.
 // A work item is (expert, token tile of <= kTileN bucket rows, weight tile
 // of 128 rows); the items of a launch are laid out by a plan kernel.
 //   gate/up: the 128 rows interleave 64 gate rows and the same 64 up rows
@@ -246,11 +244,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
   asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
-}
-
-// bulk prefetch of global bytes into L2 (16-byte aligned, a multiple of 16 bytes)
-__device__ __forceinline__ void prefetch_l2(const void* p, uint32_t bytes) {
-  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
 }
 
 __device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
@@ -531,18 +524,10 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           }
         }
       };
-      // The raw ring holds three super-block columns, less than a DRAM round
-      // trip of MMA work: the weight rows of the CTA's next item are
-      // prefetched into L2 a whole item ahead, so the ring's loads hit L2.
-      auto prefetch_rows = [&](const uint8_t* const (&src)[4]) {
-#pragma unroll
-        for (int g = 0; g < 4; ++g) prefetch_l2(src[g], (uint32_t)(nb * slab_bytes));
-      };
       for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
         const PItem it = a.items[item];
         const uint8_t* src[4];
         rows_of(it, src);
-        if (item == (int)blockIdx.x) prefetch_rows(src);
         const int nbox = (it.count + kBoxRows - 1) / kBoxRows;
         for (int b = 0; b < nb && ok; ++b) {
           const int rs = ri % kRaw;
@@ -556,12 +541,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           tma_load_2d(b2, &a.map_s, 0, (int)((2 * b) * a.P + it.start), full_raw(rs));
           tma_load_2d(b2 + 2048, &a.map_s, 0, (int)((2 * b + 1) * a.P + it.start), full_raw(rs));
           ++ri;
-          // (after the item's first copies are on their way: the lookups take two L2 round trips)
-          if (b == 0 && item + (int)gridDim.x < n_items) {
-            const uint8_t* nsrc[4];
-            rows_of(a.items[item + gridDim.x], nsrc);
-            prefetch_rows(nsrc);
-          }
           for (int c = 0; c < 256 / kStageK && ok; ++c) {
             if (!(ok = wait_bar(empty_b(bs), pb ^ 1, abort_flag, a.status, w1))) break;
             mbar_expect_tx(full_b(bs), 2 * nbox * kBoxRows * 128);
@@ -1062,6 +1041,203 @@ cudaError_t launch_sums_t(const SumsArgs& a, cudaStream_t s) {
   return launch_gemm_t<FMT, 2>(g, ((a.T + kTileN - 1) / kTileN) * n_wtiles, s);
 }
 
+// ---------------------------------------------------------------- router logits on the tensor cores
+// logits[t, e] = sum_h x[t, h] * W[e, h] (+ bias[e]) for a prefill chunk, on
+// tcgen05 kind::tf32 with the three-term split of each fp32 operand
+// (a = a_hi + a_lo, a_hi = tf32(a) rounded to nearest, a_lo = a - a_hi
+// exactly): a*b ~ a_hi*b_hi + a_hi*b_lo + a_lo*b_hi.  Each product keeps
+// about 21 significant bits and the sums are fp32 in TMEM, an error of the
+// order of fp32's own rounding, far inside the forward-error bound
+// (H + 8) u sum |w x| that the top-k decisions are checked against.
+// (Pulsar README, "What it does today": a softmax or sigmoid router per MoE
+// layer; its logits come from the unquantized activations.)
+//
+// One CTA per 128-token x 256-expert tile, K in stages of 32 fp32 (one
+// 128-byte swizzle atom): warp 0 issues the TMA loads of x and W, warps 2-5
+// split each stage in place (hi) and into a second plane (lo), warp 1
+// issues 3 x 4 MMAs per stage into one 256-column TMEM accumulator, and
+// warps 2-5 write the tile (+ bias) at the end.
+constexpr int kRtM = 128, kRtN = 256, kRtK = 32, kRtStages = 2;
+constexpr int kRtABytes = kRtM * kRtK * 4, kRtBBytes = kRtN * kRtK * 4;  // 16 KB, 32 KB
+constexpr int kRtStageBytes = 2 * (kRtABytes + kRtBBytes);              // raw/hi and lo planes
+constexpr int kRtThreads = 192;
+constexpr int kRtSmBar = kRtStages * kRtStageBytes;
+constexpr int kRtSmAlloc = kRtSmBar + 8 * 8 + 16 + 1024;
+static_assert(kRtSmAlloc <= 232448, "router tile shared memory");
+
+struct RouterTcArgs {
+  CUtensorMap map_x;  // x [T][H] fp32, box {32, 128}, 128-byte swizzle
+  CUtensorMap map_w;  // W [E][H] fp32, box {32, 256}, 128-byte swizzle
+  const float* bias;
+  float* logits;
+  int T, H, E;
+  int* status;
+};
+
+// Instruction descriptor: kind::tf32, A and B tf32 (format 2), D fp32, both K-major.
+__device__ __forceinline__ uint32_t idesc_tf32(int M, int N) {
+  uint32_t d = 0;
+  d |= 1u << 4;   // D format f32
+  d |= 2u << 7;   // A format tf32
+  d |= 2u << 10;  // B format tf32
+  d |= (uint32_t)(N >> 3) << 17;
+  d |= (uint32_t)(M >> 4) << 24;
+  return d;
+}
+__device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64_t bdesc, uint32_t idesc, bool acc) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"((int)acc));
+}
+__device__ __forceinline__ float tf32_rna(float v) {
+  uint32_t r;
+  asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
+  return __uint_as_float(r);
+}
+
+__global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_constant__ RouterTcArgs a) {
+  extern __shared__ uint8_t sm_raw[];
+  uint8_t* sm = sm_raw + ((1024 - (smem_u32(sm_raw) & 1023)) & 1023);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const uint32_t sbase = smem_u32(sm);
+  const uint32_t bar0 = sbase + kRtSmBar;
+  auto full = [&](int s) { return bar0 + 8 * s; };                    // TMA bytes landed
+  auto split = [&](int s) { return bar0 + 8 * (kRtStages + s); };     // hi/lo planes written
+  auto empty = [&](int s) { return bar0 + 8 * (2 * kRtStages + s); }; // MMAs of the stage done
+  const uint32_t done = bar0 + 8 * (3 * kRtStages);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kRtSmBar + 8 * 8);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kRtSmBar + 8 * 8 + 4);
+  // stage s: A hi at 0, B hi at kRtABytes, A lo, B lo after them
+  auto a_hi = [&](int s) { return s * kRtStageBytes; };
+  auto b_hi = [&](int s) { return s * kRtStageBytes + kRtABytes; };
+  auto a_lo = [&](int s) { return s * kRtStageBytes + kRtABytes + kRtBBytes; };
+  auto b_lo = [&](int s) { return s * kRtStageBytes + 2 * kRtABytes + kRtBBytes; };
+  const int m0 = blockIdx.y * kRtM, n0 = blockIdx.x * kRtN;
+  const int nk = a.H / kRtK;
+
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 256;" ::"r"(smem_u32(s_tmem)));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
+  }
+  if (tid == 32) {
+    for (int s = 0; s < kRtStages; ++s) {
+      mbar_init(full(s), 1);
+      mbar_init(split(s), 4);
+      mbar_init(empty(s), 1);
+    }
+    mbar_init(done, 1);
+    *abort_flag = 0;
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *s_tmem;
+  long long w0 = 0, w1 = 0;
+  bool ok = true;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (lane == 0) {
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % kRtStages;
+        const uint32_t ph = (kb / kRtStages) & 1;
+        if (!(ok = wait_bar(empty(s), ph ^ 1, abort_flag, a.status, w0))) break;
+        mbar_expect_tx(full(s), kRtABytes + kRtBBytes);
+        tma_load_2d(sbase + a_hi(s), &a.map_x, kRtK * kb, m0, full(s));
+        tma_load_2d(sbase + b_hi(s), &a.map_w, kRtK * kb, n0, full(s));
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t idesc = idesc_tf32(kRtM, kRtN);
+      for (int kb = 0; kb < nk && ok; ++kb) {
+        const int s = kb % kRtStages;
+        const uint32_t ph = (kb / kRtStages) & 1;
+        if (!(ok = wait_bar(split(s), ph, abort_flag, a.status, w1))) break;
+        tc_fence_after();
+        const uint64_t ah = desc_sw128(sbase + a_hi(s)), bh = desc_sw128(sbase + b_hi(s));
+        const uint64_t al = desc_sw128(sbase + a_lo(s)), bl = desc_sw128(sbase + b_lo(s));
+#pragma unroll
+        for (int k8 = 0; k8 < kRtK / 8; ++k8) {  // K = 8 tf32 = 32 bytes per MMA
+          const uint64_t o = (uint64_t)(2 * k8);
+          mma_tf32(tmem, al + o, bh + o, idesc, kb > 0 || k8 > 0);
+          mma_tf32(tmem, ah + o, bl + o, idesc, true);
+          mma_tf32(tmem, ah + o, bh + o, idesc, true);
+        }
+        mma_commit(empty(s));
+      }
+      if (ok) mma_commit(done);
+    }
+  } else {
+    // ------------------------------------------------ split (warps 2-5), then the epilogue
+    const int ct = tid - 64;  // 0..127
+    for (int kb = 0; kb < nk && ok; ++kb) {
+      const int s = kb % kRtStages;
+      const uint32_t ph = (kb / kRtStages) & 1;
+      if (!(ok = warp_wait(full(s), ph, abort_flag, a.status, w0))) break;
+      // the swizzle permutes 16-byte chunks only, so each chunk splits in place
+      float4* hiA = reinterpret_cast<float4*>(sm + a_hi(s));
+      float4* loA = reinterpret_cast<float4*>(sm + a_lo(s));
+      for (int i = ct; i < (kRtABytes + kRtBBytes) / 16; i += 128) {
+        float4 v = hiA[i];  // A and B hi planes are adjacent, as are the lo planes
+        float4 h, l;
+        h.x = tf32_rna(v.x); l.x = v.x - h.x;
+        h.y = tf32_rna(v.y); l.y = v.y - h.y;
+        h.z = tf32_rna(v.z); l.z = v.z - h.z;
+        h.w = tf32_rna(v.w); l.w = v.w - h.w;
+        hiA[i] = h;
+        loA[i] = l;
+      }
+      fence_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(split(s));
+    }
+    if (ok) ok = warp_wait(done, 0, abort_flag, a.status, w1, 128);
+    if (ok) {
+      tc_fence_after();
+      const int qd = warp & 3;  // TMEM lanes 32 qd .. 32 qd + 31
+      const int t = m0 + 32 * qd + lane;
+      const uint32_t tl = tmem + ((uint32_t)(32 * qd) << 16);
+      for (int c0 = 0; c0 < kRtN; c0 += 8) {
+        if (n0 + c0 >= a.E) break;  // warp-uniform
+        float v[8];
+        tmem_ld8(tl + c0, v);
+        tmem_wait_ld();
+        if (t < a.T) {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int e = n0 + c0 + j;
+            if (e < a.E) a.logits[(int64_t)t * a.E + e] = v[j] + (a.bias ? __ldg(a.bias + e) : 0.0f);
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, 256;" ::"r"(tmem));
+  }
+}
+
+// 2-D fp32 tensor map: `inner` elements per row, `rows` rows, box {box_inner, box_rows}, 128-byte swizzle
+bool make_map_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
+                  uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t dims[2] = {inner, rows};
+  const cuuint64_t strides[1] = {inner * 4};
+  const cuuint32_t box[2] = {box_inner, box_rows};
+  const cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace
 
 SumsPlan sums_plan(int N, int K, int T) {
@@ -1097,6 +1273,32 @@ int prefill_tile_tokens() { return kTileN; }
 size_t prefill_item_capacity(int64_t P, int E, int S, int H, int I) {
   const int64_t EpS = E + S;
   return (size_t)(P / kTileN + EpS) * (size_t)std::max(I / 64, H / 128);
+}
+
+cudaError_t launch_router_tc(const float* x, const float* w, const float* bias, int T, int H, int E,
+                             float* logits, int* status, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (H % kRtK) return cudaErrorInvalidValue;
+  RouterTcArgs a{};
+  if (!make_map_f32(&a.map_x, x, (uint64_t)H, (uint64_t)T, kRtK, kRtM) ||
+      !make_map_f32(&a.map_w, w, (uint64_t)H, (uint64_t)E, kRtK, kRtN))
+    return cudaErrorInvalidValue;
+  a.bias = bias;
+  a.logits = logits;
+  a.T = T;
+  a.H = H;
+  a.E = E;
+  a.status = status;
+  static bool opted = false;
+  if (!opted) {
+    cudaError_t err = cudaFuncSetAttribute(router_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kRtSmAlloc);
+    if (err != cudaSuccess) return err;
+    opted = true;
+  }
+  const dim3 grid((E + kRtN - 1) / kRtN, (T + kRtM - 1) / kRtM);
+  note_launch();
+  router_tc_kernel<<<grid, kRtThreads, kRtSmAlloc, s>>>(a);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s) {

@@ -80,8 +80,10 @@ __global__ void __launch_bounds__(128) router_kernel(const float* __restrict__ x
 // (rows ty*4 + {0..3} and 64 + ty*4 + {0..3}, columns likewise): every thread
 // reads float4 pairs from shared memory per k and issues 64 FMAs.
 constexpr int kRgTile = 128, kRgK = 16, kRgPad = 4;
-// token count from which the tiled GEMM replaces the per-expert GEMV
+// token count from which the tiled GEMM replaces the per-expert GEMV, and
+// from which the tensor-core GEMM (128-token tiles) replaces both
 constexpr int kRouterGemmMinT = 64;
+constexpr int kRouterTcMinT = 128;
 
 __global__ void __launch_bounds__(256) router_gemm_kernel(const float* __restrict__ x, const float* __restrict__ w,
                                                           const float* __restrict__ bias, int T, int H, int E,
@@ -348,8 +350,9 @@ cudaError_t launch_q8k_quantize(const float* x, int64_t T, int64_t K, int8_t* q,
 }
 
 cudaError_t launch_router(const float* x, const float* w, const float* bias, int T, int H, int E, float* logits,
-                          cudaStream_t s) {
+                          cudaStream_t s, int* status) {
   if (T == 0) return cudaSuccess;
+  if (T >= kRouterTcMinT && H % 32 == 0) return launch_router_tc(x, w, bias, T, H, E, logits, status, s);
   if (T >= kRouterGemmMinT) {
     const dim3 grid((E + kRgTile - 1) / kRgTile, (T + kRgTile - 1) / kRgTile);
     note_launch();

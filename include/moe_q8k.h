@@ -38,9 +38,16 @@
  *     u_j; weight = d*(u_j - 32)*(q - 4).
  *   Q6_K-style: 210 bytes, 6-bit codes, sixteen sub-blocks with int8 scales;
  *     weight = d*scale_j*(q - 32).
+ *   IQ2-style grid format: 70 bytes (2.19 bits per weight); per group of 8
+ *     weights a grid index u and 7 sign bits (the 8th sign makes the minus
+ *     signs even), per 32 weights a 4-bit scale t; weight = d*(2t+1)*sign*
+ *     C[u][i], C the 256 vectors of {1,3,5}^8 with the smallest sums of
+ *     squares (equal sums in increasing base-3 order, element 0 first).
  * (Pulsar README, "What it does today": Q4_K/Q6_K matmuls on q8_K
- * activations; "Get a model": q3_K/q5_K/q6_K tensors; the "-style" layouts
- * are this library's own.)  Every matrix pointer must be 16-byte aligned.
+ * activations, IQ2_XXS builds; "Get a model": q3_K/q5_K/q6_K tensors;
+ * Strata engine article, finding 7: i-quant codebook lookups cost decode
+ * compute.  The "-style" layouts and the grid are this library's own.)
+ * Every matrix pointer must be 16-byte aligned.
  */
 #ifndef MOE_Q8K_H
 #define MOE_Q8K_H
@@ -72,7 +79,8 @@ typedef enum {
   MOE_FMT_Q2K = 1, /* Q2_K-style: 84 B                                             */
   MOE_FMT_Q5K = 2, /* Q5_K-style: 176 B (Q4_K-style with 5-bit codes)             */
   MOE_FMT_Q3K = 3, /* Q3_K-style: 110 B, 3-bit codes, signed 6-bit scales, no min  */
-  MOE_FMT_Q6K = 4  /* Q6_K-style: 210 B, 6-bit codes, int8 scales, no min          */
+  MOE_FMT_Q6K = 4, /* Q6_K-style: 210 B, 6-bit codes, int8 scales, no min          */
+  MOE_FMT_IQ2G = 5 /* IQ2-style grid format: 70 B, grid indices and signs          */
 } moe_wfmt;
 typedef enum { MOE_ROUTE_SOFTMAX = 0, MOE_ROUTE_SIGMOID = 1 } moe_route_kind;
 

@@ -35,20 +35,23 @@ def to_dev(a, torch, device="cuda"):
     return torch.from_numpy(np.ascontiguousarray(a)).to(device)
 
 
-def routing_ok(gpu_ids, oracle_ids, gap, logits=None):
+def routing_ok(gpu_ids, oracle_ids, gap, logits=None, tie=None):
     """ids must match the oracle's except at near-ties: tokens whose oracle
-    gap l_(k) - l_(k+1) is below NEAR_TIE may select a different set, and
-    tokens whose selected logits hold two within NEAR_TIE of each other may
-    order them differently.  Returns the number of such near-tie tokens whose
-    ids differ (reported, not failed)."""
+    gap l_(k) - l_(k+1) is below the tie threshold may select a different
+    set, and tokens whose selected logits hold two within it of each other
+    may order them differently.  The threshold is NEAR_TIE, or per token
+    `tie` (the parity rule's max(NEAR_TIE, twice the device's logit error)).
+    Returns the number of such near-tie tokens whose ids differ (reported,
+    not failed)."""
     gpu_ids = np.asarray(gpu_ids)
     oracle_ids = np.asarray(oracle_ids)
+    tie = np.full(len(gpu_ids), NEAR_TIE) if tie is None else np.asarray(tie)
     mism = (gpu_ids != oracle_ids).any(axis=1)
-    allowed = np.asarray(gap) < NEAR_TIE
+    allowed = np.asarray(gap) < tie
     if logits is not None:
         sel = np.take_along_axis(np.asarray(logits), oracle_ids, axis=1)
         same_set = (np.sort(gpu_ids, axis=1) == np.sort(oracle_ids, axis=1)).all(axis=1)
-        inner = np.abs(np.diff(sel, axis=1)).min(axis=1) < NEAR_TIE if sel.shape[1] > 1 else np.zeros(len(sel), bool)
+        inner = np.abs(np.diff(sel, axis=1)).min(axis=1) < tie if sel.shape[1] > 1 else np.zeros(len(sel), bool)
         allowed |= same_set & inner
     hard = mism & ~allowed
     if hard.any():

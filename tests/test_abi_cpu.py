@@ -39,7 +39,7 @@ def test_status_strings(lib):
 
 
 @pytest.mark.parametrize("bad", [dict(H=500), dict(I=0), dict(E=0), dict(E=2000), dict(top_k=0), dict(top_k=17),
-                                 dict(E=4, top_k=5), dict(n_shared=3), dict(route=2), dict(fmt=5), dict(T_max=0),
+                                 dict(E=4, top_k=5), dict(n_shared=3), dict(route=2), dict(fmt=6), dict(T_max=0),
                                  dict(H=16640)])
 def test_invalid_descriptors(lib, bad):
     d = desc(**bad)

@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FORMATS, N_SUB
+from synth.layout import FMT_Q4K, FMT_Q2K, FMT_Q5K, FMT_Q3K, FMT_Q6K, FMT_IQ2G, FORMATS, N_SUB
 from tests import fieldpack
 from oracle import parity
 from tests.gpu_util import assert_close_rows, routing_ok, to_dev
@@ -107,6 +107,31 @@ def test_subblock_dots_extreme_fields(moe, fmt):
     np.testing.assert_array_equal(isum.cpu().numpy(), np.broadcast_to(want, isum.shape))
 
 
+def test_subblock_dots_iq2g_extreme_groups(moe):
+    """IQ2-style grid format: the group of largest magnitude sum (the last grid entry, every sign
+    positive) and the all-ones group with seven minus signs (the 8th sign then makes it eight),
+    against q_a = -127 and +127: the integer sums equal the hand-computable 4 * (sum of the group)
+    * q_a per 32-weight sub-block, bit for bit."""
+    fmt, N, K = FMT_IQ2G, 256, 512
+    grid = oracle.iq2g_grid()
+    top = grid[255].astype(np.int64)
+    neg_ones = -np.ones(8, np.int64)
+    q = np.empty((N, 2, 256), np.int64)
+    q[:, 0] = np.tile(top, 32)
+    q[:, 1] = np.tile(neg_ones, 32)
+    sc = np.full((N, 2, 8), 31)
+    w = fieldpack.pack_fields(fmt, N, K, q, sc, np.zeros((N, 2, 8)), np.ones((N, 2), np.float16),
+                              np.zeros((N, 2), np.float16))
+    xq = np.stack([np.full(K, -127, np.int8), np.full(K, 127, np.int8)])
+    isum = torch.empty((2, N, 2, 8), dtype=torch.int32, device="cuda")
+    bsum = torch.empty((2, 2, 8), dtype=torch.int32, device="cuda")
+    moe.moe_debug_subblock_dots(fmt, dev(w), N, K, dev(xq), isum, bsum)
+    got = isum.cpu().numpy()
+    for t, qa in enumerate((-127, 127)):
+        assert (got[t, :, 0] == 4 * int(top.sum()) * qa).all()
+        assert (got[t, :, 1] == 4 * -8 * qa).all()
+
+
 def test_subblock_dots_extreme_codes(moe):
     """q_w = 15 with scale 63 against q_a = -127 everywhere: the largest sums."""
     fmt, N, K = FMT_Q4K, 256, 512
@@ -138,11 +163,24 @@ def test_route_topk(moe, route, T, H, E, k, bias):
     gap = torch.empty((T,), dtype=torch.float32, device="cuda")
     moe.moe_route_topk(dev(x), dev(wr), None if b is None else dev(b), k, route, logits, ids, gates, gap)
     rl, rids, rg, rgap = oracle.route(x, wr, b, k, route)
-    np.testing.assert_allclose(logits.cpu().numpy(), rl, rtol=0, atol=1e-4 * np.abs(rl).max())
-    routing_ok(ids.cpu().numpy(), rids, rgap, rl)
-    # gates against the oracle's gates for the GPU's ids
-    _, _, rg2, _ = oracle.route(x, wr, b, k, route, forced_ids=ids.cpu().numpy())
-    np.testing.assert_allclose(gates.cpu().numpy(), rg2, rtol=1e-5, atol=1e-6)
+    # logits within the fp32 forward-error bound of a length-H dot product (any order), and within
+    # 1e-4 of the largest logit
+    l = logits.cpu().numpy().astype(np.float64)
+    lbound = (H + 8) * parity.U32 * (np.abs(x.astype(np.float64)) @ np.abs(wr.astype(np.float64)).T)
+    if b is not None:
+        lbound += parity.U32 * np.abs(b.astype(np.float64))[None, :]
+    lerr = np.abs(l - rl)
+    assert (lerr <= lbound).all(), f"logit error {lerr.max():.3e} above its bound"
+    np.testing.assert_allclose(l, rl, rtol=0, atol=1e-4 * np.abs(rl).max())
+    gids = ids.cpu().numpy()
+    routing_ok(gids, rids, rgap, rl, tie=np.maximum(parity.NEAR_TIE, 2 * lerr.max(axis=1)))
+    # gates against the oracle's gates for the GPU's ids: the first-order change of a renormalised gate
+    # under the device's own logit errors, plus the rounding of its exp and division (the parity rule)
+    _, _, rg2, _ = oracle.route(x, wr, b, k, route, forced_ids=gids)
+    dl = np.take_along_axis(lerr, gids, axis=1).max(axis=1, keepdims=True)
+    gtol = np.abs(rg2) * (2 * dl + 16 * parity.U32) + parity.GATE_ATOL
+    gd = gates.cpu().numpy().astype(np.float64)
+    assert (np.abs(gd - rg2) <= gtol).all(), f"gate error {np.abs(gd - rg2).max():.3e}"
     g = gap.cpu().numpy()
     fin = np.isfinite(rgap)
     np.testing.assert_allclose(g[fin], rgap[fin], rtol=0, atol=1e-4)
@@ -261,6 +299,11 @@ CASES = [
     (FMT_Q3K, 0, 512, 256, 8, 2, 1, 512, False),     # tensor-core prefill
     (FMT_Q5K, 0, 512, 256, 8, 2, 1, 512, False),     # a prefill-size chunk on the GEMV path
     (FMT_Q6K, 1, 768, 512, 16, 4, 0, 300, True),
+    # the IQ2-style grid format: decode (single launch), the GEMV path, a prefill-size chunk
+    (FMT_IQ2G, 0, 2048, 512, 64, 8, 1, 1, False),
+    (FMT_IQ2G, 1, 1024, 512, 64, 10, 1, 4, False),
+    (FMT_IQ2G, 1, 512, 256, 40, 10, 1, 40, False),
+    (FMT_IQ2G, 0, 512, 256, 8, 2, 1, 512, False),
 ]
 
 

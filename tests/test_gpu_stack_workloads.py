@@ -113,10 +113,11 @@ def check_stack_layer(moe, wl, run, l):
     return metrics
 
 
-@pytest.mark.parametrize("fmt", [synth.FMT_Q5K, synth.FMT_Q3K, synth.FMT_Q6K], ids=["q5k", "q3k", "q6k"])
+@pytest.mark.parametrize("fmt", [synth.FMT_Q5K, synth.FMT_Q3K, synth.FMT_Q6K, synth.FMT_IQ2G],
+                         ids=["q5k", "q3k", "q6k", "iq2g"])
 def test_decode_stack_other_formats(moe, fmt):
     """The decode workload's shape (40 layers, H 2048, 256 experts top-8 + shared, I 512, 1 token) with
-    Q5_K/Q3_K/Q6_K-style weights made on the device, as one moe_stack_forward."""
+    Q5_K/Q3_K/Q6_K-style or IQ2-style grid weights made on the device, as one moe_stack_forward."""
     import dataclasses
 
     import synth.gpu

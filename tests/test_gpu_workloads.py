@@ -107,7 +107,7 @@ def test_device_generator_matches_host_generator(moe):
     import synth.gpu
     base = WORKLOADS["decode_h2048_e256k8s1_i512_q4k_l40_t1"]
     for wl in [base, WORKLOADS["verify_h4096_e512k10s1_i1024_q2k_l48_t4"]] + \
-            [dataclasses.replace(base, fmt=f) for f in (synth.FMT_Q5K, synth.FMT_Q3K, synth.FMT_Q6K)]:
+            [dataclasses.replace(base, fmt=f) for f in (synth.FMT_Q5K, synth.FMT_Q3K, synth.FMT_Q6K, synth.FMT_IQ2G)]:
         bank = synth.gpu.ExpertBank(wl.fmt, wl.H, wl.I, 3, 2, wl.seed)
         for layer, e, m in [(0, 0, 0), (1, 2, 1), (1, 1, 2)]:
             want = _host_experts(wl, layer, [e])[e][m]
