@@ -195,7 +195,9 @@ constexpr int kPrefillMinTokensPerExpert = 16;
 // below 2^24 (Q4_K/Q2_K/Q3_K-style).  The Q5_K-style (63 * 31 * 127 * 128
 // > 2^24 per half) and Q6_K-style (|127 * 63| > 2048) formats run their
 // large batches on the dp4a GEMV kernels.
-inline bool prefill_format(int fmt) { return fmt == MOE_FMT_Q4K || fmt == MOE_FMT_Q2K || fmt == MOE_FMT_Q3K; }
+inline bool prefill_format(int fmt) {
+  return fmt == MOE_FMT_Q4K || fmt == MOE_FMT_Q2K || fmt == MOE_FMT_Q3K || fmt == MOE_FMT_IQ2G;
+}
 inline bool prefill_path(int64_t T, int k, int E, int fmt) {
   return prefill_format(fmt) && T * k > kSmallPairs && T * k >= (int64_t)kPrefillMinTokensPerExpert * E;
 }

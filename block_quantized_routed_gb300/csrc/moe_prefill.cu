@@ -36,9 +36,11 @@
 // does today"; Strata, 0.1.13 prefill notes: grouped int8 tensor-core expert
 // GEMM that unpacks super-blocks to shared memory and rescales per block).
 // tcgen05 offers no int8 kind on sm_103a, hence exact-integer fp16.  The
-// Q4_K, Q2_K and Q3_K-style formats run here; for the Q3_K-style format
-// (weight = d * sc * (q - 4), sc = u - 32) A = sc * q and the min term
-// carries 4 * sc with scale d.  (Q5_K-style products reach 63 * 31 per
+// Q4_K, Q2_K and Q3_K-style formats and the IQ2-style grid format run here;
+// for the Q3_K-style format (weight = d * sc * (q - 4), sc = u - 32) A =
+// sc * q and the min term carries 4 * sc with scale d; for the grid format
+// A = (2t + 1) * sign * C[u][i] (|A| <= 155, from fp16 tables of the grid
+// and of the sign masks in shared memory) and the min term is zero.  (Q5_K-style products reach 63 * 31 per
 // weight and 3.2e7 per half super-block, Q6_K-style 127 * 63 per weight:
 // beyond the exact range, so those formats take the dp4a GEMV kernels.)
 //
@@ -316,6 +318,31 @@ __device__ __forceinline__ uint4 scaled8(uint32_t w0, uint32_t w1, __half2 sc2, 
   return o;
 }
 
+// IQ2-style grid format in the expanders: each grid entry as 8 fp16
+// magnitudes, and for each 7-bit sign byte the mask that flips the fp16
+// sign bit of the negative elements (the 8th sign from the parity of the
+// seven).  Filled at the kernel's start; only the grid-format kernels use it.
+__shared__ uint4 s_iq2g_half[256 + 128];
+
+__device__ __forceinline__ void stage_iq2g_half_tables() {
+  for (int i = threadIdx.x; i < 256 + 128; i += blockDim.x) {
+    uint32_t h[4];
+    if (i < 256) {
+      const uint64_t v = g_iq2g_grid.v[i];
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        h[p] = pack_h2((float)((v >> (16 * p)) & 0xFF), (float)((v >> (16 * p + 8)) & 0xFF));
+    } else {
+      const uint32_t s7 = (uint32_t)(i - 256);
+      const uint32_t s8 = s7 | ((uint32_t)(__popc(s7) & 1) << 7);
+#pragma unroll
+      for (int p = 0; p < 4; ++p)
+        h[p] = (((s8 >> (2 * p)) & 1) ? 0x8000u : 0u) | (((s8 >> (2 * p + 1)) & 1) ? 0x80000000u : 0u);
+    }
+    s_iq2g_half[i] = make_uint4(h[0], h[1], h[2], h[3]);
+  }
+}
+
 // ---------------------------------------------------------------- planning
 // One CTA: per expert with tokens and a present gate pointer, its token tiles
 // (ceil(c/kTileN) tiles of balanced size) x weight tiles, expert by expert.
@@ -468,6 +495,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kSmMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmMisc + 4);
 
+  if constexpr (FMT == kIQ2G) stage_iq2g_half_tables();  // read after the barrier below
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], 512;" ::"r"(smem_u32(s_tmem)));
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
@@ -575,7 +603,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         uint8_t* a2 = sm + kSmA2 + rs * 4096;
         // scales and mins, extracted on demand (no per-thread arrays)
         uint64_t sm_lo, sm_hi;
-        if constexpr (FMT == kQ4K || FMT == kQ3K) {
+        if constexpr (FMT == kIQ2G) {
+          // nibble j = t_j (scale 2 t_j + 1); no min
+          sm_lo = *reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 4 * lr);
+          sm_hi = 0;
+        } else if constexpr (FMT == kQ4K || FMT == kQ3K) {
           // 96-bit string of 6-bit fields: field f = bits 6f.. (Q4_K: scale j = f j,
           // min j = f 8 + j; Q3_K: u_j = f j, scale u_j - 32); sm_hi = bits 48..
           const uint32_t* smw = reinterpret_cast<const uint32_t*>(slab + F::kSmOff + 12 * lr);
@@ -588,13 +620,15 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           sm_hi = (uint64_t)v.z | ((uint64_t)v.w << 32);
         }
         auto scale_of = [&](int j) -> int {
-          if constexpr (FMT == kQ4K) return (int)((sm_lo >> (6 * j)) & 63);
+          if constexpr (FMT == kIQ2G) return 2 * (int)((sm_lo >> (4 * j)) & 15) + 1;
+          else if constexpr (FMT == kQ4K) return (int)((sm_lo >> (6 * j)) & 63);
           else if constexpr (FMT == kQ3K) return (int)(((j < 8 ? sm_lo >> (6 * j) : sm_hi >> (6 * (j - 8)))) & 63) - 32;
           else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7))) & 15);
         };
         // the min-term coefficient: the min, or o * scale (Q3_K-style, o = 4)
         auto min_of = [&](int j) -> int {
-          if constexpr (FMT == kQ4K) return (int)((sm_hi >> (6 * j)) & 63);
+          if constexpr (FMT == kIQ2G) return j < 0;  // no min
+          else if constexpr (FMT == kQ4K) return (int)((sm_hi >> (6 * j)) & 63);
           else if constexpr (FMT == kQ3K) return 4 * scale_of(j);
           else return (int)(((j < 8 ? sm_lo : sm_hi) >> (8 * (j & 7) + 4)) & 15);
         };
@@ -615,7 +649,34 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         for (int c = 0; c < 256 / kStageK; ++c) {
           if (!(ok = warp_wait(empty_a(as), pa ^ 1, abort_flag, a.status, w1))) break;
           uint8_t* A = sm + kSmA + as * kAStage;
-          if constexpr (FMT == kQ4K) {
+          if constexpr (FMT == kIQ2G) {
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const int j = 4 * c + 2 * hx + jj;  // sub-block of 32 weights = groups 4j .. 4j + 3
+              const uint4 li = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * (j >> 2) + 16 * lr);
+              const uint4 ls = *reinterpret_cast<const uint4*>(slab + F::kCodeOff + 512 * (2 + (j >> 2)) + 16 * lr);
+              const int ws = j & 3;
+              const uint32_t iw = ws == 0 ? li.x : ws == 1 ? li.y : ws == 2 ? li.z : li.w;
+              const uint32_t sw = ws == 0 ? ls.x : ws == 1 ? ls.y : ws == 2 ? ls.z : ls.w;
+              const __half2 sc2 = __float2half2_rn((float)scale_of(j));
+              const int k0 = 64 * hx + 32 * jj;
+#pragma unroll
+              for (int gg = 0; gg < 4; ++gg) {
+                // 8 weights: the grid magnitudes with their signs flipped, times the scale (exact: |.| <= 155)
+                const uint4 mag = s_iq2g_half[(iw >> (8 * gg)) & 0xFF];
+                const uint4 neg = s_iq2g_half[256 + ((sw >> (8 * gg)) & 0x7F)];
+                const uint32_t hv[4] = {mag.x ^ neg.x, mag.y ^ neg.y, mag.z ^ neg.z, mag.w ^ neg.w};
+                uint4 o;
+                uint32_t* op = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                  const __half2 prod = __hmul2(*reinterpret_cast<const __half2*>(&hv[p]), sc2);
+                  op[p] = *reinterpret_cast<const uint32_t*>(&prod);
+                }
+                *reinterpret_cast<uint4*>(A + sw128_off(r, k0 + 8 * gg)) = o;
+              }
+            }
+          } else if constexpr (FMT == kQ4K) {
 #pragma unroll
             for (int jj = 0; jj < 2; ++jj) {
               const int j = 4 * c + 2 * hx + jj;  // sub-block of 32 codes
@@ -1264,6 +1325,7 @@ cudaError_t launch_prefill_sums(const SumsArgs& a, cudaStream_t s) {
     case kQ4K: return launch_sums_t<kQ4K>(a, s);
     case kQ2K: return launch_sums_t<kQ2K>(a, s);
     case kQ3K: return launch_sums_t<kQ3K>(a, s);
+    case kIQ2G: return launch_sums_t<kIQ2G>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }
@@ -1306,6 +1368,7 @@ cudaError_t launch_prefill_ffn(const PrefillArgs& a, cudaStream_t s) {
     case kQ4K: return launch_prefill_fmt<kQ4K>(a, s);
     case kQ2K: return launch_prefill_fmt<kQ2K>(a, s);
     case kQ3K: return launch_prefill_fmt<kQ3K>(a, s);
+    case kIQ2G: return launch_prefill_fmt<kIQ2G>(a, s);
     default: return cudaErrorInvalidValue;
   }
 }

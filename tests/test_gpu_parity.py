@@ -552,7 +552,8 @@ def test_bounded_wait_runs_out_and_reports(moe):
 # ------------------------------------------------------- tensor-core integer sums
 
 @pytest.mark.parametrize("fmt,N,K,T", [(FMT_Q4K, 256, 512, 200), (FMT_Q2K, 256, 768, 130), (FMT_Q4K, 512, 256, 16),
-                                       (FMT_Q2K, 256, 256, 1), (FMT_Q3K, 256, 512, 200), (FMT_Q3K, 512, 256, 3)])
+                                       (FMT_Q2K, 256, 256, 1), (FMT_Q3K, 256, 512, 200), (FMT_Q3K, 512, 256, 3),
+                                       (FMT_IQ2G, 256, 512, 200), (FMT_IQ2G, 512, 256, 3)])
 def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     """S = sum_j sc_j isum_j and M = sum_j mn_j bsum_j of every (token, row, super-block), as the tcgen05
     GEMM forms them in TMEM, equal the oracle's int64 sums bit for bit.  Rows 0-31 carry an all-extreme
@@ -562,7 +563,11 @@ def test_prefill_integer_sums_bit_exact(moe, fmt, N, K, T):
     assert 130 > moe.moe_prefill_tile_tokens() >= 32
     rng = np.random.default_rng(N + K + T + fmt)
     q, sc, mn, d, dmin = fieldpack.random_fields(fmt, N, K, rng)
-    q[:32, 0] = fieldpack.QMAX[fmt]
+    if fmt == FMT_IQ2G:  # the grid entry of largest magnitude sum, all signs +, the largest scale
+        grid = oracle.iq2g_grid()
+        q[:32, 0] = np.tile(grid[np.argmax(grid.sum(axis=1))], 32)
+    else:
+        q[:32, 0] = fieldpack.QMAX[fmt]
     sc[:32, 0] = fieldpack.SCALE_RANGE[fmt][0] if fmt == FMT_Q3K else fieldpack.SCALE_RANGE[fmt][1]
     mn[:32, 0] = fieldpack.MIN_RANGE[fmt][1]
     w = fieldpack.pack_fields(fmt, N, K, q, sc, mn, d, dmin)
