@@ -120,7 +120,7 @@ constexpr int kSmA2 = kSmRaw + kRaw * kRawBytes;     // mins tile [128 rows][16]
 constexpr int kSmB2 = kSmA2 + kRaw * 4096;           // code-sum tile [128 tokens][16] per raw stage
 constexpr int kSmDa = kSmB2 + kRaw * 4096;           // per epilogue warp: the block scales of its 32 tokens
 constexpr int kSmBar = kSmDa + kEpiWarps * 32 * 4;
-constexpr int kNumBars = 2 * kStagesA + 2 * kStagesB + 2 * kRaw + 4;
+constexpr int kNumBars = kStagesA + 2 * kStagesB + 2 * kRaw + 4;
 constexpr int kSmMisc = kSmBar + 8 * 32;
 constexpr int kSmUsed = kSmMisc + 16;
 constexpr int kSmAlloc = kSmUsed + 1024;             // slack for aligning the base
@@ -483,15 +483,17 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   const int N_out = MODE == 0 ? a.I : MODE == 1 ? a.H : a.dbg_n;
   const uint32_t sbase = smem_u32(sm);
   const uint32_t bar0 = sbase + kSmBar;
-  // barrier slots: full_a, empty_a, full_b, empty_b, full_raw, empty_raw, tfull, tempty
+  // barrier slots: full_a, full_b, empty_b, full_raw, empty_raw, tfull, tempty.
+  // A weight slot has no barrier of its own: the MMAs of stage m read weight
+  // slot m % kStagesA and activation slot m % kStagesB and commit once, to
+  // empty_b, which the expanders wait on too.
   auto full_a = [&](int s) { return bar0 + 8 * s; };
-  auto empty_a = [&](int s) { return bar0 + 8 * (kStagesA + s); };
-  auto full_b = [&](int s) { return bar0 + 8 * (2 * kStagesA + s); };
-  auto empty_b = [&](int s) { return bar0 + 8 * (2 * kStagesA + kStagesB + s); };
-  auto full_raw = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + s); };
-  auto empty_raw = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + kRaw + s); };
-  auto tfull = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + 2 * kRaw + s); };
-  auto tempty = [&](int s) { return bar0 + 8 * (2 * kStagesA + 2 * kStagesB + 2 * kRaw + 2 + s); };
+  auto full_b = [&](int s) { return bar0 + 8 * (kStagesA + s); };
+  auto empty_b = [&](int s) { return bar0 + 8 * (kStagesA + kStagesB + s); };
+  auto full_raw = [&](int s) { return bar0 + 8 * (kStagesA + 2 * kStagesB + s); };
+  auto empty_raw = [&](int s) { return bar0 + 8 * (kStagesA + 2 * kStagesB + kRaw + s); };
+  auto tfull = [&](int s) { return bar0 + 8 * (kStagesA + 2 * kStagesB + 2 * kRaw + s); };
+  auto tempty = [&](int s) { return bar0 + 8 * (kStagesA + 2 * kStagesB + 2 * kRaw + 2 + s); };
   uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kSmMisc);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kSmMisc + 4);
 
@@ -501,10 +503,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;");
   }
   if (tid == 32) {
-    for (int s = 0; s < kStagesA; ++s) {
-      mbar_init(full_a(s), kExpWarps);
-      mbar_init(empty_a(s), 1);
-    }
+    for (int s = 0; s < kStagesA; ++s) mbar_init(full_a(s), kExpWarps);
     for (int s = 0; s < kStagesB; ++s) {
       mbar_init(full_b(s), 1);
       mbar_init(empty_b(s), 1);
@@ -593,7 +592,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
     const int lr = MODE == 0 ? ((r >> 1) & 31) : (r & 31);         // row inside the slab
     uint32_t ri = 0;
     int as = 0;
-    uint32_t pa = 0;
+    uint32_t ka = 0;  // stages written so far
     bool ok = true;
     for (int item = blockIdx.x; item < n_items && ok; item += gridDim.x) {
       for (int b = 0; b < nb && ok; ++b) {
@@ -647,7 +646,14 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
         }
 #pragma unroll
         for (int c = 0; c < 256 / kStageK; ++c) {
-          if (!(ok = warp_wait(empty_a(as), pa ^ 1, abort_flag, a.status, w1))) break;
+          // slot `as` was last read by the MMAs of stage ka - kStagesA: wait for
+          // that stage's commit on its activation slot's barrier (stage m
+          // completes phase m / kStagesB of empty_b(m % kStagesB))
+          if (ka >= (uint32_t)kStagesA) {
+            const uint32_t m = ka - kStagesA;
+            if (!(ok = warp_wait(empty_b(m % kStagesB), (m / kStagesB) & 1, abort_flag, a.status, w1))) break;
+          }
+          ++ka;
           uint8_t* A = sm + kSmA + as * kAStage;
           if constexpr (FMT == kIQ2G) {
 #pragma unroll
@@ -719,7 +725,7 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
           fence_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(full_a(as));
-          if (++as == kStagesA) { as = 0; pa ^= 1; }
+          if (++as == kStagesA) as = 0;
         }
         if (!ok) break;
         __syncwarp();
@@ -730,9 +736,11 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
   } else if (warp == kWarpMma) {
     // ------------------------------------------------------------ MMA issuer
     // Per super-block: stage 0 (8 MMAs into S0, one commit group), stage 1
-    // (8 MMAs into S1, then the min MMA into M, one commit group).  The first
-    // commit after a run of MMAs costs the issuing thread a few hundred
-    // cycles, so commits are grouped behind as much MMA work as possible.
+    // (8 MMAs into S1, then the min MMA into M, one commit group).  A commit
+    // costs the issuing thread a few hundred cycles, so each stage commits
+    // once for its slots (empty_b: the expanders read the weight slot's
+    // release from it too), plus once per super-block for the raw stage and
+    // the epilogue.
     if (lane == 0) {
       const uint64_t dA0 = desc_sw128(sbase + kSmA), dB0 = desc_sw128(sbase + kSmB);
       const uint64_t dA2 = desc_plain(sbase + kSmA2, 128, 256), dB2 = desc_plain(sbase + kSmB2, 2048, 128);
@@ -779,7 +787,6 @@ __global__ void __launch_bounds__(kPThreads, 1) prefill_gemm_kernel(const __grid
               mma_f16(tmem + tmem_slot(3 * tb + 2), dA2 + (uint64_t)((rs * 4096) >> 4),
                       dB2 + (uint64_t)((rs * 4096) >> 4), idesc, false);
             }
-            mma_commit(empty_a(as));
             mma_commit(empty_b(bs));
             if (last) {
               mma_commit(empty_raw(rs));
