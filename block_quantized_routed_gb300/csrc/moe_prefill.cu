@@ -1120,22 +1120,24 @@ cudaError_t launch_sums_t(const SumsArgs& a, cudaStream_t s) {
 // (Pulsar README, "What it does today": a softmax or sigmoid router per MoE
 // layer; its logits come from the unquantized activations.)
 //
-// One CTA per 128-token x 256-expert tile, K in stages of 32 fp32 (one
-// 128-byte swizzle atom): warp 0 issues the TMA loads of x and W, warps 2-5
+// One CTA per 128-token x 256-expert tile, K in a ring of four stages of
+// 16 fp32 (64-byte rows, 64-byte swizzle): warp 0 issues the TMA loads of x
+// and W, warps 2-5
 // split each stage in place (hi) and into a second plane (lo), warp 1
 // issues 3 x 4 MMAs per stage into one 256-column TMEM accumulator, and
 // warps 2-5 write the tile (+ bias) at the end.
-constexpr int kRtM = 128, kRtN = 256, kRtK = 32, kRtStages = 2;
+constexpr int kRtM = 128, kRtN = 256, kRtK = 16, kRtStages = 4;
 constexpr int kRtABytes = kRtM * kRtK * 4, kRtBBytes = kRtN * kRtK * 4;  // 16 KB, 32 KB
 constexpr int kRtStageBytes = 2 * (kRtABytes + kRtBBytes);              // raw/hi and lo planes
 constexpr int kRtThreads = 192;
 constexpr int kRtSmBar = kRtStages * kRtStageBytes;
-constexpr int kRtSmAlloc = kRtSmBar + 8 * 8 + 16 + 1024;
+constexpr int kRtNumBars = 3 * kRtStages + 1;  // full, split, empty per stage; done
+constexpr int kRtSmAlloc = kRtSmBar + 8 * kRtNumBars + 16 + 1024;
 static_assert(kRtSmAlloc <= 232448, "router tile shared memory");
 
 struct RouterTcArgs {
-  CUtensorMap map_x;  // x [T][H] fp32, box {32, 128}, 128-byte swizzle
-  CUtensorMap map_w;  // W [E][H] fp32, box {32, 256}, 128-byte swizzle
+  CUtensorMap map_x;  // x [T][H] fp32, box {16, 128}, 64-byte swizzle
+  CUtensorMap map_w;  // W [E][H] fp32, box {16, 256}, 64-byte swizzle
   const float* bias;
   float* logits;
   int T, H, E;
@@ -1158,6 +1160,16 @@ __device__ __forceinline__ void mma_tf32(uint32_t tmem_d, uint64_t adesc, uint64
       " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"((int)acc));
 }
+// K-major, 64-byte swizzle: 8-row groups 512 bytes apart; the start may
+// advance by 32-byte K steps inside the 64-byte row.
+__device__ __forceinline__ uint64_t desc_sw64(uint32_t addr) {
+  uint64_t d = (uint64_t)((addr & 0x3FFFF) >> 4);
+  d |= (uint64_t)1 << 16;
+  d |= (uint64_t)(512 >> 4) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)4 << 61;
+  return d;
+}
 __device__ __forceinline__ float tf32_rna(float v) {
   uint32_t r;
   asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(v));
@@ -1174,8 +1186,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
   auto split = [&](int s) { return bar0 + 8 * (kRtStages + s); };     // hi/lo planes written
   auto empty = [&](int s) { return bar0 + 8 * (2 * kRtStages + s); }; // MMAs of the stage done
   const uint32_t done = bar0 + 8 * (3 * kRtStages);
-  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kRtSmBar + 8 * 8);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kRtSmBar + 8 * 8 + 4);
+  uint32_t* s_tmem = reinterpret_cast<uint32_t*>(sm + kRtSmBar + 8 * kRtNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(sm + kRtSmBar + 8 * kRtNumBars + 4);
   // stage s: A hi at 0, B hi at kRtABytes, A lo, B lo after them
   auto a_hi = [&](int s) { return s * kRtStageBytes; };
   auto b_hi = [&](int s) { return s * kRtStageBytes + kRtABytes; };
@@ -1226,8 +1238,8 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
         const uint32_t ph = (kb / kRtStages) & 1;
         if (!(ok = wait_bar(split(s), ph, abort_flag, a.status, w1))) break;
         tc_fence_after();
-        const uint64_t ah = desc_sw128(sbase + a_hi(s)), bh = desc_sw128(sbase + b_hi(s));
-        const uint64_t al = desc_sw128(sbase + a_lo(s)), bl = desc_sw128(sbase + b_lo(s));
+        const uint64_t ah = desc_sw64(sbase + a_hi(s)), bh = desc_sw64(sbase + b_hi(s));
+        const uint64_t al = desc_sw64(sbase + a_lo(s)), bl = desc_sw64(sbase + b_lo(s));
 #pragma unroll
         for (int k8 = 0; k8 < kRtK / 8; ++k8) {  // K = 8 tf32 = 32 bytes per MMA
           const uint64_t o = (uint64_t)(2 * k8);
@@ -1292,7 +1304,7 @@ __global__ void __launch_bounds__(kRtThreads, 1) router_tc_kernel(const __grid_c
   }
 }
 
-// 2-D fp32 tensor map: `inner` elements per row, `rows` rows, box {box_inner, box_rows}, 128-byte swizzle
+// 2-D fp32 tensor map: `inner` elements per row, `rows` rows, box {box_inner, box_rows}, 64-byte swizzle
 bool make_map_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_inner,
                   uint32_t box_rows) {
   auto fn = encode_fn();
@@ -1302,7 +1314,7 @@ bool make_map_f32(CUtensorMap* map, const void* base, uint64_t inner, uint64_t r
   const cuuint32_t box[2] = {box_inner, box_rows};
   const cuuint32_t estr[2] = {1, 1};
   return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
