@@ -203,13 +203,27 @@ __device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
+// the same test without suspending the thread (test_wait): the fast path of a wait
+__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
 constexpr int kEpilogueSleepNs = 64;  // the epilogue warps poll with a short back-off (they wait a super-block of MMAs)
 
 // Bounded wait for phase `parity`.  Gives up when another role has aborted,
 // or after about a second, recording a timeout; false = abort.
-// `spent` accumulates the cycles waited (per-role wait statistics).
+// `spent` accumulates the cycles waited (per-role wait statistics).  A phase
+// already complete costs one non-blocking test and no clock reads (the MMA
+// thread runs several such checks per stage).
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int* abort_flag, int* status,
                                          long long& spent, int sleep_ns = 0) {
+  if (mbar_test(bar, parity)) return true;
   const long long t0 = clock64();  // before the first try: try_wait itself may suspend the thread
   while (!mbar_try(bar, parity)) {
     if (sleep_ns) __nanosleep(sleep_ns);  // a waiter off the critical path leaves issue slots to the others
