@@ -214,7 +214,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-constexpr int kEpilogueSleepNs = 64;  // the epilogue warps poll with a short back-off (they wait a super-block of MMAs)
+constexpr int kEpilogueSleepNs = 0;  // no back-off between the epilogue's polls (a 64 ns one cost 1.7% of the step)
 
 // Bounded wait for phase `parity`.  Gives up when another role has aborted,
 // or after about a second, recording a timeout; false = abort.
