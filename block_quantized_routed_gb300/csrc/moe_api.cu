@@ -155,13 +155,23 @@ bool stack_takes_pipelined(const moe_layer_desc& d, int n_layers, int T, int sms
 
 void trace_record(cudaStream_t s) {
   if (!g_trace_events || g_trace_next >= g_trace_n) return;
-  cudaEvent_t ev = static_cast<cudaEvent_t>(g_trace_events[g_trace_next++]);
-  if (!ev || cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal) != cudaSuccess) {
+  cudaEvent_t ev = static_cast<cudaEvent_t>(g_trace_events[g_trace_next]);
+  // under stream capture the record must become an event-record node of the
+  // graph (the External flag); outside capture that flag is not valid and a
+  // plain record is the same operation
+  cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+  cudaError_t err = ev ? cudaStreamIsCapturing(s, &cs) : cudaErrorInvalidResourceHandle;
+  if (err == cudaSuccess)
+    err = cs == cudaStreamCaptureStatusActive ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                                              : cudaEventRecord(ev, s);
+  if (err != cudaSuccess) {
     // a profiling record must not turn into the next launch's error: consume
-    // the error and stop tracing
+    // the error and stop tracing (moe_trace_used counts only what was recorded)
     cudaGetLastError();
     g_trace_events = nullptr;
+    return;
   }
+  ++g_trace_next;
 }
 
 }  // namespace moe

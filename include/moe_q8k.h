@@ -361,9 +361,11 @@ const char* moe_status_string(int status);
  * created by the caller with timing enabled) on their stream, immediately
  * before and after each launch: two entries per single-launch decode layer
  * (moe_layer_forward with T <= 16 and T*top_k <= 256), four per expert-FFN
- * sequence otherwise (gate/up kernel, then down kernel).  Records use
- * cudaEventRecordExternal, so they also work inside stream capture.  When
- * the array is used up, recording stops.  events = NULL or n_events = 0
+ * sequence otherwise (gate/up kernel, then down kernel).  Under stream
+ * capture a record is made with cudaEventRecordExternal (an event-record
+ * node of the graph), outside capture with a plain cudaEventRecord.  When
+ * the array is used up, or a record fails (the error is consumed), recording
+ * stops.  events = NULL or n_events = 0
  * turns the hook off.  Returns MOE_OK or MOE_ERR_INVALID_ARG. */
 int moe_trace_events(void* const* events, int32_t n_events);
 

@@ -360,6 +360,55 @@ def test_layer_forward_is_deterministic(moe):
     np.testing.assert_array_equal(a.view(np.uint32), b.view(np.uint32))
 
 
+@pytest.mark.parametrize("T", [1, 40, 300])
+def test_trace_events_bracket_launches(moe, T):
+    """The launch-trace hook records its events eagerly (plain records) and
+    under stream capture (event-record nodes): two per single-launch decode
+    layer (T = 1), four per expert-FFN sequence (T = 40: GEMV kernels,
+    T = 300: tensor prefill); each bracket spans a launch that really ran
+    (positive duration, inside the caller's own bracket around the call)."""
+    fmt, route, H, I, E, k, S = FMT_Q4K, 0, 1024, 512, 32, 4, 1
+    ex = _experts_host(fmt, E + S, H, I, 5)
+    table = moe.expert_table([tuple(dev(m) for m in e) for e in ex])
+    desc = dict(H=H, I=I, E=E, top_k=k, n_shared=S, route=route, fmt=fmt, T_max=T)
+    layer = moe.MoeLayer(desc, table, dev(synth.router_weight(E, H, 5)))
+    x = dev(synth.activations(T, H, 5))
+    out = torch.empty_like(x)
+    want = 2 if moe.moe_layer_path(desc, T) == 0 else 4
+    events = [torch.cuda.Event(enable_timing=True) for _ in range(8)]
+    outer = [torch.cuda.Event(enable_timing=True) for _ in range(2)]
+    stream = torch.cuda.current_stream()
+
+    def spans_within(used):
+        torch.cuda.synchronize()
+        total = outer[0].elapsed_time(outer[1])
+        spans = [events[i].elapsed_time(events[i + 1]) for i in range(0, used, 2)]
+        assert all(0 < sp <= total for sp in spans), (spans, total)
+
+    # eager: the hook records on the launching stream
+    moe.moe_trace_events(events)
+    outer[0].record(stream)
+    layer.forward(x, out=out)
+    outer[1].record(stream)
+    used = moe.moe_trace_used()
+    moe.moe_trace_events(None)
+    assert used == want, used
+    spans_within(used)
+    # captured: the records become nodes of the graph, replayed with it
+    g = torch.cuda.CUDAGraph()
+    moe.moe_trace_events(events)
+    with torch.cuda.graph(g):
+        layer.forward(x, out=out)
+    used = moe.moe_trace_used()
+    moe.moe_trace_events(None)
+    assert used == want, used
+    outer[0].record(stream)
+    g.replay()
+    outer[1].record(stream)
+    spans_within(used)
+    assert moe.moe_get_status(layer.ws) == 0
+
+
 @pytest.mark.parametrize("T", [6, 512])
 def test_layer_forward_null_expert_is_not_mine(moe, T):
     fmt, H, I, E, k, S = FMT_Q4K, 512, 256, 8, 2, 1
