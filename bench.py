@@ -120,13 +120,40 @@ KERNEL_SOURCES = {"decode_fused_kernel": ["moe_decode_kernels.cuh"], "decode_sta
                   "gateup_kernel": ["moe_ffn.cu"]}
 
 
+def code_only(src):
+    """C/C++/CUDA source with its comments removed (string and character
+    literals kept as they are), so that an edit of a comment does not count
+    as a change of the code."""
+    out, i, n = [], 0, len(src)
+    while i < n:
+        c = src[i]
+        if c in "\"'":
+            j = i + 1
+            while j < n and src[j] != c:
+                j += 2 if src[j] == "\\" else 1
+            out.append(src[i:j + 1])
+            i = j + 1
+        elif src.startswith("//", i):
+            j = src.find("\n", i)
+            i = n if j < 0 else j
+        elif src.startswith("/*", i):
+            j = src.find("*/", i + 2)
+            i = n if j < 0 else j + 2
+            out.append(" ")
+        else:
+            out.append(c)
+            i += 1
+    return "\n".join(line.rstrip() for line in "".join(out).split("\n"))
+
+
 def kernel_source_hash(kernel):
-    """Hash of the sources a kernel is built from, to tell whether a profile still applies."""
+    """Hash of the code (comments removed) of the sources a kernel is built
+    from, to tell whether a profile still applies."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "block_quantized_routed_gb300", "csrc")
-    for f in KERNEL_SOURCES[kernel] + ["moe_device.cuh", "moe_internal.h"]:
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    h.update(open(os.path.join(ROOT, "include", "moe_q8k.h"), "rb").read())
+    paths = [os.path.join(csrc, f) for f in KERNEL_SOURCES[kernel] + ["moe_device.cuh", "moe_internal.h"]]
+    for path in paths + [os.path.join(ROOT, "include", "moe_q8k.h")]:
+        h.update(code_only(open(path, encoding="utf-8").read()).encode())
     return h.hexdigest()[:16]
 
 
@@ -484,31 +511,62 @@ def run_ours(args, wl, T):
     snap = snapshot_layers(moe, wl, T, desc, L, stacked, ws if stacked else None,
                            None if stacked else layers, check_layers, xin, out, ids_buf)
 
-    # CUDA graph of one step, with trace events around the expert launches
+    # CUDA graphs of one step, one per input rotation: each reads its rotation's
+    # inputs where they already sit in HBM (no copy inside the timed steps),
+    # with trace events around the expert launches
+    def body_rot(r):
+        def xin_r(l):
+            return out[l - 1] if l in links else xs[r][l]
+        if stacked:
+            rows_r = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=xin_r(l),
+                           residual=xin_r(l), out=out[l], ids_out=ids_buf[l]) for l in range(L)]
+            tab = moe.stack_pointer_table(rows_r, device=dev)
+            return lambda: moe.moe_stack_forward(desc, tab, T, ws)
+
+        def run_layers():
+            for l in range(L):
+                layers[l].forward(xin_r(l), residual=xin_r(l), out=out[l], ids_out=ids_buf[l])
+        return run_layers
+
     events = [torch.cuda.Event(enable_timing=True) for _ in range(4 * L)]
     use_graph = not args.no_graph
-    graph = None
-    moe.moe_trace_events(events)
-    n_launch0 = moe.moe_kernel_launch_count()
+    graphs = []
+    rot_bodies = []                      # keep each rotation's pointer table alive with its graph
+    launches_per_step = n_traced = 0
     if use_graph:
-        graph = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(graph):
-            body()
+        for r in range(R):
+            body_r = body_rot(r)
+            rot_bodies.append(body_r)
+            moe.moe_trace_events(events)
+            n_launch0 = moe.moe_kernel_launch_count()
+            g_ = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g_):
+                body_r()
+            if r == 0:
+                launches_per_step = moe.moe_kernel_launch_count() - n_launch0   # this library's kernels in one step
+                n_traced = moe.moe_trace_used()
+            moe.moe_trace_events(None)
+            graphs.append(g_)
     else:
+        moe.moe_trace_events(events)
+        n_launch0 = moe.moe_kernel_launch_count()
         body()
-    launches_per_step = moe.moe_kernel_launch_count() - n_launch0   # this library's kernels in one step
-    n_traced = moe.moe_trace_used()
-    moe.moe_trace_events(None)
+        launches_per_step = moe.moe_kernel_launch_count() - n_launch0
+        n_traced = moe.moe_trace_used()
+        moe.moe_trace_events(None)
 
     stream = torch.cuda.current_stream()
 
+    eager_traced = [n_traced]
+
     def step(i):
-        x_static.copy_(xs[i % R], non_blocking=True)
         if use_graph:
-            graph.replay()
+            graphs[i % R].replay()
         else:
+            x_static.copy_(xs[i % R], non_blocking=True)
             moe.moe_trace_events(events)
             body()
+            eager_traced[0] = moe.moe_trace_used()
             moe.moe_trace_events(None)
 
     W = max(3, args.warmup if args.warmup is not None else 20)
@@ -588,6 +646,9 @@ def run_ours(args, wl, T):
     last_r = (W + K - 1) % R
     peak, peak_src = measured_peaks()
     router_bytes = wl.E * wl.H * 4
+    traced = n_traced if use_graph else eager_traced[0]
+    if traced < (2 if stacked else 2 * L) or (not stacked and traced not in (2 * L, 4 * L)):
+        raise RuntimeError(f"the launch trace recorded {traced} events; the roofline needs every launch bracketed")
     if stacked:
         # one launch per step moves every layer's router weights and active experts' 3 matrices
         launch_ms = events[0].elapsed_time(events[1])
@@ -616,7 +677,7 @@ def run_ours(args, wl, T):
                     "down_kernel_tflops": dn_tf, "down_avg_launch_us": 1e3 * float(np.mean(dn_ms)),
                     "down_frac": dn_tf / tpeak}
     else:
-        per_layer = n_traced // L
+        per_layer = traced // L
         if per_layer == 2:
             fz_ms = [events[2 * l].elapsed_time(events[2 * l + 1]) for l in range(L)]
             alg = union[last_r] * exp_bytes + router_bytes
@@ -642,17 +703,61 @@ def run_ours(args, wl, T):
     # end to end through the public call with host buffers, every step: a
     # pinned H2D copy of the step's inputs, the C-ABI call(s) themselves
     # (argument checks and launches on the host, no graph replay), and a D2H
-    # copy of the outputs
+    # copy of the outputs.  Two input and two output buffers: a step's H2D
+    # copy (one copy stream) and the previous step's D2H copy (another) run
+    # while the step before computes; the steps themselves run in order on
+    # the compute stream, sharing one workspace.
     x_pinned = torch.from_numpy(x_host).pin_memory()
-    out_pinned = torch.empty((L, T, H), dtype=torch.float32).pin_memory()
+    out_pinned = [torch.empty((L, T, H), dtype=torch.float32).pin_memory() for _ in range(2)]
+    xb = [x_static, torch.empty_like(x_static)]
+    ob = [out, torch.empty_like(out)]
+    ib = [ids_buf, torch.empty_like(ids_buf)]
+
+    def make_body(j):
+        def xin_j(l):
+            return ob[j][l - 1] if l in links else xb[j][l]
+        if stacked:
+            if j == 0:
+                tab = stack
+            else:
+                rows_j = [dict(table=tables[l], w_router=routers[l], router_bias=biases[l], x=xin_j(l),
+                               residual=xin_j(l), out=ob[j][l], ids_out=ib[j][l]) for l in range(L)]
+                tab = moe.stack_pointer_table(rows_j, device=dev)
+            return lambda: moe.moe_stack_forward(desc, tab, T, ws)
+
+        def run_layers():
+            for l in range(L):
+                layers[l].forward(xin_j(l), residual=xin_j(l), out=ob[j][l], ids_out=ib[j][l])
+        return run_layers
+
+    bodies = [make_body(0), make_body(1)]
+    h2d_s, d2h_s = torch.cuda.Stream(device=dev), torch.cuda.Stream(device=dev)
+    h2d_done = [torch.cuda.Event() for _ in range(2)]
+    comp_done = [torch.cuda.Event() for _ in range(2)]
+    d2h_done = [torch.cuda.Event() for _ in range(2)]
     Ke = max(10, min(K, 2000))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     torch.cuda.synchronize()
     e0.record(stream)
+    h2d_s.wait_event(e0)
     for i in range(Ke):
-        x_static.copy_(x_pinned[i % R], non_blocking=True)
-        body()
-        out_pinned.copy_(out, non_blocking=True)
+        j = i % 2
+        with torch.cuda.stream(h2d_s):
+            if i >= 2:
+                h2d_s.wait_event(comp_done[j])        # step i - 2 has read xb[j]
+            xb[j].copy_(x_pinned[i % R], non_blocking=True)
+            h2d_done[j].record(h2d_s)
+        stream.wait_event(h2d_done[j])
+        if i >= 2:
+            stream.wait_event(d2h_done[j])            # the D2H of step i - 2 has read ob[j]
+        bodies[j]()
+        comp_done[j].record(stream)
+        with torch.cuda.stream(d2h_s):
+            d2h_s.wait_event(comp_done[j])
+            out_pinned[j].copy_(ob[j], non_blocking=True)
+            d2h_done[j].record(d2h_s)
+    stream.wait_event(d2h_done[(Ke - 1) % 2])
+    stream.wait_event(d2h_done[Ke % 2])
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
@@ -674,6 +779,9 @@ def run_ours(args, wl, T):
                          "plus %.0f MB of router weights (L2 129 MB)" % (
                              np.mean(union.sum(axis=1)) * exp_bytes / 1e6, L * wl.E * wl.H * 4 / 1e6),
                    "graph": use_graph, "rotations": R, "single_launch_stack": stacked,
+                   "timed_step": ("replay of one CUDA graph per input rotation; each graph reads its rotation's "
+                                  "inputs where they sit in HBM" if use_graph else
+                                  "device copy of the rotation's inputs, then the eager launches"),
                    "layer_inputs": (f"chained order (layers {links} read the previous layer's output)"
                                     if links else "independent"),
                    "path": ["decode_fused", "gemv", "tensor_prefill"][path]},
@@ -687,7 +795,8 @@ def run_ours(args, wl, T):
         "decode_phases_us": phases,
         "e2e": {"value": tokens_per_step / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
-                "how": "per step: pinned H2D of x, the C-ABI call through the binding (no graph), D2H of out"},
+                "how": "per step: pinned H2D of x, the C-ABI call through the binding (no graph), D2H of out; "
+                       "two buffers each way, copies on two copy streams overlapping the previous step"},
         "gpu_launches": launches_per_step * K,
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
